@@ -1,0 +1,238 @@
+/*
+ * CPU oracle for the block-sparse attention forward pass and the tile layout.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the plain, slow, obviously correct
+ * FP64 statement of what the GPU library computes.  Only the tests, the smoke
+ * check and the benchmark's CPU-baseline leg may load it.  It shares no code,
+ * header, table or helper with the CUDA library, and the library never calls it.
+ *
+ * Source of the definition: the FastVideo kernel page (hao-ai-lab/FastVideo
+ * commit 8503617, fastvideo-kernel/python).
+ *   - Commit adding the sm_121a tile-128 block-sparse forward: the operation
+ *     takes q, k, v, q2k_idx, q2k_num and variable_block_sizes and returns the
+ *     attention output; each query tile attends to the key tiles its
+ *     selection lists; tiles are 64 or 128 tokens.
+ *   - sm_121a hardening commit, "Kernel" items: a NaN softmax sum yields a NaN
+ *     output row (the test is l != 0, not l > 0); rows without keys stay 0;
+ *     keys past a tile's valid count are masked, so NaN/Inf stored in padding
+ *     rows of K or V cannot reach the output.
+ *   - Attn-QAT SM100 commit: "softmax statistics" are an output of the forward
+ *     pass (here: the natural-log log-sum-exp per query row).
+ *
+ * Readings where the page is silent (stated once here, used below):
+ *   - q2k_idx is [B,H,NT,max_kv], q2k_num is [B,H,NT], block_sizes is [NT];
+ *     the selection is per (batch, head, query tile).
+ *   - Selected key tiles must be distinct and in [0, NT); anything else is an
+ *     input error (return code), never silently accepted.
+ *   - A query row r of tile t with r >= block_sizes[t] is padding: output +0,
+ *     lse = -inf.  An empty key list gives output +0 and lse = -inf.
+ *   - m is the maximum score with NaN propagating; l = sum exp(s - m);
+ *     out = (sum exp(s - m) v) / l when l != 0, else 0; lse = m + log(l).
+ *   - Padding rows of Q, K and V are never read.
+ *
+ * The definition is computed literally: all scores of a row first, then the
+ * maximum, then the weights; no online softmax, no tiling, FP64 throughout,
+ * sums in index order.  Build with -ffp-contract=off so no multiply-add is
+ * fused and results are identical on every host.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_OK 0
+#define ORACLE_ERR_ARG -1
+#define ORACLE_ERR_INDEX -7
+#define ORACLE_ERR_NOMEM -8
+
+/* bf16 is the top half of an IEEE binary32, so the widening is exact. */
+static double bf16_to_double(uint16_t bits) {
+    uint32_t u = (uint32_t)bits << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+typedef struct {
+    const uint16_t *q, *k, *v;     /* bf16 bits, tile-major [B,H,NT*T,D] */
+    const int32_t *q2k_idx, *q2k_num, *block_sizes;
+    int B, H, NT, T, D, max_kv;
+    double scale;
+    const int64_t *units;          /* flat (b*H + h)*NT + t */
+    int64_t n_units;
+    double *out;                   /* [n_units, T, D] */
+    double *lse;                   /* [n_units, T] or NULL */
+    int64_t next;                  /* shared work cursor */
+    pthread_mutex_t lock;
+    int status;
+} job_t;
+
+/* One query tile: every valid row r < n_t gets the softmax over the valid rows
+ * of its selected key tiles. */
+static int one_query_tile(job_t *J, int64_t unit, int64_t slot, double *scores, double *qrow,
+                          double *acc) {
+    const int T = J->T, D = J->D, NT = J->NT;
+    const int64_t Sp = (int64_t)NT * T;
+    const int t = (int)(unit % NT);
+    const int64_t bh = unit / NT;
+    const int n_t = J->block_sizes[t];
+    const int K = J->q2k_num[unit];
+    const int32_t *sel = J->q2k_idx + unit * J->max_kv;
+    const uint16_t *Qp = J->q + bh * Sp * D;
+    const uint16_t *Kp = J->k + bh * Sp * D;
+    const uint16_t *Vp = J->v + bh * Sp * D;
+    double *O = J->out + slot * (int64_t)T * D;
+    double *L = J->lse ? J->lse + slot * (int64_t)T : NULL;
+
+    for (int r = 0; r < T; ++r) {
+        for (int d = 0; d < D; ++d) O[(int64_t)r * D + d] = 0.0;
+        if (L) L[r] = -INFINITY;
+        if (r >= n_t) continue;                       /* padding query row */
+
+        for (int d = 0; d < D; ++d) qrow[d] = bf16_to_double(Qp[((int64_t)t * T + r) * D + d]);
+
+        /* 1. scores over the key list, in list order */
+        int64_t n = 0;
+        for (int i = 0; i < K; ++i) {
+            const int j = sel[i];
+            for (int c = 0; c < J->block_sizes[j]; ++c) {
+                const uint16_t *krow = Kp + ((int64_t)j * T + c) * D;
+                double dot = 0.0;
+                for (int d = 0; d < D; ++d) dot += qrow[d] * bf16_to_double(krow[d]);
+                scores[n++] = J->scale * dot;
+            }
+        }
+        if (n == 0) continue;                         /* no keys: row stays 0 */
+
+        /* 2. maximum, NaN propagating */
+        double m = -INFINITY;
+        for (int64_t e = 0; e < n; ++e) {
+            if (isnan(scores[e]) || isnan(m)) m = NAN;
+            else if (scores[e] > m) m = scores[e];
+        }
+
+        /* 3. weights, their sum, and the weighted sum of values */
+        double l = 0.0;
+        for (int d = 0; d < D; ++d) acc[d] = 0.0;
+        int64_t e = 0;
+        for (int i = 0; i < K; ++i) {
+            const int j = sel[i];
+            for (int c = 0; c < J->block_sizes[j]; ++c, ++e) {
+                const double w = exp(scores[e] - m);
+                const uint16_t *vrow = Vp + ((int64_t)j * T + c) * D;
+                l += w;
+                for (int d = 0; d < D; ++d) acc[d] += w * bf16_to_double(vrow[d]);
+            }
+        }
+        for (int d = 0; d < D; ++d) O[(int64_t)r * D + d] = (l != 0.0) ? acc[d] / l : 0.0;
+        if (L) L[r] = m + log(l);
+    }
+    return ORACLE_OK;
+}
+
+static void *worker(void *arg) {
+    job_t *J = (job_t *)arg;
+    int64_t max_keys = (int64_t)J->max_kv * J->T;
+    double *scores = (double *)malloc(sizeof(double) * (size_t)(max_keys > 0 ? max_keys : 1));
+    double *qrow = (double *)malloc(sizeof(double) * (size_t)J->D);
+    double *acc = (double *)malloc(sizeof(double) * (size_t)J->D);
+    if (!scores || !qrow || !acc) {
+        pthread_mutex_lock(&J->lock);
+        J->status = ORACLE_ERR_NOMEM;
+        pthread_mutex_unlock(&J->lock);
+    } else {
+        for (;;) {
+            pthread_mutex_lock(&J->lock);
+            int64_t slot = J->next++;
+            pthread_mutex_unlock(&J->lock);
+            if (slot >= J->n_units) break;
+            one_query_tile(J, J->units[slot], slot, scores, qrow, acc);
+        }
+    }
+    free(scores);
+    free(qrow);
+    free(acc);
+    return NULL;
+}
+
+/* Checks the selection of every requested unit: counts in [0, max_kv], indices
+ * in [0, NT) and pairwise distinct. */
+static int check_units(const job_t *J) {
+    const int64_t total = (int64_t)J->B * J->H * J->NT;
+    for (int t = 0; t < J->NT; ++t)
+        if (J->block_sizes[t] < 0 || J->block_sizes[t] > J->T) return ORACLE_ERR_ARG;
+    for (int64_t s = 0; s < J->n_units; ++s) {
+        const int64_t u = J->units[s];
+        if (u < 0 || u >= total) return ORACLE_ERR_ARG;
+        const int K = J->q2k_num[u];
+        if (K < 0 || K > J->max_kv) return ORACLE_ERR_INDEX;
+        const int32_t *sel = J->q2k_idx + u * J->max_kv;
+        for (int i = 0; i < K; ++i) {
+            if (sel[i] < 0 || sel[i] >= J->NT) return ORACLE_ERR_INDEX;
+            for (int i2 = 0; i2 < i; ++i2)
+                if (sel[i2] == sel[i]) return ORACLE_ERR_INDEX;
+        }
+    }
+    return ORACLE_OK;
+}
+
+/* Block-sparse attention forward, FP64, for the listed query tiles.
+ *   q, k, v     bf16 bit patterns, tile-major [B, H, NT*T, D]
+ *   units       flat query-tile ids (b*H + h)*NT + t, n_units of them
+ *   out         [n_units, T, D] doubles; lse [n_units, T] doubles or NULL
+ * Returns 0, or a negative error for bad arguments / bad selections. */
+int oracle_block_sparse_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                            const int32_t *q2k_idx, const int32_t *q2k_num,
+                            const int32_t *block_sizes, int B, int H, int NT, int T, int D,
+                            int max_kv, double scale, const int64_t *units, int64_t n_units,
+                            double *out, double *lse, int nthreads) {
+    if (!q || !k || !v || !q2k_idx || !q2k_num || !block_sizes || !units || !out) return ORACLE_ERR_ARG;
+    if (B <= 0 || H <= 0 || NT <= 0 || T <= 0 || D <= 0 || max_kv < 0 || n_units < 0) return ORACLE_ERR_ARG;
+    job_t J;
+    memset(&J, 0, sizeof J);
+    J.q = q; J.k = k; J.v = v;
+    J.q2k_idx = q2k_idx; J.q2k_num = q2k_num; J.block_sizes = block_sizes;
+    J.B = B; J.H = H; J.NT = NT; J.T = T; J.D = D; J.max_kv = max_kv;
+    J.scale = scale; J.units = units; J.n_units = n_units; J.out = out; J.lse = lse;
+    int rc = check_units(&J);
+    if (rc != ORACLE_OK) return rc;
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 256) nthreads = 256;
+    pthread_mutex_init(&J.lock, NULL);
+    pthread_t th[256];
+    int started = 0;
+    for (int i = 0; i < nthreads; ++i) {
+        if (pthread_create(&th[i], NULL, worker, &J) != 0) break;
+        ++started;
+    }
+    if (started == 0) worker(&J);
+    for (int i = 0; i < started; ++i) pthread_join(th[i], NULL);
+    pthread_mutex_destroy(&J.lock);
+    return J.status;
+}
+
+/* Tile layout: dst[b, h, row, :] = src[b, row_to_token[row], h, :] for every
+ * tile-major row; a row whose map entry is -1 is padding and is written as +0.
+ *   src bf16 bits [B, S, H, D]; dst bf16 bits [B, H, NT*T, D].
+ * Source: the fused tile_to_bhsd commit on the same page (one pass that
+ * scatters token-major Q/K/V into tile-major BHSD). */
+int oracle_tile_layout(const uint16_t *src, const int32_t *row_to_token, uint16_t *dst, int B, int S,
+                       int H, int D, int NT, int T) {
+    if (!src || !row_to_token || !dst || B <= 0 || S < 0 || H <= 0 || D <= 0 || NT <= 0 || T <= 0)
+        return ORACLE_ERR_ARG;
+    const int64_t Sp = (int64_t)NT * T;
+    for (int64_t row = 0; row < Sp; ++row) {
+        const int32_t s = row_to_token[row];
+        if (s < -1 || s >= S) return ORACLE_ERR_INDEX;
+    }
+    for (int b = 0; b < B; ++b)
+        for (int h = 0; h < H; ++h)
+            for (int64_t row = 0; row < Sp; ++row) {
+                const int32_t s = row_to_token[row];
+                uint16_t *o = dst + (((int64_t)b * H + h) * Sp + row) * D;
+                for (int d = 0; d < D; ++d)
+                    o[d] = (s < 0) ? (uint16_t)0 : src[(((int64_t)b * S + s) * H + h) * D + d];
+            }
+    return ORACLE_OK;
+}
