@@ -1,0 +1,202 @@
+"""GB300 (sm_103a) block-sparse attention forward: Python binding.
+
+A thin ``ctypes`` layer over the C ABI in ``include/vsa.h`` (library
+``_build/libvsa.so``).  It only marshals arguments -- tensor pointers, sizes,
+the current CUDA stream -- every step of the computation runs in the
+library's CUDA kernels.  PyTorch provides device memory and streams.  There
+is no CPU fallback: if the library is missing, importing the binding raises.
+
+The functions named ``vsa_*`` mirror the C entry points one to one.  The
+helpers ``block_sparse_attention`` and ``tile_layout`` allocate outputs and
+the workspace with torch and call them.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libvsa.so")
+
+VSA_OK, VSA_ERR_ARG, VSA_ERR_ALIGN, VSA_ERR_LIMITS, VSA_ERR_ARCH = 0, -1, -2, -3, -4
+VSA_ERR_CUDA, VSA_ERR_TIMEOUT, VSA_ERR_INDEX, VSA_ERR_WORKSPACE = -5, -6, -7, -8
+VSA_KERNEL_NONE, VSA_KERNEL_ATTN_TCGEN05, VSA_KERNEL_LAYOUT, VSA_KERNEL_VALIDATE = 0, 1, 2, 3
+VSA_MAX_BATCH_HEADS, VSA_MAX_TILES = 65535, 8192
+
+
+class VsaDims(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("H", ctypes.c_int32), ("num_tiles", ctypes.c_int32),
+                ("tile", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("max_kv", ctypes.c_int32),
+                ("scale", ctypes.c_float)]
+
+
+class VsaRoute(ctypes.Structure):
+    _fields_ = [("kernel", ctypes.c_int32), ("tile", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("grid", ctypes.c_int32), ("block", ctypes.c_int32), ("stages", ctypes.c_int32),
+                ("work_items", ctypes.c_int64), ("sort_bins", ctypes.c_int32),
+                ("smem_bytes", ctypes.c_int32)]
+
+    def as_dict(self):
+        return {k: getattr(self, k) for k, _ in self._fields_}
+
+
+class VsaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {vsa_status_string(status)} ({status})")
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"libvsa.so is not built ({LIB_PATH}); run __graft_entry__.build() "
+                           "or python -m block_sparse_attention_gathered_gb300.build")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+    dims_p = ctypes.POINTER(VsaDims)
+    sig = {
+        "vsa_block_sparse_workspace_size": ([dims_p], sz),
+        "vsa_block_sparse_fwd": ([P, P, P, P, P, P, P, P, dims_p, P, sz, P], i32),
+        "vsa_tile_layout": ([P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, P], i32),
+        "vsa_validate_indices": ([P, P, P, dims_p, P, P], i32),
+        "vsa_check_device_status": ([P], i32),
+        "vsa_last_route": ([ctypes.POINTER(VsaRoute)], i32),
+        "vsa_status_string": ([i32], ctypes.c_char_p),
+        "vsa_version": ([], i32),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes, fn.restype = args, res
+    return lib
+
+
+_lib = _load()
+EXPORTED = ("vsa_block_sparse_workspace_size", "vsa_block_sparse_fwd", "vsa_tile_layout",
+            "vsa_validate_indices", "vsa_check_device_status", "vsa_last_route",
+            "vsa_status_string", "vsa_version")
+
+
+def library() -> ctypes.CDLL:
+    return _lib
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def make_dims(B, H, num_tiles, tile, head_dim, max_kv, scale=None) -> VsaDims:
+    return VsaDims(int(B), int(H), int(num_tiles), int(tile), int(head_dim), int(max_kv),
+                   float(scale) if scale is not None else 0.0)
+
+
+def vsa_status_string(status: int) -> str:
+    return _lib.vsa_status_string(int(status)).decode()
+
+
+def vsa_version() -> int:
+    return int(_lib.vsa_version())
+
+
+def vsa_block_sparse_workspace_size(dims: VsaDims) -> int:
+    return int(_lib.vsa_block_sparse_workspace_size(ctypes.byref(dims)))
+
+
+def vsa_block_sparse_fwd(q, k, v, q2k_idx, q2k_num, block_sizes, out, lse, dims: VsaDims,
+                         workspace: torch.Tensor, stream=None) -> None:
+    """Calls the C entry point on device tensors; raises VsaError on a status."""
+    st = _lib.vsa_block_sparse_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(q2k_idx), _ptr(q2k_num),
+                                   _ptr(block_sizes), _ptr(out), _ptr(lse), ctypes.byref(dims),
+                                   _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                   _stream(stream))
+    if st != VSA_OK:
+        raise VsaError(st, "vsa_block_sparse_fwd")
+
+
+def vsa_tile_layout(q_tok, k_tok, v_tok, q_tile, k_tile, v_tile, row_to_token, B, S, H, D,
+                    num_tiles, tile, stream=None) -> None:
+    st = _lib.vsa_tile_layout(_ptr(q_tok), _ptr(k_tok), _ptr(v_tok), _ptr(q_tile), _ptr(k_tile),
+                              _ptr(v_tile), _ptr(row_to_token), int(B), int(S), int(H), int(D),
+                              int(num_tiles), int(tile), _stream(stream))
+    if st != VSA_OK:
+        raise VsaError(st, "vsa_tile_layout")
+
+
+def vsa_validate_indices(q2k_idx, q2k_num, block_sizes, dims: VsaDims, dev_status: torch.Tensor,
+                         stream=None) -> None:
+    st = _lib.vsa_validate_indices(_ptr(q2k_idx), _ptr(q2k_num), _ptr(block_sizes),
+                                   ctypes.byref(dims), _ptr(dev_status), _stream(stream))
+    if st != VSA_OK:
+        raise VsaError(st, "vsa_validate_indices")
+
+
+def vsa_check_device_status(stream=None) -> int:
+    return int(_lib.vsa_check_device_status(_stream(stream)))
+
+
+def vsa_last_route() -> dict:
+    r = VsaRoute()
+    st = _lib.vsa_last_route(ctypes.byref(r))
+    if st != VSA_OK:
+        raise VsaError(st, "vsa_last_route")
+    return r.as_dict()
+
+
+# ------------------------------------------------------------------ helpers
+def _check_bf16_cuda(*ts):
+    for t in ts:
+        if t is None:
+            continue
+        if not t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError("expected contiguous bf16 CUDA tensors")
+
+
+def block_sparse_attention(q, k, v, q2k_idx, q2k_num, block_sizes, tile: int,
+                           scale: Optional[float] = None, want_lse: bool = False,
+                           out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                           stream=None):
+    """Block-sparse attention forward on tile-major bf16 ``[B, H, NT*tile, D]``.
+
+    Returns ``out`` (bf16, same shape) or ``(out, lse)`` with ``lse`` fp32
+    ``[B, H, NT*tile]`` when ``want_lse``."""
+    _check_bf16_cuda(q, k, v)
+    B, H, Sp, D = q.shape
+    if Sp % tile:
+        raise ValueError("sequence length is not a multiple of the tile")
+    NT = Sp // tile
+    q2k_idx = q2k_idx.contiguous()
+    dims = make_dims(B, H, NT, tile, D, q2k_idx.shape[-1], scale)
+    if out is None:
+        out = torch.empty_like(q)
+    lse = torch.empty((B, H, Sp), dtype=torch.float32, device=q.device) if want_lse else None
+    need = vsa_block_sparse_workspace_size(dims)
+    if need == 0:
+        raise VsaError(VSA_ERR_ARG if B * H <= VSA_MAX_BATCH_HEADS and NT <= VSA_MAX_TILES
+                       else VSA_ERR_LIMITS, "vsa_block_sparse_workspace_size")
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    vsa_block_sparse_fwd(q, k, v, q2k_idx, q2k_num.contiguous(), block_sizes.contiguous(), out, lse,
+                         dims, workspace, stream)
+    return (out, lse) if want_lse else out
+
+
+def tile_layout(q_tok, k_tok, v_tok, row_to_token, num_tiles: int, tile: int, stream=None):
+    """Token-major bf16 ``[B, S, H, D]`` (any of the three may be None) ->
+    tile-major ``[B, H, num_tiles*tile, D]``; padding rows are +0."""
+    src = [t for t in (q_tok, k_tok, v_tok)]
+    ref = next(t for t in src if t is not None)
+    _check_bf16_cuda(*src)
+    B, S, H, D = ref.shape
+    dst = [None if t is None else torch.empty((B, H, num_tiles * tile, D), dtype=torch.bfloat16,
+                                              device=ref.device) for t in src]
+    vsa_tile_layout(src[0], src[1], src[2], dst[0], dst[1], dst[2], row_to_token.contiguous(),
+                    B, S, H, D, num_tiles, tile, stream)
+    return tuple(dst)

@@ -1,0 +1,432 @@
+// Host side of the C ABI declared in include/vsa.h: argument and limit checks,
+// the per-device cache, TMA descriptor encoding, the on-device work ordering
+// (host scheduler step), the opt-in selection check and the device status
+// word.
+//
+// Limits and fail-closed behaviour follow the sm_121a hardening commit on the
+// FastVideo kernel page (hao-ai-lab/FastVideo commit 8503617): batch*heads <=
+// 65535 and rows < 2^31 are checked before any launch; a device the kernels
+// were not built for is refused with an error instead of returning
+// uninitialised output; the SM count and the shared-memory opt-in are cached
+// per device in atomics.
+#include <atomic>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "vsa.h"
+#include "vsa_internal.h"
+
+namespace vsa {
+namespace {
+
+__device__ int32_t g_device_status;  // bits kFlag*; read and cleared by vsa_check_device_status
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceCache {
+    std::atomic<int> state{0};  // 0 unknown, 1 supported sm_103, -1 unsupported
+    std::atomic<int> sm_count{0};
+    std::atomic<unsigned> attn_prepared{0};  // bit per (tile, head_dim) variant
+    std::atomic<int32_t *> status_ptr{nullptr};
+};
+DeviceCache g_dev[kMaxDevices];
+
+thread_local vsa_route t_route{};
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
+                                  CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                  CUtensorMapFloatOOBfill);
+std::once_flag g_encode_once;
+EncodeTiledFn g_encode = nullptr;
+
+EncodeTiledFn encode_fn() {
+    std::call_once(g_encode_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    });
+    return g_encode;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Current device, checked to be an sm_103 part; fills its cache entry.
+vsa_status current_device(int *dev_out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return VSA_ERR_CUDA;
+    }
+    if (dev < 0 || dev >= kMaxDevices) return VSA_ERR_ARCH;
+    DeviceCache &c = g_dev[dev];
+    int st = c.state.load(std::memory_order_acquire);
+    if (st == 0) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return VSA_ERR_CUDA;
+        }
+        st = (major == 10 && minor == 3) ? 1 : -1;
+        if (st == 1) {
+            int32_t *p = nullptr;
+            if (cudaGetSymbolAddress(reinterpret_cast<void **>(&p), g_device_status) != cudaSuccess) {
+                cudaGetLastError();
+                return VSA_ERR_CUDA;
+            }
+            c.status_ptr.store(p, std::memory_order_release);
+            c.sm_count.store(sms, std::memory_order_release);
+        }
+        c.state.store(st, std::memory_order_release);
+    }
+    if (st != 1) return VSA_ERR_ARCH;
+    *dev_out = dev;
+    return VSA_OK;
+}
+
+vsa_status check_dims(const vsa_dims *d) {
+    if (!d) return VSA_ERR_ARG;
+    if (d->B <= 0 || d->H <= 0 || d->num_tiles <= 0 || d->max_kv < 0) return VSA_ERR_ARG;
+    if (d->tile != 64 && d->tile != 128) return VSA_ERR_ARG;
+    if (d->head_dim != 64 && d->head_dim != 128) return VSA_ERR_ARG;
+    if (!std::isfinite(d->scale)) return VSA_ERR_ARG;
+    if ((int64_t)d->B * d->H > VSA_MAX_BATCH_HEADS) return VSA_ERR_LIMITS;
+    if (d->num_tiles > VSA_MAX_TILES) return VSA_ERR_LIMITS;
+    const int64_t rows = (int64_t)d->B * d->H * d->num_tiles * d->tile;
+    if (rows + kItemRows >= (int64_t(1) << VSA_MAX_ROWS_LOG2)) return VSA_ERR_LIMITS;
+    if ((int64_t)d->B * d->H * d->num_tiles * (int64_t)d->max_kv >= (int64_t(1) << 31)) return VSA_ERR_LIMITS;
+    return VSA_OK;
+}
+
+int64_t items_per_seq(const vsa_dims *d) { return ((int64_t)d->num_tiles * d->tile + kItemRows - 1) / kItemRows; }
+
+constexpr size_t kWsHeader = 256;  // work counter, padded
+
+size_t workspace_bytes_for(const vsa_dims *d) {
+    const int64_t n_items = (int64_t)d->B * d->H * items_per_seq(d);
+    return kWsHeader + (size_t)n_items * sizeof(int32_t);
+}
+
+vsa_status encode_rows_map(CUtensorMap *m, const void *ptr, int64_t rows, int D, int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return VSA_ERR_CUDA;
+    cuuint64_t gdim[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+    cuuint64_t gstride[1] = {(cuuint64_t)D * 2};
+    cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1u, 1u};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), gdim, gstride, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? VSA_OK : VSA_ERR_CUDA;
+}
+
+// ------------------------------------------------------------------ schedule
+// Orders the 256-row work items by their total number of selected key tiles,
+// largest first (a counting sort into `bins` buckets), and resets the work
+// counter the attention kernel's CTAs draw from.  One CTA; equal keys land in
+// any order, which does not change any output (items are independent).
+constexpr int kSchedThreads = 1024;
+
+__global__ void __launch_bounds__(kSchedThreads)
+    schedule_kernel(const int32_t *__restrict__ q2k_num, int NT, int T, int max_kv, int G, int n_items, int bins,
+                    int32_t *__restrict__ order, int32_t *__restrict__ counter) {
+    extern __shared__ int32_t sh[];
+    int32_t *hist = sh;          // [bins], indexed by descending rank
+    int32_t *cursor = sh + bins;  // [bins]
+    __shared__ int32_t warp_tot[kSchedThreads / 32];
+    const int tid = threadIdx.x;
+    const int per_item = (T == 128) ? 2 : 4;
+    const int64_t wmax = (int64_t)per_item * (max_kv > 0 ? max_kv : 1);
+    for (int i = tid; i < bins; i += kSchedThreads) hist[i] = 0;
+    __syncthreads();
+    auto rank_of = [&](int item) -> int {
+        const int bh = item / G, g = item - (item / G) * G;
+        int64_t w = 0;
+        for (int k = 0; k < per_item; ++k) {
+            const int t = g * per_item + k;
+            if (t >= NT) break;
+            int n = __ldg(q2k_num + (int64_t)bh * NT + t);
+            n = n < 0 ? 0 : (n > max_kv ? max_kv : n);
+            w += n;
+        }
+        const int bin = (int)(w * (bins - 1) / wmax);
+        return bins - 1 - bin;  // larger weight -> smaller rank
+    };
+    for (int i = tid; i < n_items; i += kSchedThreads) atomicAdd(&hist[rank_of(i)], 1);
+    __syncthreads();
+    // exclusive scan of hist over ranks: each thread owns a contiguous run
+    const int per = (bins + kSchedThreads - 1) / kSchedThreads;
+    const int lo = tid * per, hi = min(bins, lo + per);
+    int32_t run = 0;
+    for (int i = lo; i < hi; ++i) run += hist[i];
+    int32_t incl = run;
+    const int lane = tid & 31, wid = tid >> 5;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) warp_tot[wid] = incl;
+    __syncthreads();
+    if (wid == 0) {
+        int32_t x = warp_tot[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int32_t y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        warp_tot[lane] = x;  // inclusive over warps
+    }
+    __syncthreads();
+    int32_t pos = incl - run + (wid > 0 ? warp_tot[wid - 1] : 0);
+    for (int i = lo; i < hi; ++i) {
+        cursor[i] = pos;
+        pos += hist[i];
+    }
+    __syncthreads();
+    for (int i = tid; i < n_items; i += kSchedThreads) order[atomicAdd(&cursor[rank_of(i)], 1)] = i;
+    if (tid == 0) *counter = 0;
+}
+
+// ------------------------------------------------------------------ validate
+__global__ void validate_kernel(const int32_t *__restrict__ q2k_idx, const int32_t *__restrict__ q2k_num,
+                                const int32_t *__restrict__ block_sizes, int64_t n_rows, int NT, int T, int max_kv,
+                                int32_t *dev_status) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    bool bad = false;
+    if (i < NT) {
+        const int n = block_sizes[i];
+        bad |= (n < 0 || n > T);
+    }
+    if (i < n_rows) {
+        const int K = q2k_num[i];
+        if (K < 0 || K > max_kv) {
+            bad = true;
+        } else {
+            const int32_t *sel = q2k_idx + i * max_kv;
+            for (int a = 0; a < K && !bad; ++a) {
+                const int j = sel[a];
+                if (j < 0 || j >= NT) bad = true;
+                for (int b = 0; b < a && !bad; ++b)
+                    if (sel[b] == j) bad = true;
+            }
+        }
+    }
+    if (bad) atomicExch(dev_status, (int32_t)VSA_ERR_INDEX);
+}
+
+}  // namespace
+}  // namespace vsa
+
+using namespace vsa;
+
+extern "C" {
+
+int32_t vsa_version(void) { return 1000; }
+
+const char *vsa_status_string(vsa_status s) {
+    switch (s) {
+        case VSA_OK: return "ok";
+        case VSA_ERR_ARG: return "invalid argument";
+        case VSA_ERR_ALIGN: return "pointer not 16-byte aligned";
+        case VSA_ERR_LIMITS: return "launch limit exceeded";
+        case VSA_ERR_ARCH: return "device is not sm_103 (GB300)";
+        case VSA_ERR_CUDA: return "CUDA runtime error";
+        case VSA_ERR_TIMEOUT: return "device-side wait timed out";
+        case VSA_ERR_INDEX: return "invalid selection index, count or row map";
+        case VSA_ERR_WORKSPACE: return "workspace missing or too small";
+    }
+    return "unknown status";
+}
+
+size_t vsa_block_sparse_workspace_size(const vsa_dims *dims) {
+    if (check_dims(dims) != VSA_OK) return 0;
+    return workspace_bytes_for(dims);
+}
+
+vsa_status vsa_block_sparse_fwd(const void *q, const void *k, const void *v, const int32_t *q2k_idx,
+                                const int32_t *q2k_num, const int32_t *block_sizes, void *out, float *lse,
+                                const vsa_dims *dims, void *workspace, size_t workspace_bytes,
+                                vsa_stream_t stream) {
+    vsa_status st = check_dims(dims);
+    if (st != VSA_OK) return st;
+    if (!q || !k || !v || !q2k_num || !block_sizes || !out || (!q2k_idx && dims->max_kv > 0))
+        return VSA_ERR_ARG;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) || !aligned(q2k_num, 4) ||
+        !aligned(block_sizes, 4) || (q2k_idx && !aligned(q2k_idx, 4)) || (lse && !aligned(lse, 4)))
+        return VSA_ERR_ALIGN;
+    const size_t need = workspace_bytes_for(dims);
+    if (!workspace || workspace_bytes < need) return VSA_ERR_WORKSPACE;
+    if (!aligned(workspace, 16)) return VSA_ERR_ALIGN;
+    int dev = 0;
+    if ((st = current_device(&dev)) != VSA_OK) return st;
+    DeviceCache &dc = g_dev[dev];
+
+    const int T = dims->tile, D = dims->head_dim, NT = dims->num_tiles;
+    const unsigned variant_bit = 1u << ((T == 128 ? 2 : 0) + (D == 128 ? 1 : 0));
+    if (!(dc.attn_prepared.load(std::memory_order_acquire) & variant_bit)) {
+        if (attn_prepare(T, D, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return VSA_ERR_CUDA;
+        }
+        dc.attn_prepared.fetch_or(variant_bit, std::memory_order_acq_rel);
+    }
+
+    const int64_t Sp = (int64_t)NT * T;
+    const int64_t rows = (int64_t)dims->B * dims->H * Sp;
+    CUtensorMap tm_q, tm_k, tm_v;
+    if ((st = encode_rows_map(&tm_q, q, rows, D, kUnitRows)) != VSA_OK) return st;
+    if ((st = encode_rows_map(&tm_k, k, rows, D, T)) != VSA_OK) return st;
+    if ((st = encode_rows_map(&tm_v, v, rows, D, T)) != VSA_OK) return st;
+
+    const int G = (int)items_per_seq(dims);
+    const int n_items = (int)((int64_t)dims->B * dims->H * G);
+    const int per_item = (T == 128) ? 2 : 4;
+    const int64_t wmax = (int64_t)per_item * (dims->max_kv > 0 ? dims->max_kv : 1);
+    const int bins = (int)(wmax + 1 < 2048 ? wmax + 1 : 2048);
+    int32_t *counter = reinterpret_cast<int32_t *>(workspace);
+    int32_t *order = reinterpret_cast<int32_t *>(reinterpret_cast<char *>(workspace) + kWsHeader);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+    schedule_kernel<<<1, kSchedThreads, 2 * bins * sizeof(int32_t), s>>>(q2k_num, NT, T, dims->max_kv, G, n_items,
+                                                                        bins, order, counter);
+    if (cudaGetLastError() != cudaSuccess) return VSA_ERR_CUDA;
+
+    AttnParams p;
+    p.q2k_idx = q2k_idx;
+    p.q2k_num = q2k_num;
+    p.block_sizes = block_sizes;
+    p.out = out;
+    p.lse = lse;
+    p.order = order;
+    p.work_counter = counter;
+    p.status = dc.status_ptr.load(std::memory_order_acquire);
+    p.NT = NT;
+    p.max_kv = dims->max_kv;
+    p.G = G;
+    p.bm_words = (NT + 31) / 32;
+    p.n_items = n_items;
+    p.Sp = Sp;
+    const float scale = dims->scale > 0.f ? dims->scale : 1.0f / std::sqrt((float)D);
+    p.scale_log2 = scale * 1.4426950408889634f;
+    const int sms = dc.sm_count.load(std::memory_order_acquire);
+    const int grid = n_items < sms ? n_items : sms;
+    if (launch_attn(T, D, tm_q, tm_k, tm_v, p, grid, s) != cudaSuccess) return VSA_ERR_CUDA;
+
+    const AttnLaunchInfo info = attn_launch_info(T, D, p.bm_words);
+    t_route.kernel = VSA_KERNEL_ATTN_TCGEN05;
+    t_route.tile = T;
+    t_route.head_dim = D;
+    t_route.grid = grid;
+    t_route.block = kAttnThreads;
+    t_route.stages = info.stages;
+    t_route.work_items = n_items;
+    t_route.sort_bins = bins;
+    t_route.smem_bytes = info.smem_bytes;
+    return VSA_OK;
+}
+
+vsa_status vsa_tile_layout(const void *q_tok, const void *k_tok, const void *v_tok, void *q_tile, void *k_tile,
+                           void *v_tile, const int32_t *row_to_token, int32_t B, int32_t S, int32_t H, int32_t D,
+                           int32_t num_tiles, int32_t tile, vsa_stream_t stream) {
+    if (!row_to_token || B <= 0 || S < 0 || H <= 0 || D <= 0 || (D % 8) != 0 || num_tiles <= 0 || tile <= 0)
+        return VSA_ERR_ARG;
+    const void *src[3] = {q_tok, k_tok, v_tok};
+    void *dst[3] = {q_tile, k_tile, v_tile};
+    LayoutParams p;
+    p.n_tensors = 0;
+    for (int i = 0; i < 3; ++i) {
+        if ((src[i] == nullptr) != (dst[i] == nullptr)) return VSA_ERR_ARG;
+        if (!src[i]) continue;
+        if (!aligned(src[i], 16) || !aligned(dst[i], 16)) return VSA_ERR_ALIGN;
+        p.src[p.n_tensors] = src[i];
+        p.dst[p.n_tensors] = dst[i];
+        ++p.n_tensors;
+    }
+    for (int i = p.n_tensors; i < 3; ++i) {
+        p.src[i] = nullptr;
+        p.dst[i] = nullptr;
+    }
+    if (p.n_tensors == 0) return VSA_ERR_ARG;
+    if (!aligned(row_to_token, 4)) return VSA_ERR_ALIGN;
+    if (B > 65535) return VSA_ERR_LIMITS;
+    if ((int64_t)B * H > VSA_MAX_BATCH_HEADS) return VSA_ERR_LIMITS;
+    const int64_t Sp = (int64_t)num_tiles * tile;
+    if ((int64_t)B * H * Sp >= (int64_t(1) << VSA_MAX_ROWS_LOG2) || (int64_t)B * S * H >= (int64_t(1) << 31))
+        return VSA_ERR_LIMITS;
+    int dev = 0;
+    vsa_status st = current_device(&dev);
+    if (st != VSA_OK) return st;
+    DeviceCache &dc = g_dev[dev];
+    p.row_to_token = row_to_token;
+    p.status = dc.status_ptr.load(std::memory_order_acquire);
+    p.B = B;
+    p.S = S;
+    p.H = H;
+    p.Dv = D / 8;
+    p.Sp = Sp;
+    if (launch_layout(p, dc.sm_count.load(std::memory_order_acquire), reinterpret_cast<cudaStream_t>(stream)) !=
+        cudaSuccess)
+        return VSA_ERR_CUDA;
+    t_route = vsa_route{};
+    t_route.kernel = VSA_KERNEL_LAYOUT;
+    t_route.tile = tile;
+    t_route.head_dim = D;
+    return VSA_OK;
+}
+
+vsa_status vsa_validate_indices(const int32_t *q2k_idx, const int32_t *q2k_num, const int32_t *block_sizes,
+                                const vsa_dims *dims, int32_t *dev_status, vsa_stream_t stream) {
+    vsa_status st = check_dims(dims);
+    if (st != VSA_OK) return st;
+    if (!q2k_num || !block_sizes || !dev_status || (!q2k_idx && dims->max_kv > 0)) return VSA_ERR_ARG;
+    if (!aligned(q2k_num, 4) || !aligned(block_sizes, 4) || !aligned(dev_status, 4) ||
+        (q2k_idx && !aligned(q2k_idx, 4)))
+        return VSA_ERR_ALIGN;
+    int dev = 0;
+    if ((st = current_device(&dev)) != VSA_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(dev_status, 0, sizeof(int32_t), s) != cudaSuccess) return VSA_ERR_CUDA;
+    const int64_t n_rows = (int64_t)dims->B * dims->H * dims->num_tiles;
+    const int64_t n = n_rows > dims->num_tiles ? n_rows : dims->num_tiles;
+    const int threads = 256;
+    validate_kernel<<<(unsigned)((n + threads - 1) / threads), threads, 0, s>>>(
+        q2k_idx, q2k_num, block_sizes, n_rows, dims->num_tiles, dims->tile, dims->max_kv, dev_status);
+    if (cudaGetLastError() != cudaSuccess) return VSA_ERR_CUDA;
+    t_route = vsa_route{};
+    t_route.kernel = VSA_KERNEL_VALIDATE;
+    return VSA_OK;
+}
+
+vsa_status vsa_check_device_status(vsa_stream_t stream) {
+    int dev = 0;
+    vsa_status st = current_device(&dev);
+    if (st != VSA_OK) return st;
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return VSA_ERR_CUDA;
+    }
+    int32_t word = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&word, g_device_status, sizeof word) != cudaSuccess ||
+        cudaMemcpyToSymbol(g_device_status, &zero, sizeof zero) != cudaSuccess) {
+        cudaGetLastError();
+        return VSA_ERR_CUDA;
+    }
+    if (word & kFlagTimeout) return VSA_ERR_TIMEOUT;
+    if (word & kFlagIndex) return VSA_ERR_INDEX;
+    return VSA_OK;
+}
+
+vsa_status vsa_last_route(vsa_route *route) {
+    if (!route) return VSA_ERR_ARG;
+    *route = t_route;
+    return VSA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,64 @@
+// Internal interface between the host API (vsa_api.cu) and the kernels.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace vsa {
+
+// Bits of the device status word.
+enum : int32_t { kFlagIndex = 1, kFlagTimeout = 2 };
+
+// Query rows of one work item: two 128-row units, each one MMA M=128.
+constexpr int kUnitRows = 128;
+constexpr int kItemRows = 256;
+constexpr int kAttnThreads = 320;  // 8 softmax warps, 1 MMA warp, 1 producer warp
+constexpr int kMaxTiles = 8192;     // VSA_MAX_TILES
+
+struct AttnParams {
+    const int32_t *q2k_idx;      // [B*H*NT, max_kv]
+    const int32_t *q2k_num;      // [B*H*NT]
+    const int32_t *block_sizes;  // [NT]
+    void *out;                   // bf16 [B*H*Sp, D]
+    float *lse;                  // [B*H*Sp] or nullptr
+    const int32_t *order;        // [n_items] work order (longest first)
+    int32_t *work_counter;       // next slot of `order` to hand out
+    int32_t *status;             // device status word
+    int32_t NT;
+    int32_t max_kv;
+    int32_t G;                   // work items per (b, h)
+    int32_t bm_words;            // 32-bit words of one selection bitmap
+    int32_t n_items;
+    int64_t Sp;                  // NT * tile
+    float scale_log2;            // softmax scale * log2(e)
+};
+
+struct AttnLaunchInfo {
+    int stages;
+    int smem_bytes;
+};
+
+// Dynamic shared memory and ring depth of the attention kernel variant.
+AttnLaunchInfo attn_launch_info(int tile, int head_dim, int bm_words);
+
+// Enables the variant's shared-memory size on the current device (once).
+cudaError_t attn_prepare(int tile, int head_dim, int device);
+
+cudaError_t launch_attn(int tile, int head_dim, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
+                        const CUtensorMap &tm_v, const AttnParams &p, int grid, cudaStream_t stream);
+
+struct LayoutParams {
+    const void *src[3];
+    void *dst[3];
+    const int32_t *row_to_token;
+    int32_t *status;
+    int32_t n_tensors;
+    int32_t B, S, H, Dv;  // Dv = head_dim / 8 (16-byte vectors per row)
+    int64_t Sp;
+};
+
+cudaError_t launch_layout(const LayoutParams &p, int num_sms, cudaStream_t stream);
+
+}  // namespace vsa

@@ -1,0 +1,175 @@
+/*
+ * vsa.h -- C ABI of the GB300 (sm_103a) block-sparse attention library.
+ *
+ * The operation is the block-sparse attention forward pass of video sparse
+ * attention as described on the FastVideo kernel page (hao-ai-lab/FastVideo
+ * commit 8503617, fastvideo-kernel/python):
+ *   - commit adding the sm_121a tile-128 forward: inputs q, k, v, q2k_idx,
+ *     q2k_num, variable_block_sizes; output out; tiles of 64 or 128 tokens;
+ *     each query tile attends only to the key tiles its selection lists;
+ *   - sm_121a hardening commit: keys past a tile's valid count are masked,
+ *     NaN/Inf padding never reaches the output, a query row with no keys is 0,
+ *     a NaN softmax sum gives a NaN row; launch limits batch*heads <= 65535,
+ *     rows < 2^31, tiles < 2^22, checked before launch; a GPU the kernel was
+ *     not built for gets an error, never uninitialised output;
+ *   - fused tile_to_bhsd commit: one pass that scatters token-major Q/K/V into
+ *     tile-major BHSD;
+ *   - Attn-QAT SM100 commit: the forward pass also yields softmax statistics
+ *     (here the natural-log log-sum-exp of each query row).
+ *
+ * Conventions for every call
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *     keeps no reference after the call returns and allocates no device
+ *     memory.  Scratch memory is passed in by the caller (workspace).
+ *   - bf16 tensors are contiguous, 16-byte aligned.  Tile-major layout is
+ *     [B, H, num_tiles*tile, head_dim]: row t*tile + r holds token r of tile t;
+ *     rows r >= block_sizes[t] are padding and their contents are never read.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
+ *     default stream).  Argument, limit and architecture errors are returned
+ *     synchronously before anything is launched.  Errors detected on the
+ *     device (bad indices, a wait that timed out) are recorded in a device
+ *     status word and reported by vsa_check_device_status().
+ *   - Only GPUs of compute capability 10.3 (sm_103) are supported; any other
+ *     device returns VSA_ERR_ARCH.
+ */
+#ifndef VSA_H
+#define VSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *vsa_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+    VSA_OK = 0,
+    VSA_ERR_ARG = -1,       /* null pointer, bad size, unsupported tile or head_dim */
+    VSA_ERR_ALIGN = -2,     /* a pointer is not 16-byte aligned */
+    VSA_ERR_LIMITS = -3,    /* a launch limit below is exceeded */
+    VSA_ERR_ARCH = -4,      /* the current device is not sm_103 */
+    VSA_ERR_CUDA = -5,      /* a CUDA runtime call or launch failed */
+    VSA_ERR_TIMEOUT = -6,   /* a device-side wait gave up (reported later) */
+    VSA_ERR_INDEX = -7,     /* bad q2k_idx / q2k_num / row map seen on the device */
+    VSA_ERR_WORKSPACE = -8  /* workspace missing or smaller than required */
+} vsa_status;
+
+/* Launch limits.  The first two follow the page's MaxBatchHeads / MaxRows;
+ * the tile limit is this kernel's own (the per-CTA selection bitmap lives in
+ * shared memory), tighter than the page's 2^22. */
+#define VSA_MAX_BATCH_HEADS 65535
+#define VSA_MAX_ROWS_LOG2 31        /* B*H*num_tiles*tile < 2^31 */
+#define VSA_MAX_TILES 8192          /* num_tiles <= 8192 */
+
+typedef struct {
+    int32_t B;          /* batch */
+    int32_t H;          /* heads */
+    int32_t num_tiles;  /* tiles per sequence (NT) */
+    int32_t tile;       /* tokens per tile: 64 or 128 */
+    int32_t head_dim;   /* 64 or 128 */
+    int32_t max_kv;     /* row length of q2k_idx (>= 0) */
+    float scale;        /* softmax scale; <= 0 selects 1/sqrt(head_dim) */
+} vsa_dims;
+
+/* Identifies the kernel that ran, for tests (route assertion). */
+typedef struct {
+    int32_t kernel;       /* VSA_KERNEL_* */
+    int32_t tile;
+    int32_t head_dim;
+    int32_t grid;         /* CTAs launched (persistent) */
+    int32_t block;        /* threads per CTA */
+    int32_t stages;       /* K/V ring depth in shared memory */
+    int64_t work_items;   /* 256-query-row work items scheduled */
+    int32_t sort_bins;    /* bins of the on-device work ordering */
+    int32_t smem_bytes;   /* dynamic shared memory per CTA */
+} vsa_route;
+
+#define VSA_KERNEL_NONE 0
+#define VSA_KERNEL_ATTN_TCGEN05 1
+#define VSA_KERNEL_LAYOUT 2
+#define VSA_KERNEL_VALIDATE 3
+
+/* Bytes of workspace vsa_block_sparse_fwd needs for `dims` (the on-device work
+ * order and its counter).  Returns 0 when `dims` is invalid. */
+size_t vsa_block_sparse_workspace_size(const vsa_dims *dims);
+
+/*
+ * Block-sparse attention forward (commit adding the sm_121a tile-128
+ * forward; sm_121a hardening commit for the masking and NaN rules).
+ *
+ *   q, k, v      bf16 [B, H, NT*tile, D] tile-major, read only
+ *   q2k_idx      int32 [B, H, NT, max_kv]; entries [0, q2k_num) of each row are
+ *                the selected key tiles, distinct, in [0, NT); order is free
+ *   q2k_num      int32 [B, H, NT], each in [0, max_kv]
+ *   block_sizes  int32 [NT], each in [0, tile]: valid tokens of each tile
+ *                (shared by queries and keys; Sq == Sk)
+ *   out          bf16 [B, H, NT*tile, D]: for a valid query row r < n_t,
+ *                softmax(scale * q_r . K_L^T) V_L over the valid rows L of the
+ *                selected key tiles; +0 when L is empty; a NaN softmax sum
+ *                gives a NaN row; padding rows r >= n_t are written as +0.
+ *   lse          NULL, or fp32 [B, H, NT*tile]: natural-log log-sum-exp of the
+ *                scaled scores per row; -inf for padding rows and empty rows.
+ *   workspace    device scratch of vsa_block_sparse_workspace_size(dims) bytes,
+ *                16-byte aligned; contents need not be initialised; must not
+ *                be used by another call that runs concurrently.
+ *
+ * Out-of-range or repeated indices and out-of-range counts never fault: they
+ * are skipped / clamped and flagged as VSA_ERR_INDEX in the device status
+ * word.  Use vsa_validate_indices() to check a selection up front.
+ * With tile == 64, two tiles share one 128-row MMA; a non-finite value in a
+ * VALID V row can then also reach the rows of the paired tile (padding rows
+ * are always safe).
+ */
+vsa_status vsa_block_sparse_fwd(const void *q, const void *k, const void *v, const int32_t *q2k_idx,
+                                const int32_t *q2k_num, const int32_t *block_sizes, void *out,
+                                float *lse, const vsa_dims *dims, void *workspace,
+                                size_t workspace_bytes, vsa_stream_t stream);
+
+/*
+ * Fused tile layout (fused tile_to_bhsd commit): one pass over up to three
+ * tensors that gathers token-major rows into tile-major order.
+ *
+ *   x_tok        bf16 [B, S, H, D] token-major (q, k, v; a pair may be NULL/NULL)
+ *   x_tile       bf16 [B, H, NT*tile, D] tile-major output
+ *   row_to_token int32 [NT*tile]: source token of every tile-major row, or -1
+ *                for a padding row, which is written as +0.  A value outside
+ *                [-1, S) writes +0 and flags VSA_ERR_INDEX on the device.
+ *   D            head_dim, a multiple of 8 (16-byte rows)
+ */
+vsa_status vsa_tile_layout(const void *q_tok, const void *k_tok, const void *v_tok, void *q_tile,
+                           void *k_tile, void *v_tile, const int32_t *row_to_token, int32_t B,
+                           int32_t S, int32_t H, int32_t D, int32_t num_tiles, int32_t tile,
+                           vsa_stream_t stream);
+
+/*
+ * Opt-in selection check (sm_121a hardening commit, launch-limit and
+ * fail-closed items).  Writes to *dev_status (a device int32): 0 when every
+ * q2k_num is in [0, max_kv], every live index is in [0, NT) and distinct within
+ * its row, and every block size is in [0, tile]; VSA_ERR_INDEX otherwise.
+ * Asynchronous; never traps.
+ */
+vsa_status vsa_validate_indices(const int32_t *q2k_idx, const int32_t *q2k_num,
+                                const int32_t *block_sizes, const vsa_dims *dims,
+                                int32_t *dev_status, vsa_stream_t stream);
+
+/* Synchronises `stream`, then reads and clears the current device's status
+ * word: VSA_OK, VSA_ERR_INDEX or VSA_ERR_TIMEOUT (the most severe seen since
+ * the last check). */
+vsa_status vsa_check_device_status(vsa_stream_t stream);
+
+/* Route of the last successful launch on the calling host thread. */
+vsa_status vsa_last_route(vsa_route *route);
+
+/* Static description of a status code. */
+const char *vsa_status_string(vsa_status status);
+
+/* Library ABI version (major*1000 + minor). */
+int32_t vsa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VSA_H */

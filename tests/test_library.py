@@ -1,0 +1,122 @@
+"""Host-side checks of the C-ABI library (no GPU needed).
+
+The library must load, export every entry point declared in include/vsa.h,
+and reject bad arguments and over-limit sizes with a status code before it
+touches the device (the sm_121a hardening commit on the FastVideo kernel page:
+limits are checked before launch; errors are reported, never silently
+accepted).  Pointers below are fake but never dereferenced: every call fails
+its host-side checks first.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def vsa():
+    from block_sparse_attention_gathered_gb300 import build as B
+    B.build()
+    import block_sparse_attention_gathered_gb300 as V
+    return V
+
+
+def _declared_symbols():
+    text = open(os.path.join(ROOT, "include", "vsa.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(vsa_[a-z_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(vsa):
+    declared = _declared_symbols()
+    assert len(declared) >= 8
+    lib = ctypes.CDLL(vsa.LIB_PATH)
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert set(declared) == set(vsa.EXPORTED)
+    assert vsa.vsa_version() == 1000
+
+
+def test_status_strings(vsa):
+    for code in range(0, -9, -1):
+        s = vsa.vsa_status_string(code)
+        assert s and s != "unknown status"
+    assert vsa.vsa_status_string(-99) == "unknown status"
+
+
+FAKE = 0x100000  # 16-byte aligned, never dereferenced
+
+
+def _fwd(vsa, dims, q=FAKE, k=FAKE, v=FAKE, idx=FAKE, num=FAKE, bs=FAKE, out=FAKE, lse=None,
+         ws=FAKE, ws_bytes=1 << 30):
+    P = ctypes.c_void_p
+    return vsa.library().vsa_block_sparse_fwd(P(q), P(k), P(v), P(idx), P(num), P(bs), P(out),
+                                               P(lse) if lse else None, ctypes.byref(dims), P(ws),
+                                               ws_bytes, None)
+
+
+def test_argument_errors(vsa):
+    ok = vsa.make_dims(1, 2, 4, 64, 64, 2)
+    assert _fwd(vsa, vsa.make_dims(1, 2, 4, 32, 64, 2)) == vsa.VSA_ERR_ARG          # tile
+    assert _fwd(vsa, vsa.make_dims(1, 2, 4, 64, 96, 2)) == vsa.VSA_ERR_ARG          # head_dim
+    assert _fwd(vsa, vsa.make_dims(0, 2, 4, 64, 64, 2)) == vsa.VSA_ERR_ARG          # batch
+    assert _fwd(vsa, vsa.make_dims(1, 2, 0, 64, 64, 2)) == vsa.VSA_ERR_ARG          # tiles
+    assert _fwd(vsa, vsa.make_dims(1, 2, 4, 64, 64, -1)) == vsa.VSA_ERR_ARG         # max_kv
+    assert _fwd(vsa, vsa.make_dims(1, 2, 4, 64, 64, 2, float("nan"))) == vsa.VSA_ERR_ARG
+    assert _fwd(vsa, ok, q=0) == vsa.VSA_ERR_ARG
+    assert _fwd(vsa, ok, out=0) == vsa.VSA_ERR_ARG
+    assert _fwd(vsa, ok, num=0) == vsa.VSA_ERR_ARG
+    assert _fwd(vsa, ok, q=FAKE + 8) == vsa.VSA_ERR_ALIGN
+    assert _fwd(vsa, ok, out=FAKE + 2) == vsa.VSA_ERR_ALIGN
+    assert _fwd(vsa, ok, lse=FAKE + 2) == vsa.VSA_ERR_ALIGN
+    assert _fwd(vsa, ok, ws=0) == vsa.VSA_ERR_WORKSPACE
+    assert _fwd(vsa, ok, ws_bytes=16) == vsa.VSA_ERR_WORKSPACE
+
+
+def test_launch_limits(vsa):
+    # batch * heads <= 65535
+    assert _fwd(vsa, vsa.make_dims(256, 256, 4, 64, 64, 2)) == vsa.VSA_ERR_LIMITS
+    assert vsa.vsa_block_sparse_workspace_size(vsa.make_dims(256, 256, 4, 64, 64, 2)) == 0
+    # tiles <= 8192 (selection bitmap held in shared memory)
+    assert _fwd(vsa, vsa.make_dims(1, 1, 8193, 64, 64, 2)) == vsa.VSA_ERR_LIMITS
+    # rows < 2^31
+    assert _fwd(vsa, vsa.make_dims(16, 4096, 8192, 128, 64, 2)) == vsa.VSA_ERR_LIMITS
+    assert _fwd(vsa, vsa.make_dims(65535, 1, 257, 128, 128, 1)) == vsa.VSA_ERR_LIMITS
+
+
+def test_workspace_size(vsa):
+    # header (256 bytes) + one int32 per 256-query-row work item
+    d = vsa.make_dims(1, 6, 244, 128, 128, 244)
+    assert vsa.vsa_block_sparse_workspace_size(d) == 256 + 4 * 6 * 122
+    d = vsa.make_dims(2, 8, 63, 64, 64, 31)
+    assert vsa.vsa_block_sparse_workspace_size(d) == 256 + 4 * 16 * 16
+
+
+def test_layout_argument_errors(vsa):
+    P = ctypes.c_void_p
+    L = vsa.library().vsa_tile_layout
+    f = lambda *a: L(*[P(x) if x else None for x in a[:7]], *a[7:], None)
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, 1, 8, 2, 64, 1, 8) == vsa.VSA_ERR_ARG       # map
+    assert f(FAKE, 0, 0, FAKE, FAKE, 0, FAKE, 1, 8, 2, 64, 1, 8) == vsa.VSA_ERR_ARG            # pair
+    assert f(0, 0, 0, 0, 0, 0, FAKE, 1, 8, 2, 64, 1, 8) == vsa.VSA_ERR_ARG                     # none
+    assert f(FAKE, 0, 0, FAKE, 0, 0, FAKE, 1, 8, 2, 60, 1, 8) == vsa.VSA_ERR_ARG               # D%8
+    assert f(FAKE + 4, 0, 0, FAKE, 0, 0, FAKE, 1, 8, 2, 64, 1, 8) == vsa.VSA_ERR_ALIGN
+
+
+def test_validate_argument_errors(vsa):
+    P = ctypes.c_void_p
+    d = vsa.make_dims(1, 2, 4, 64, 64, 2)
+    V = vsa.library().vsa_validate_indices
+    assert V(P(FAKE), P(FAKE), P(FAKE), ctypes.byref(d), None, None) == vsa.VSA_ERR_ARG
+    assert V(P(FAKE), P(FAKE + 2), P(FAKE), ctypes.byref(d), P(FAKE), None) == vsa.VSA_ERR_ALIGN
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
+def test_no_device_is_an_error_not_a_launch(vsa):
+    st = _fwd(vsa, vsa.make_dims(1, 2, 4, 64, 64, 2))
+    assert st in (vsa.VSA_ERR_CUDA, vsa.VSA_ERR_ARCH)
+    assert vsa.vsa_check_device_status(0) in (vsa.VSA_ERR_CUDA, vsa.VSA_ERR_ARCH)
