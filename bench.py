@@ -1,0 +1,357 @@
+"""Benchmark: block-sparse attention forward on one GB300 per rank.
+
+One step = the whole hot path on one batch of synthetic input: the fused tile
+layout of token-major Q/K/V, the on-device work ordering, and the tcgen05
+attention kernel with LSE.  Default workload: the dense-limit case of the
+FastVideo kernel page's Attn-QAT SM100 commit -- 6 heads, 31200 tokens (244
+tiles of 128, last tile 96), head_dim 128, every query tile selecting every key
+tile, bf16, LSE on.
+
+Prints ONE JSON line (rank 0).  ``value`` is effective TFLOPS on selected tiles
+(4*D*sum n_t*n_j over the selected tile pairs, valid tokens only) over the
+device-timed step; ``e2e`` repeats the measurement through the C ABI from
+pinned host buffers with the host<->device copies inside the timed region.
+With ``--impl reference`` the CPU oracle is timed instead, on a bounded sample
+of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+METRIC = "effective BF16 TFLOPS on selected tiles"
+UNIT = "TFLOP/s"
+FALLBACK_BF16_TFLOPS = 1900.0
+FALLBACK_HBM_GBS = 6800.0
+
+# DRAM bytes (read + write) per attention launch from an ncu capture, keyed by
+# the SHA-256 of the attention kernel source the capture was taken with; a
+# changed kernel reports null until it is captured again.
+ATTN_TRAFFIC = {}
+
+
+def _rank_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d.get("bf16_tflops", FALLBACK_BF16_TFLOPS), d.get("hbm_gbs", FALLBACK_HBM_GBS), "measured"
+    return FALLBACK_BF16_TFLOPS, FALLBACK_HBM_GBS, "fallback"
+
+
+def _attn_source_hash():
+    with open(os.path.join(ROOT, "block_sparse_attention_gathered_gb300", "csrc", "vsa_attn.cu"), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.t.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def _cpu_sample_units(w, budget_s: float, nthreads: int):
+    """Pick a bounded, seeded sample of query tiles for the oracle, sized from a
+    one-tile probe to take about ``budget_s`` on ``nthreads`` host threads."""
+    import numpy as np
+    import oracle
+    rng = np.random.default_rng(1234)
+    total = w.B * w.H * w.NT
+    refs = [oracle.tile_layout(x, w.row_to_token, w.NT, w.T) for x in (w.q_tok, w.k_tok, w.v_tok)] \
+        if w.token_major else [x for x in (w.q, w.k, w.v)]
+    t0 = time.perf_counter()
+    oracle.block_sparse_attention(refs[0], refs[1], refs[2], w.q2k_idx, w.q2k_num, w.block_sizes, w.T,
+                                  w.scale, units=[0], nthreads=1)
+    one = max(time.perf_counter() - t0, 1e-3)
+    n = int(max(1, min(total, budget_s * nthreads / one)))
+    n = max(n - n % nthreads, min(total, nthreads))
+    units = sorted(rng.choice(total, size=min(n, total), replace=False).tolist())
+    return refs, units
+
+
+def _unit_flops(w, units):
+    bs = w.block_sizes.tolist()
+    D = w.D
+    tot = 0
+    for u in units:
+        b, h, t = u // (w.H * w.NT), (u // w.NT) % w.H, u % w.NT
+        sel = w.q2k_idx[b, h, t, :int(w.q2k_num[b, h, t])].tolist()
+        tot += 4 * D * bs[t] * sum(bs[j] for j in sel)
+    return tot
+
+
+def cpu_oracle_run(w, budget_s: float):
+    import oracle
+    nthreads = oracle.default_threads()
+    refs, units = _cpu_sample_units(w, budget_s, nthreads)
+    t0 = time.perf_counter()
+    oracle.block_sparse_attention(refs[0], refs[1], refs[2], w.q2k_idx, w.q2k_num, w.block_sizes, w.T, w.scale,
+                                  units=units, want_lse=w.want_lse, nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    fl = _unit_flops(w, units)
+    return {"value": fl / dt / 1e12, "unit": UNIT, "cores": nthreads, "kind": "oracle",
+            "sample": f"{len(units)} of {w.B * w.H * w.NT} query tiles of {w.name} (seeded), "
+                      f"{fl:.3e} effective flops in {dt:.1f} s, FP64"}
+
+
+def run_reference(args, cfg):
+    rank, world, _ = _rank_env()
+    if rank != 0:
+        return
+    w = W.make_workload(cfg)
+    import oracle
+    oracle.build()
+    nthreads = oracle.default_threads()
+    refs, units = _cpu_sample_units(w, 4.0, nthreads)
+    fl = _unit_flops(w, units)
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        oracle.block_sparse_attention(refs[0], refs[1], refs[2], w.q2k_idx, w.q2k_num, w.block_sizes, w.T,
+                                      w.scale, units=units, want_lse=w.want_lse, nthreads=nthreads)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    ms = 1e3 * sum(times) / len(times)
+    val = fl / (ms / 1e3) / 1e12
+    sample = f"{len(units)} of {w.B * w.H * w.NT} query tiles of {w.name} per step (seeded), FP64"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "S": w.S or w.Sp, "head_dim": w.D, "tile": w.T,
+                   "num_tiles": w.NT, "density": "100%" if cfg == 5 else "per workload",
+                   "lse": w.want_lse},
+        "cpu_baseline": {"value": val, "unit": UNIT, "cores": nthreads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def run_ours(args, cfg):
+    import block_sparse_attention_gathered_gb300 as vsa
+
+    rank, world, local = _rank_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    w = W.make_workload(cfg)
+    assert w.token_major
+    eff = W.effective_flops(w)
+    B, H, D, T, NT, S = w.B, w.H, w.D, w.T, w.NT, w.S
+    Sp = w.Sp
+
+    q_tok, k_tok, v_tok = (x.to(dev) for x in (w.q_tok, w.k_tok, w.v_tok))
+    r2t = w.row_to_token.to(dev)
+    idx, num, bs = w.q2k_idx.to(dev), w.q2k_num.to(dev), w.block_sizes.to(dev)
+    tiles = [torch.empty((B, H, Sp, D), dtype=torch.bfloat16, device=dev) for _ in range(3)]
+    out = torch.empty((B, H, Sp, D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, H, Sp), dtype=torch.float32, device=dev) if w.want_lse else None
+    dims = vsa.make_dims(B, H, NT, T, D, w.max_kv, w.scale)
+    ws = torch.empty(vsa.vsa_block_sparse_workspace_size(dims), dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)  # > 129 MB L2
+    stream = torch.cuda.current_stream()
+
+    def step(qt, kt, vt):
+        vsa.vsa_tile_layout(qt, kt, vt, tiles[0], tiles[1], tiles[2], r2t, B, S, H, D, NT, T, stream)
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        vsa.vsa_block_sparse_fwd(tiles[0], tiles[1], tiles[2], idx, num, bs, out, lse, dims, ws, stream)
+        a1.record(stream)
+        return a0, a1
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(max(args.warmup, 3)):
+        step(q_tok, k_tok, v_tok)
+    barrier()
+    if vsa.vsa_check_device_status() != 0:
+        raise RuntimeError("device status error during warm-up")
+
+    # ---------------------------------------------------------------- device-timed steps
+    pairs, attn = [], []
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        barrier()
+        for _ in range(args.steps):
+            flush.zero_()  # L2 flush, outside the timed events
+            s0 = torch.cuda.Event(enable_timing=True)
+            s1 = torch.cuda.Event(enable_timing=True)
+            s0.record(stream)
+            a0, a1 = step(q_tok, k_tok, v_tok)
+            s1.record(stream)
+            pairs.append((s0, s1))
+            attn.append((a0, a1))
+        barrier()
+    step_ms = [a.elapsed_time(b) for a, b in pairs]
+    attn_ms = [a.elapsed_time(b) for a, b in attn]
+    ms = sum(step_ms) / len(step_ms)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    if vsa.vsa_check_device_status() != 0:
+        raise RuntimeError("device status error in the timed region")
+
+    # ---------------------------------------------------------------- end to end from host buffers
+    hq, hk, hv = (x.pin_memory() for x in (w.q_tok, w.k_tok, w.v_tok))
+    hidx, hnum, hbs, hr2t = (x.pin_memory() for x in (w.q2k_idx, w.q2k_num, w.block_sizes, w.row_to_token))
+    hout = torch.empty((B, H, Sp, D), dtype=torch.bfloat16).pin_memory()
+    hlse = torch.empty((B, H, Sp), dtype=torch.float32).pin_memory() if lse is not None else None
+    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hidx, hnum, hbs, hr2t))
+    d2h = hout.numel() * 2 + (hlse.numel() * 4 if hlse is not None else 0)
+
+    def e2e_step():
+        for d_, h_ in ((q_tok, hq), (k_tok, hk), (v_tok, hv), (idx, hidx), (num, hnum), (bs, hbs), (r2t, hr2t)):
+            d_.copy_(h_, non_blocking=True)
+        step(q_tok, k_tok, v_tok)
+        hout.copy_(out, non_blocking=True)
+        if hlse is not None:
+            hlse.copy_(lse, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    barrier()
+    e_ms = []
+    for _ in range(args.steps):
+        flush.zero_()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        e2e_step()
+        e1.record(stream)
+        e_ms.append((e0, e1))
+    barrier()
+    e2e_ms = sum(a.elapsed_time(b) for a, b in e_ms) / len(e_ms)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    route = vsa.vsa_last_route()
+    peak, hbm, src = _peaks()
+    attn_avg = sum(attn_ms) / len(attn_ms)
+    achieved = eff / (attn_avg / 1e3) / 1e12
+    h = _attn_source_hash()
+    traffic = ATTN_TRAFFIC.get((w.name, h))
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": world * eff / (ms / 1e3) / 1e12, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "B": B, "H": H, "S": S, "head_dim": D, "tile": T, "num_tiles": NT,
+                       "density": "100%", "lse": True, "effective_flops": eff,
+                       "padded_flops": W.padded_flops(w), "l2": "flushed (256 MB write) between steps",
+                       "step": "tile layout (q,k,v) + work ordering + tcgen05 attention"},
+            "attn_ms": attn_avg, "layout_plus_sched_ms": ms - attn_avg,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak, "traffic": traffic,
+                         "peak_source": f"{src} bf16 burst (cuBLAS)", "kernel": "attn_fwd_kernel<128,128>"},
+            "e2e": {"value": world * eff / (e2e_ms / 1e3) / 1e12, "unit": UNIT, "ms_per_step": e2e_ms,
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": 3 * args.steps,
+            "clocks": clk.summary(),
+            "route": route,
+        }
+        if not args.no_cpu_baseline and world == 1:
+            line["cpu_baseline"] = cpu_oracle_run(w, args.cpu_seconds)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", type=int, default=5, choices=[2, 4, 5])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args, args.config)
+    else:
+        run_ours(args, args.config)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,84 @@
+"""Comparison helpers for GPU-vs-oracle parity tests.
+
+The bar (block-sparse forward, BF16 in / FP32 accumulate): over valid,
+non-NaN query rows, max |gpu - ref| <= 2e-2 and ||gpu - ref||_2 / ||ref||_2 <=
+5e-3 with the FP64 oracle rounded to FP32; rows the oracle gives as exact zero
+(empty selections, padding) must be bitwise +0.0; NaN rows must be NaN in every
+element on both sides; padding rows of the output must be +0.0.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+MAX_ABS = 2e-2
+REL_RMS = 5e-3
+LSE_ABS = 2e-3
+
+
+def unit_rows(units, NT, T):
+    """(bh, t) pairs of flat unit ids."""
+    return [(u // NT, u % NT) for u in units]
+
+
+def gather_gpu_units(out: torch.Tensor, units, NT, T):
+    """GPU tile-major output -> [n_units, T, D] float32 numpy (exact widening)."""
+    B, H, Sp, D = out.shape
+    flat = out.reshape(B * H, Sp, D)
+    idx = torch.tensor([bh for bh, _ in unit_rows(units, NT, T)], dtype=torch.long)
+    tiles = torch.stack([flat[bh, t * T:(t + 1) * T] for bh, t in unit_rows(units, NT, T)])
+    return tiles.float().cpu().numpy()
+
+
+def gather_gpu_lse(lse: torch.Tensor, units, NT, T):
+    B, H, Sp = lse.shape
+    flat = lse.reshape(B * H, Sp)
+    return torch.stack([flat[bh, t * T:(t + 1) * T] for bh, t in unit_rows(units, NT, T)]).cpu().numpy()
+
+
+def assert_parity(gpu: np.ndarray, ref: np.ndarray, block_sizes, units, NT, T, gpu_lse=None, ref_lse=None,
+                  label=""):
+    """gpu [n, T, D] float32; ref [n, T, D] float64 from the oracle."""
+    bs = np.asarray(block_sizes)
+    ref32 = ref.astype(np.float32)
+    n = gpu.shape[0]
+    valid = np.zeros((n, T), dtype=bool)
+    for i, (_, t) in enumerate(unit_rows(units, NT, T)):
+        valid[i, :int(bs[t])] = True
+    # padding rows: +0 exactly
+    pad = gpu[~valid]
+    assert (pad.view(np.uint32) == 0).all(), f"{label}: padding rows not +0"
+    ref_nan = np.isnan(ref32).all(-1)
+    gpu_nan = np.isnan(gpu).all(-1)
+    assert (np.isnan(ref32).any(-1) == ref_nan).all()
+    np.testing.assert_array_equal(gpu_nan[valid], ref_nan[valid], err_msg=f"{label}: NaN rows differ")
+    assert not (np.isnan(gpu).any(-1) & ~gpu_nan)[valid].any(), f"{label}: partial NaN row"
+    zero_rows = (ref32 == 0).all(-1) & valid
+    assert (gpu[zero_rows].view(np.uint32) == 0).all(), f"{label}: empty rows not +0"
+    live = valid & ~ref_nan
+    g, r = gpu[live].astype(np.float64), ref32[live].astype(np.float64)
+    if g.size:
+        err = np.abs(g - r)
+        mx = float(err.max())
+        rel = float(np.linalg.norm(g - r) / max(np.linalg.norm(r), 1e-30))
+        assert mx <= MAX_ABS, f"{label}: max abs {mx:.3e}"
+        assert rel <= REL_RMS, f"{label}: rel rms {rel:.3e}"
+    if gpu_lse is not None:
+        rl = ref_lse.astype(np.float32)
+        assert np.isneginf(gpu_lse[~valid]).all(), f"{label}: padding lse not -inf"
+        np.testing.assert_array_equal(np.isneginf(gpu_lse[valid]), np.isneginf(rl[valid]))
+        np.testing.assert_array_equal(np.isnan(gpu_lse[valid]), np.isnan(rl[valid]))
+        fin = valid & np.isfinite(rl)
+        if fin.any():
+            d = float(np.abs(gpu_lse[fin].astype(np.float64) - rl[fin]).max())
+            assert d <= LSE_ABS, f"{label}: lse max abs {d:.3e}"
+
+
+def sample_units(B, H, NT, n, seed, must=()):
+    """Seeded sample of flat unit ids, always including `must` (e.g. tails)."""
+    rng = np.random.default_rng(seed)
+    total = B * H * NT
+    picked = set(int(u) for u in must if 0 <= u < total)
+    while len(picked) < min(n, total):
+        picked.add(int(rng.integers(total)))
+    return sorted(picked)

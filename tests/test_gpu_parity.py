@@ -1,0 +1,235 @@
+"""GPU parity: the CUDA path (through the C ABI) against the FP64 CPU oracle.
+
+Every case draws seeded inputs from ``workloads``, runs the library's kernels
+on the GPU, and compares with ``oracle`` on the same inputs (see
+``tests/_parity.py`` for the bar).  Output buffers are pre-filled with NaN so
+that any row the kernel fails to write shows up (the NaN-filled allocator of
+the sm_121a test list on the FastVideo kernel page).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from tests import _parity as PT
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def vsa():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from block_sparse_attention_gathered_gb300 import build as B
+    B.build()
+    import block_sparse_attention_gathered_gb300 as V
+    assert V.vsa_check_device_status() == 0
+    return V
+
+
+def _bits(x: torch.Tensor) -> np.ndarray:
+    return x.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def _to_tile_major(w, vsa, oracle_mod):
+    """Returns GPU tile-major q, k, v and the oracle's tile-major bit arrays.
+    Token-major workloads go through the GPU layout kernel, which must match
+    the oracle's layout bit for bit."""
+    dev = "cuda"
+    if w.token_major:
+        r2t = w.row_to_token.to(dev)
+        gq, gk, gv = vsa.tile_layout(w.q_tok.to(dev), w.k_tok.to(dev), w.v_tok.to(dev), r2t, w.NT, w.T)
+        refs = [oracle_mod.tile_layout(x, w.row_to_token, w.NT, w.T) for x in (w.q_tok, w.k_tok, w.v_tok)]
+        for g, r in zip((gq, gk, gv), refs):
+            assert np.array_equal(_bits(g), r), "layout kernel differs from the oracle layout"
+        return (gq, gk, gv), refs
+    return tuple(x.to(dev) for x in (w.q, w.k, w.v)), [_bits(x) for x in (w.q, w.k, w.v)]
+
+
+def _run(vsa, q, k, v, w, scale=None):
+    dev = q.device
+    out = torch.full_like(q, float("nan"))
+    res = vsa.block_sparse_attention(q, k, v, w.q2k_idx.to(dev), w.q2k_num.to(dev), w.block_sizes.to(dev),
+                                     w.T, scale=w.scale if scale is None else scale, want_lse=True, out=out)
+    torch.cuda.synchronize()
+    assert vsa.vsa_check_device_status() == 0
+    return res
+
+
+def _check(w, gpu_out, gpu_lse, refs, oracle_mod, units, label):
+    ref, ref_lse = oracle_mod.block_sparse_attention(refs[0], refs[1], refs[2], w.q2k_idx, w.q2k_num,
+                                                     w.block_sizes, w.T, w.scale, units=units)
+    g = PT.gather_gpu_units(gpu_out, units, w.NT, w.T)
+    gl = PT.gather_gpu_lse(gpu_lse, units, w.NT, w.T)
+    PT.assert_parity(g, ref, w.block_sizes.numpy(), units, w.NT, w.T, gl, ref_lse, label=label)
+
+
+def test_tiny_full(vsa, oracle_mod):
+    w = W.make_workload(1)
+    (q, k, v), refs = _to_tile_major(w, vsa, oracle_mod)
+    out, lse = _run(vsa, q, k, v, w)
+    units = list(range(w.B * w.H * w.NT))
+    _check(w, out, lse, refs, oracle_mod, units, "tiny")
+    r = vsa.vsa_last_route()
+    assert r["kernel"] == vsa.VSA_KERNEL_ATTN_TCGEN05 and (r["tile"], r["head_dim"]) == (64, 64)
+    assert r["work_items"] == 2 and r["grid"] == 2
+
+
+def test_ragged_nan_padding_full(vsa, oracle_mod):
+    w = W.make_workload(3)
+    (q, k, v), refs = _to_tile_major(w, vsa, oracle_mod)
+    out, lse = _run(vsa, q, k, v, w)
+    units = list(range(w.B * w.H * w.NT))
+    _check(w, out, lse, refs, oracle_mod, units, "ragged")
+    # empty selections give exactly +0 and -inf
+    empty = (w.q2k_num == 0).nonzero().tolist()
+    assert empty
+    for b, h, t in empty[:20]:
+        rows = out[b, h, t * 64:(t + 1) * 64]
+        assert (rows.view(torch.int16) == 0).all()
+        assert torch.isneginf(lse[b, h, t * 64:(t + 1) * 64]).all()
+
+
+def test_uniform_sampled(vsa, oracle_mod):
+    w = W.make_workload(2)
+    (q, k, v), refs = _to_tile_major(w, vsa, oracle_mod)
+    out, lse = _run(vsa, q, k, v, w)
+    units = PT.sample_units(w.B, w.H, w.NT, 24, seed=2, must=(0, w.B * w.H * w.NT - 1))
+    _check(w, out, lse, refs, oracle_mod, units, "uniform")
+    assert torch.isfinite(out.float()).all()
+
+
+def test_video_topk_sampled(vsa, oracle_mod):
+    w = W.make_workload(4)
+    (q, k, v), refs = _to_tile_major(w, vsa, oracle_mod)
+    out, lse = _run(vsa, q, k, v, w)
+    partial = [t for t in range(w.NT) if int(w.block_sizes[t]) < 128]
+    must = [h * w.NT + t for h, t in ((0, partial[0]), (5, partial[-1]), (11, w.NT - 1))]
+    units = PT.sample_units(w.B, w.H, w.NT, 24, seed=4, must=must)
+    _check(w, out, lse, refs, oracle_mod, units, "video")
+
+
+def test_dense_limit_sampled(vsa, oracle_mod):
+    """Full size, in the bench's launch configuration (layout + attention, LSE on)."""
+    w = W.make_workload(5)
+    (q, k, v), refs = _to_tile_major(w, vsa, oracle_mod)
+    out, lse = _run(vsa, q, k, v, w)
+    last = w.NT - 1
+    units = PT.sample_units(w.B, w.H, w.NT, 16, seed=5, must=(last, w.H * w.NT - 1, 0))
+    _check(w, out, lse, refs, oracle_mod, units, "dense")
+    # properties over the whole output: valid rows finite, padding rows +0
+    assert torch.isfinite(out[:, :, :31200].float()).all()
+    assert (out[:, :, 31200:].view(torch.int16) == 0).all()
+    assert torch.isneginf(lse[:, :, 31200:]).all() and torch.isfinite(lse[:, :, :31200]).all()
+    r = vsa.vsa_last_route()
+    assert r["kernel"] == vsa.VSA_KERNEL_ATTN_TCGEN05 and (r["tile"], r["head_dim"]) == (128, 128)
+    assert r["work_items"] == 6 * 122
+    assert r["grid"] == min(6 * 122, torch.cuda.get_device_properties(0).multi_processor_count)
+
+
+def _random_case(seed, B, H, NT, T, D, pad="naninf", empty_frac=0.15, full=False):
+    g = torch.Generator().manual_seed(seed)
+    bs = torch.full((NT,), T, dtype=torch.int32) if full else torch.randint(1, T + 1, (NT,), generator=g).int()
+    if not full:
+        bs[torch.rand(NT, generator=g) < 0.1] = 0           # a few empty tiles
+        bs[NT // 2] = T
+    counts = torch.randint(0, NT + 1, (B, H, NT), generator=g).int()
+    counts[torch.rand((B, H, NT), generator=g) < empty_frac] = 0
+    idx = W.random_selection(g, B, H, NT, counts, NT)
+    q, k, v = (torch.randn((B, H, NT * T, D), generator=g).to(torch.bfloat16) for _ in range(3))
+    if not full:
+        q, k, v = (W.pad_tile_major(x, bs, T, pad) for x in (q, k, v))
+    return W.Workload("random", B, H, D, T, NT, bs, idx, counts, 1.0 / math.sqrt(D), True, q=q, k=k, v=v)
+
+
+@pytest.mark.parametrize("T,D,NT", [(64, 64, 9), (64, 128, 7), (128, 64, 5), (128, 128, 5), (64, 64, 1),
+                                    (128, 128, 3)])
+def test_variants_ragged(vsa, oracle_mod, T, D, NT):
+    w = _random_case(100 + T + D + NT, 2, 3, NT, T, D)
+    (q, k, v), refs = _to_tile_major(w, vsa, oracle_mod)
+    out, lse = _run(vsa, q, k, v, w)
+    _check(w, out, lse, refs, oracle_mod, list(range(w.B * w.H * w.NT)), f"T{T}D{D}NT{NT}")
+
+
+def test_many_waves(vsa, oracle_mod):
+    """More work items than SMs: every CTA takes several items."""
+    w = _random_case(7, 4, 48, 6, 128, 64, full=True)
+    (q, k, v), refs = _to_tile_major(w, vsa, oracle_mod)
+    out, lse = _run(vsa, q, k, v, w)
+    assert vsa.vsa_last_route()["work_items"] == 4 * 48 * 3
+    units = PT.sample_units(w.B, w.H, w.NT, 64, seed=8)
+    _check(w, out, lse, refs, oracle_mod, units, "waves")
+
+
+def test_all_empty_and_zero_max_kv(vsa):
+    dev = "cuda"
+    B, H, NT, T, D = 1, 2, 4, 128, 128
+    q = torch.randn((B, H, NT * T, D), device=dev).to(torch.bfloat16)
+    bs = torch.full((NT,), T, dtype=torch.int32, device=dev)
+    for max_kv in (3, 0):
+        idx = torch.zeros((B, H, NT, max_kv), dtype=torch.int32, device=dev)
+        num = torch.zeros((B, H, NT), dtype=torch.int32, device=dev)
+        out = torch.full_like(q, float("nan"))
+        out, lse = vsa.block_sparse_attention(q, q, q, idx, num, bs, T, want_lse=True, out=out)
+        torch.cuda.synchronize()
+        assert (out.view(torch.int16) == 0).all() and torch.isneginf(lse).all()
+    assert vsa.vsa_check_device_status() == 0
+
+
+def test_nan_in_valid_key_gives_nan_rows(vsa, oracle_mod):
+    w = _random_case(21, 1, 2, 5, 64, 64, full=True, empty_frac=0.0)
+    w.k = w.k.clone()
+    w.k[0, 1, 2 * 64 + 5, 7] = float("nan")   # tile 2 of head 1
+    (q, k, v), refs = _to_tile_major(w, vsa, oracle_mod)
+    out, lse = _run(vsa, q, k, v, w)
+    _check(w, out, lse, refs, oracle_mod, list(range(10)), "nan-key")
+    sel = [2 in w.q2k_idx[0, 1, t, :int(w.q2k_num[0, 1, t])].tolist() for t in range(5)]
+    assert any(sel)
+    for t in range(5):
+        assert bool(torch.isnan(out[0, 1, t * 64:(t + 1) * 64].float()).all()) == sel[t]
+
+
+def test_deterministic(vsa, oracle_mod):
+    w = W.make_workload(3)
+    (q, k, v), _ = _to_tile_major(w, vsa, oracle_mod)
+    a, la = _run(vsa, q, k, v, w)
+    b, lb = _run(vsa, q, k, v, w)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    assert torch.equal(la.view(torch.int32), lb.view(torch.int32))
+
+
+def test_bad_indices_are_flagged_not_faulted(vsa):
+    dev = "cuda"
+    B, H, NT, T, D = 1, 1, 4, 64, 64
+    q = torch.randn((B, H, NT * T, D), device=dev).to(torch.bfloat16)
+    bs = torch.full((NT,), T, dtype=torch.int32, device=dev)
+    num = torch.full((B, H, NT), 2, dtype=torch.int32, device=dev)
+    idx = torch.tensor([[[[0, 1], [1, 1], [2, 9], [3, -4]]]], dtype=torch.int32, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    d = vsa.make_dims(B, H, NT, T, D, 2)
+    vsa.vsa_validate_indices(idx, num, bs, d, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == vsa.VSA_ERR_INDEX
+    vsa.block_sparse_attention(q, q, q, idx, num, bs, T)
+    assert vsa.vsa_check_device_status() == vsa.VSA_ERR_INDEX
+    assert vsa.vsa_check_device_status() == 0          # the word is cleared by reading
+    ok = torch.tensor([[[[0, 1], [1, 2], [2, 3], [3, 0]]]], dtype=torch.int32, device=dev)
+    vsa.vsa_validate_indices(ok, num, bs, d, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+
+
+def test_layout_partial_and_bad_map(vsa, oracle_mod):
+    dev = "cuda"
+    r2t, bs, _, _ = W.video_cube_tiling((5, 6, 9), (2, 2, 4), 16)
+    S, NT = 5 * 6 * 9, int(bs.numel())
+    x = torch.randn((2, S, 3, 64)).to(torch.bfloat16)
+    (got, _, _) = vsa.tile_layout(x.to(dev), None, None, r2t.to(dev), NT, 16)
+    assert np.array_equal(_bits(got), oracle_mod.tile_layout(x, r2t, NT, 16))
+    assert vsa.vsa_check_device_status() == 0
+    bad = r2t.clone()
+    bad[3] = S + 5
+    vsa.tile_layout(x.to(dev), None, None, bad.to(dev), NT, 16)
+    assert vsa.vsa_check_device_status() == vsa.VSA_ERR_INDEX
