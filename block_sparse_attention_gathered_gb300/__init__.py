@@ -53,7 +53,7 @@ class VsaError(RuntimeError):
 def _load() -> ctypes.CDLL:
     if not os.path.exists(LIB_PATH):
         raise RuntimeError(f"libvsa.so is not built ({LIB_PATH}); run __graft_entry__.build() "
-                           "or python -m block_sparse_attention_gathered_gb300.build")
+                           "or python block_sparse_attention_gathered_gb300/build.py")
     lib = ctypes.CDLL(LIB_PATH)
     P, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
     dims_p = ctypes.POINTER(VsaDims)

@@ -22,8 +22,8 @@ pytestmark = pytest.mark.gpu
 def vsa():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
-    from block_sparse_attention_gathered_gb300 import build as B
-    B.build()
+    import __graft_entry__
+    __graft_entry__.build()
     import block_sparse_attention_gathered_gb300 as V
     assert V.vsa_check_device_status() == 0
     return V

@@ -19,8 +19,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 @pytest.fixture(scope="module")
 def vsa():
-    from block_sparse_attention_gathered_gb300 import build as B
-    B.build()
+    import __graft_entry__
+    __graft_entry__.build()
     import block_sparse_attention_gathered_gb300 as V
     return V
 
