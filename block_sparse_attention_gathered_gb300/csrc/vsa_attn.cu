@@ -504,9 +504,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                             for (int i = 0; i < 16; ++i) {
                                 const float p0 = ex2(fmaf(s[ch * 32 + 2 * i], c, neg_m));
                                 const float p1 = ex2(fmaf(s[ch * 32 + 2 * i + 1], c, neg_m));
-                                l0 += p0;
-                                l1 += p1;
                                 pk[i] = pack_bf16x2(p0, p1);
+                                // l sums the bf16 values P V actually uses, so the
+                                // weights P / l stay exactly normalised.
+                                l0 += __uint_as_float(pk[i] << 16);
+                                l1 += __uint_as_float(pk[i] & 0xffff0000u);
                             }
                             tmem_st16(tS + ch * 16, pk);
                         }

@@ -25,7 +25,6 @@ def gather_gpu_units(out: torch.Tensor, units, NT, T):
     """GPU tile-major output -> [n_units, T, D] float32 numpy (exact widening)."""
     B, H, Sp, D = out.shape
     flat = out.reshape(B * H, Sp, D)
-    idx = torch.tensor([bh for bh, _ in unit_rows(units, NT, T)], dtype=torch.long)
     tiles = torch.stack([flat[bh, t * T:(t + 1) * T] for bh, t in unit_rows(units, NT, T)])
     return tiles.float().cpu().numpy()
 
@@ -61,8 +60,7 @@ def assert_parity(gpu: np.ndarray, ref: np.ndarray, block_sizes, units, NT, T, g
         err = np.abs(g - r)
         mx = float(err.max())
         rel = float(np.linalg.norm(g - r) / max(np.linalg.norm(r), 1e-30))
-        assert mx <= MAX_ABS, f"{label}: max abs {mx:.3e}"
-        assert rel <= REL_RMS, f"{label}: rel rms {rel:.3e}"
+        assert mx <= MAX_ABS and rel <= REL_RMS, f"{label}: max abs {mx:.3e}, rel rms {rel:.3e}"
     if gpu_lse is not None:
         rl = ref_lse.astype(np.float32)
         assert np.isneginf(gpu_lse[~valid]).all(), f"{label}: padding lse not -inf"
