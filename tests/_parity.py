@@ -13,7 +13,13 @@ import torch
 
 MAX_ABS = 2e-2
 REL_RMS = 5e-3
+# LSE: the scores are accumulated in FP32 over D products, so their error grows
+# with the score's size (about D * 2^-24 * sum|q_d k_d|); bound it as an
+# absolute part plus a part relative to |lse|.
 LSE_ABS = 2e-3
+LSE_REL = 8e-6
+
+RESULTS = []  # (label, max_abs, rel_rms, lse_max_abs) of every passing comparison
 
 
 def unit_rows(units, NT, T):
@@ -68,8 +74,14 @@ def assert_parity(gpu: np.ndarray, ref: np.ndarray, block_sizes, units, NT, T, g
         np.testing.assert_array_equal(np.isnan(gpu_lse[valid]), np.isnan(rl[valid]))
         fin = valid & np.isfinite(rl)
         if fin.any():
-            d = float(np.abs(gpu_lse[fin].astype(np.float64) - rl[fin]).max())
-            assert d <= LSE_ABS, f"{label}: lse max abs {d:.3e}"
+            diff = np.abs(gpu_lse[fin].astype(np.float64) - rl[fin])
+            bound = LSE_ABS + LSE_REL * np.abs(rl[fin].astype(np.float64))
+            d = float(diff.max())
+            assert (diff <= bound).all(), f"{label}: lse max abs {d:.3e} (bound {float(bound.max()):.3e})"
+    if g.size:
+        RESULTS.append((label, mx, rel, d if gpu_lse is not None and fin.any() else None))
+        print(f"[parity] {label}: max abs {mx:.3e}, rel rms {rel:.3e}"
+              + (f", lse max abs {d:.3e}" if gpu_lse is not None and fin.any() else ""))
 
 
 def sample_units(B, H, NT, n, seed, must=()):
