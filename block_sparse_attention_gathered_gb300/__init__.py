@@ -60,6 +60,7 @@ def _load() -> ctypes.CDLL:
     sig = {
         "vsa_block_sparse_workspace_size": ([dims_p], sz),
         "vsa_block_sparse_fwd": ([P, P, P, P, P, P, P, P, dims_p, P, sz, P], i32),
+        "vsa_block_sparse_fwd_noalloc": ([P, P, P, P, P, P, P, P, dims_p, P], i32),
         "vsa_tile_layout": ([P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, P], i32),
         "vsa_validate_indices": ([P, P, P, dims_p, P, P], i32),
         "vsa_check_device_status": ([P], i32),
@@ -74,7 +75,8 @@ def _load() -> ctypes.CDLL:
 
 
 _lib = _load()
-EXPORTED = ("vsa_block_sparse_workspace_size", "vsa_block_sparse_fwd", "vsa_tile_layout",
+EXPORTED = ("vsa_block_sparse_workspace_size", "vsa_block_sparse_fwd", "vsa_block_sparse_fwd_noalloc",
+            "vsa_tile_layout",
             "vsa_validate_indices", "vsa_check_device_status", "vsa_last_route",
             "vsa_status_string", "vsa_version")
 
@@ -119,6 +121,21 @@ def vsa_block_sparse_fwd(q, k, v, q2k_idx, q2k_num, block_sizes, out, lse, dims:
                                    _stream(stream))
     if st != VSA_OK:
         raise VsaError(st, "vsa_block_sparse_fwd")
+
+
+VSA_NOALLOC_SCRATCH_BYTES = 1 << 20
+
+
+def vsa_block_sparse_fwd_noalloc(q, k, v, q2k_idx, q2k_num, block_sizes, out, lse, dims: VsaDims,
+                                 stream=None) -> None:
+    """The forward pass without a workspace, for callers that cannot allocate
+    device memory: the library's own fixed scratch array (1 MiB per GPU) is
+    used instead.  Calls on one device must not overlap on the GPU."""
+    st = _lib.vsa_block_sparse_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(q2k_idx), _ptr(q2k_num),
+                                           _ptr(block_sizes), _ptr(out), _ptr(lse), ctypes.byref(dims),
+                                           _stream(stream))
+    if st != VSA_OK:
+        raise VsaError(st, "vsa_block_sparse_fwd_noalloc")
 
 
 def vsa_tile_layout(q_tok, k_tok, v_tok, q_tile, k_tile, v_tile, row_to_token, B, S, H, D,

@@ -128,6 +128,36 @@ vsa_status vsa_block_sparse_fwd(const void *q, const void *k, const void *v, con
                                 size_t workspace_bytes, vsa_stream_t stream);
 
 /*
+ * Block-sparse attention forward for callers that cannot allocate device
+ * memory.  The paper has no counterpart to this entry point; it exists for
+ * this library's users.
+ *
+ * Same arguments, layouts and results as vsa_block_sparse_fwd, without the
+ * workspace: the scratch it needs lives in a fixed array inside the library
+ * (VSA_NOALLOC_SCRATCH_BYTES bytes of device memory, held by every GPU that
+ * loads the library until the process exits).  Useful where cudaMalloc is not
+ * available to the caller -- host callbacks, plug-ins whose device memory is
+ * owned by a host framework, or code that must keep a fixed footprint.
+ *
+ *   - Problems needing more scratch than the array holds (more than
+ *     (VSA_NOALLOC_SCRATCH_BYTES - 256) / 4 work items of 256 query rows)
+ *     return VSA_ERR_LIMITS before anything is launched.
+ *   - The first call on a device looks up the array's device address; make
+ *     that first call before any stream capture on the device.
+ *   - Calls allocate nothing (no cudaMalloc / cudaFree).  Every call on a
+ *     device shares the one array: calls that may run concurrently on the GPU
+ *     race on it and must be ordered by the caller (one stream, or events).
+ *     Each call rewrites the array's contents before use, so results never
+ *     depend on an earlier call.
+ */
+#define VSA_NOALLOC_SCRATCH_BYTES (1u << 20)
+
+vsa_status vsa_block_sparse_fwd_noalloc(const void *q, const void *k, const void *v,
+                                        const int32_t *q2k_idx, const int32_t *q2k_num,
+                                        const int32_t *block_sizes, void *out, float *lse,
+                                        const vsa_dims *dims, vsa_stream_t stream);
+
+/*
  * Fused tile layout (fused tile_to_bhsd commit): one pass over up to three
  * tensors that gathers token-major rows into tile-major order.
  *
