@@ -42,7 +42,10 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes (read + write) per attention launch from an ncu capture, keyed by
 # the SHA-256 of the attention kernel source the capture was taken with; a
 # changed kernel reports null until it is captured again.
-ATTN_TRAFFIC = {}
+ATTN_TRAFFIC = {
+    # profiles/attn_fwd_t128d128_dense_b1h6_s31200.md: 345.5 MB read + 38.8 MB written
+    ("dense_b1h6d128_s31200_t128x244_lse", "6b166f4f356a13be"): 384.27e6,
+}
 
 
 def _rank_env():
