@@ -14,18 +14,29 @@
 //   * The producer warp turns the selections of the item's tiles into
 //     shared-memory bitmaps and streams the UNION of the selected key tiles,
 //     in ascending order, through a ring of K/V stages with TMA, so a key
-//     tile that both units select is fetched once ("gathered" fetch).
-//   * The MMA warp issues S_u = Q_u K_j^T (tcgen05, smem x smem -> TMEM) for
-//     the units that select j, and O_u += P_u V_j with P read from TMEM.
+//     tile that both units select is fetched once ("gathered" fetch).  The
+//     ring is as deep as shared memory allows.
+//   * One MMA-issuing warp per unit issues S_u = Q_u K_j^T (tcgen05, smem x
+//     smem -> TMEM) for the key tiles the unit selects, and O_u += P_u V_j
+//     with P read from TMEM.  tcgen05.mma issue runs only ~2 instructions
+//     ahead of execution and every barrier wait costs the issuing thread
+//     ~100 cycles, so two issuers let one warp's waits overlap the other's
+//     issue; descriptors are precomputed and advanced by constant offsets.
 //   * Two softmax warpgroups, one per unit, run the online softmax with exp2
 //     on their TMEM rows (one thread per query row), write P (bf16) into the
 //     TMEM columns of S, rescale O only when the running maximum grows by more
 //     than 2^8 (lazy rescale), and finish with O / l.  The two units
 //     ping-pong: the tensor core works on one unit while the other's softmax
-//     runs.
-//   * Masks are applied only on tail key tiles (valid count < tile); the V
-//     rows past the valid count of a tail tile are zeroed in shared memory
-//     before P V, so NaN/Inf padding cannot reach the output (0 * NaN = NaN).
+//     runs.  The row maximum uses 3-input max, the exponent argument a packed
+//     f32x2 FMA, and l accumulates the bf16-rounded P that P V uses.
+//   * Masks are applied only on tail key tiles (valid count < tile).  For a
+//     tail tile P V runs only over the 16-key blocks that hold valid keys, and
+//     a fix-up warp zeroes the few padding rows inside the last block in
+//     shared memory first, so NaN/Inf padding in V never meets a zero weight
+//     (0 * NaN = NaN).
+//   * 12 warps: two softmax warpgroups, then a control warpgroup (two MMA
+//     issuers, the TMA producer, the V fix-up warp) that hands registers to
+//     the softmax warpgroups with setmaxnreg.
 //   * Every wait is bounded (about 2 s); on expiry the CTA sets the timeout
 //     flag, drains its outstanding copies and MMAs, frees TMEM and returns.
 #include <cuda_bf16.h>
@@ -39,8 +50,18 @@ namespace {
 using namespace ptx;
 
 constexpr int kSoftmaxWarps = 8;
-constexpr int kMmaWarp = 8;
-constexpr int kProducerWarp = 9;
+constexpr int kMmaWarp0 = 8;      // MMA issuer of unit 0; kMmaWarp0 + 1 issues for unit 1
+constexpr int kProducerWarp = 10;
+constexpr int kFixupWarp = 11;    // zeroes V padding rows of tail key tiles
+constexpr int kMaxStages = 8;
+// Register split per tile size (control warpgroup, softmax warpgroups); both
+// sum to the 384 x 168 registers the CTA is launched with.
+template <int T> struct RegSplit {
+    static constexpr uint32_t kControl = T == 128 ? 80 : 104;
+    static constexpr uint32_t kSoftmax = T == 128 ? 208 : 200;
+    static_assert(128 * kControl + 256 * kSoftmax <= kAttnThreads * 168, "register split");
+};
+constexpr uint32_t kSmemLimit = 232448;  // 227 KB opt-in per CTA
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when the max grows by > 2^8
 
@@ -52,7 +73,9 @@ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major) {
 }
 
 // Shared-memory matrix descriptor, 128-byte swizzle (rows of 128 bytes,
-// 8-row / 1024-byte swizzle atoms; buffers are 1024-byte aligned).
+// 8-row / 1024-byte swizzle atoms; buffers are 1024-byte aligned).  The start
+// address sits in the low 14 bits (address >> 4), so a byte offset b is added
+// to a descriptor as b >> 4.
 __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
     return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
            ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
@@ -67,16 +90,27 @@ struct Cfg {
     static constexpr uint32_t kQBytes = kUnitRows * D * 2;    // one unit's Q
     static constexpr uint32_t kKVChunk = T * 128;             // bytes of one K/V column chunk
     static constexpr uint32_t kStageBytes = T * D * 2;        // one K or V tile
-    static constexpr int kStages = kStageBytes >= 32768 ? 4 : 8;
     static constexpr uint32_t kTmemO0 = 0, kTmemO1 = D, kTmemS0 = 2 * D, kTmemS1 = 2 * D + T;
     static constexpr uint32_t kTmemCols = (2 * D + 2 * T <= 256) ? 256 : 512;
     static constexpr uint32_t kIdescQK = idesc_bf16(128, T, false);
     static constexpr uint32_t kIdescPV = idesc_bf16(128, D, true);
-    // barrier indices
-    static constexpr int kKvFull = 0, kKvEmpty = kStages, kQFull = 2 * kStages, kQEmpty = kQFull + 2,
-                         kSFull = kQEmpty + 2, kPFull = kSFull + 2, kODone = kPFull + 2,
-                         kBmFull = kODone + 2, kBmEmpty = kBmFull + 2, kDone = kBmEmpty + 2,
-                         kNumBars = kDone + 1;
+};
+
+// Barrier indices for a ring of NS stages.
+struct Bars {
+    int NS;
+    __host__ __device__ int kv_full(int s) const { return s; }
+    __host__ __device__ int kv_empty(int s) const { return NS + s; }
+    __host__ __device__ int vz(int s) const { return 2 * NS + s; }  // tail V rows zeroed
+    __host__ __device__ int q_full(int u) const { return 3 * NS + u; }
+    __host__ __device__ int q_empty(int u) const { return 3 * NS + 2 + u; }
+    __host__ __device__ int s_full(int u) const { return 3 * NS + 4 + u; }
+    __host__ __device__ int p_full(int u) const { return 3 * NS + 6 + u; }
+    __host__ __device__ int o_done(int u) const { return 3 * NS + 8 + u; }
+    __host__ __device__ int bm_full(int p) const { return 3 * NS + 10 + p; }
+    __host__ __device__ int bm_empty(int p) const { return 3 * NS + 12 + p; }
+    __host__ __device__ int done(int u) const { return 3 * NS + 14 + u; }
+    __host__ __device__ int count() const { return 3 * NS + 16; }
 };
 
 struct SmemPlan {
@@ -84,19 +118,37 @@ struct SmemPlan {
 };
 
 template <int T, int D>
-__host__ __device__ inline SmemPlan smem_plan(int bm_words) {
+__host__ __device__ inline SmemPlan smem_plan(int bm_words, int NS) {
     using C = Cfg<T, D>;
     SmemPlan s;
     s.q = 0;
     s.ring = 2 * C::kQBytes;
-    s.bm = s.ring + C::kStages * C::kStageBytes;
+    s.bm = s.ring + (uint32_t)NS * C::kStageBytes;
     s.hdr = s.bm + 2u * 4u * 4u * (uint32_t)bm_words;
     s.bars = s.hdr + 32;
-    s.tslot = s.bars + 8u * C::kNumBars;
+    s.tslot = s.bars + 8u * (uint32_t)Bars{NS}.count();
     s.flag = s.tslot + 4;
     s.total = ((s.flag + 4 + 15) & ~15u) + 1024;  // + slack to align the base to 1024
     return s;
 }
+
+template <int T, int D>
+inline int stages_for(int bm_words) {
+    int ns = kMaxStages;
+    while (ns > 2 && smem_plan<T, D>(bm_words, ns).total > kSmemLimit) --ns;
+    return ns;
+}
+
+// Ring position: stage index and the parity of its current fill.
+struct Ring {
+    uint32_t st = 0, ph = 0;
+    __device__ __forceinline__ void next(uint32_t ns) {
+        if (++st == ns) {
+            st = 0;
+            ph ^= 1u;
+        }
+    }
+};
 
 // Bounded wait on an mbarrier phase.  Returns false when the CTA is aborting
 // (another role gave up) or when this wait itself ran past the limit.
@@ -149,16 +201,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const AttnParams P) {
     using C = Cfg<T, D>;
-    constexpr int NS = C::kStages;
+    const int NS = P.stages;
+    const Bars BI{NS};
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t *gbase = smem_raw + (base - raw);
     const int W = P.bm_words;
-    const SmemPlan L = smem_plan<T, D>(W);
+    const SmemPlan L = smem_plan<T, D>(W, NS);
     const uint32_t sQ = base + L.q;
     const uint32_t sRing = base + L.ring;
-    uint32_t *bm = reinterpret_cast<uint32_t *>(gbase + L.bm);       // [2][4][W]
+    uint32_t *bm = reinterpret_cast<uint32_t *>(gbase + L.bm);           // [2][4][W]
     volatile int32_t *hdr = reinterpret_cast<int32_t *>(gbase + L.hdr);  // [2][4]
     const uint32_t bars = base + L.bars;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(gbase + L.tslot);
@@ -170,24 +223,26 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NS; ++s) {
-            mbar_init(BAR(C::kKvFull + s), 1);
-            mbar_init(BAR(C::kKvEmpty + s), 1);
+            mbar_init(BAR(BI.kv_full(s)), 1);
+            mbar_init(BAR(BI.kv_empty(s)), 2);  // both MMA issuers release every fill
+            mbar_init(BAR(BI.vz(s)), 32);
         }
+        #pragma unroll
         for (int u = 0; u < 2; ++u) {
-            mbar_init(BAR(C::kQFull + u), 1);
-            mbar_init(BAR(C::kQEmpty + u), 1);
-            mbar_init(BAR(C::kSFull + u), 1);
-            mbar_init(BAR(C::kPFull + u), 128);
-            mbar_init(BAR(C::kODone + u), 1);
-            mbar_init(BAR(C::kBmFull + u), 32);
-            mbar_init(BAR(C::kBmEmpty + u), 32 + 32 * kSoftmaxWarps);
+            mbar_init(BAR(BI.q_full(u)), 1);
+            mbar_init(BAR(BI.q_empty(u)), 1);
+            mbar_init(BAR(BI.s_full(u)), 1);
+            mbar_init(BAR(BI.p_full(u)), 128);
+            mbar_init(BAR(BI.o_done(u)), 1);
+            mbar_init(BAR(BI.bm_full(u)), 32);
+            mbar_init(BAR(BI.bm_empty(u)), 3 * 32 + 32 * kSoftmaxWarps);
+            mbar_init(BAR(BI.done(u)), 1);
         }
-        mbar_init(BAR(C::kDone), 1);
         *abort_flag = 0;
         fence_mbar_init();
         fence_proxy_async_smem();
     }
-    if (warp == kMmaWarp) {
+    if (warp == kMmaWarp0) {
         tmem_alloc(smem_u32(tslot), C::kTmemCols);
         tmem_relinquish();
     }
@@ -204,15 +259,22 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const int NT = P.NT;
     const int64_t Sp = P.Sp;
 
-    if (warp == kProducerWarp) {
+    // Registers: launched at 168 per thread (384 threads); the control
+    // warpgroup (MMA issuers, producer, fix-up) keeps RegSplit::kControl and
+    // the two softmax warpgroups take RegSplit::kSoftmax.  Each re-split sits inside its own
+    // role branch so no code of one role runs under the other's limit.
+    if (warp >= kSoftmaxWarps) {
+      regs_dec<RegSplit<T>::kControl>();
+      if (warp == kProducerWarp) {
         // ------------------------------------------------------------ producer
         const uint64_t pol_kv = l2_policy_evict_last();
         const uint64_t pol_q = l2_policy_evict_first();
+        Ring ring;
         uint32_t fills = 0;
         uint32_t q_loads = 0;
         for (uint32_t it = 0;; ++it) {
             const int p = it & 1;
-            if (!wait_warp(BAR(C::kBmEmpty + p), ((it >> 1) & 1u) ^ 1u, abort_flag, P.status)) break;
+            if (!wait_warp(BAR(BI.bm_empty(p)), ((it >> 1) & 1u) ^ 1u, abort_flag, P.status)) break;
             int slot = 0;
             if (lane == 0) slot = atomicAdd(P.work_counter, 1);
             slot = __shfl_sync(0xffffffffu, slot, 0);
@@ -251,19 +313,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             }
             if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(P.status, kFlagIndex);
             __syncwarp();
-            mbar_arrive(BAR(C::kBmFull + p));
+            mbar_arrive(BAR(BI.bm_full(p)));
             if (item < 0) break;
 
             const int bh = item / P.G, g = item - (item / P.G) * P.G;
             const int64_t row0 = (int64_t)bh * Sp + (int64_t)g * kItemRows;
             bool ok = true;
+            #pragma unroll
             for (int u = 0; u < 2 && ok; ++u) {
-                ok = wait_warp(BAR(C::kQEmpty + u), (it & 1u) ^ 1u, abort_flag, P.status);
+                ok = wait_warp(BAR(BI.q_empty(u)), (it & 1u) ^ 1u, abort_flag, P.status);
                 if (ok && lane == 0) {
-                    mbar_arrive_expect_tx(BAR(C::kQFull + u), C::kQBytes);
+                    mbar_arrive_expect_tx(BAR(BI.q_full(u)), C::kQBytes);
                     for (int c = 0; c < C::kChunks; ++c)
                         tma_load_2d(sQ + u * C::kQBytes + c * C::kQChunk, &tm_q, c * 64,
-                                    (int32_t)(row0 + u * kUnitRows), BAR(C::kQFull + u), pol_q);
+                                    (int32_t)(row0 + u * kUnitRows), BAR(BI.q_full(u)), pol_q);
                 }
             }
             if (!ok) break;
@@ -275,17 +338,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     bits &= bits - 1;
                     const int32_t krow = (int32_t)((int64_t)bh * Sp + (int64_t)j * T);
                     for (int kv = 0; kv < 2; ++kv) {
-                        const int st = fills % NS;
-                        ok = wait_warp(BAR(C::kKvEmpty + st), ((fills / NS) & 1u) ^ 1u, abort_flag, P.status);
+                        const uint32_t st = ring.st;
+                        ok = wait_warp(BAR(BI.kv_empty(st)), ring.ph ^ 1u, abort_flag, P.status);
                         if (!ok) break;
                         if (lane == 0) {
-                            mbar_arrive_expect_tx(BAR(C::kKvFull + st), C::kStageBytes);
+                            mbar_arrive_expect_tx(BAR(BI.kv_full(st)), C::kStageBytes);
                             for (int c = 0; c < C::kChunks; ++c)
                                 tma_load_2d(sRing + st * C::kStageBytes + c * C::kKVChunk,
                                             kv ? (const void *)&tm_v : (const void *)&tm_k, c * 64, krow,
-                                            BAR(C::kKvFull + st), pol_kv);
+                                            BAR(BI.kv_full(st)), pol_kv);
                         }
                         __syncwarp();
+                        ring.next(NS);
                         ++fills;
                     }
                 }
@@ -297,129 +361,175 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         // this drains whatever is still in flight.
         if (*abort_flag && lane == 0) {
             const uint32_t first = fills > (uint32_t)NS ? fills - NS : 0u;
-            for (uint32_t f = first; f < fills; ++f) drain_wait(BAR(C::kKvFull + f % NS), (f / NS) & 1u);
+            for (uint32_t f = first; f < fills; ++f)
+                drain_wait(BAR(BI.kv_full(f % NS)), (f / NS) & 1u);
             if (q_loads > 0)
-                for (int u = 0; u < 2; ++u) drain_wait(BAR(C::kQFull + u), (q_loads - 1) & 1u);
+                #pragma unroll
+                for (int u = 0; u < 2; ++u) drain_wait(BAR(BI.q_full(u)), (q_loads - 1) & 1u);
         }
         __syncwarp();
-    } else if (warp == kMmaWarp) {
-        // ------------------------------------------------------------ MMA issuer
-        uint32_t fills = 0;
-        uint32_t pcnt[2] = {0u, 0u};
+      } else if (warp == kFixupWarp) {
+        // ------------------------------------------------------------ tail V fix-up
+        // For a tail key tile (valid count not a multiple of 16) P V reads the
+        // last 16-key block, whose padding rows may hold NaN/Inf: zero them
+        // (rows of 128 bytes; the swizzle permutes 16-byte chunks within a row
+        // only) once the tile has landed, then release the MMA issuers.
+        Ring ring;
+        for (uint32_t it = 0;; ++it) {
+            const int p = it & 1;
+            if (!wait_warp(BAR(BI.bm_full(p)), (it >> 1) & 1u, abort_flag, P.status)) break;
+            if (hdr[p * 4] < 0) break;
+            const uint32_t *bmp = bm + p * 4 * W;
+            bool ok = true;
+            for (int w = 0; w < W && ok; ++w) {
+                uint32_t bits = bmp[w] | bmp[W + w] | bmp[2 * W + w] | bmp[3 * W + w];
+                while (bits) {
+                    const int j = w * 32 + __ffs(bits) - 1;
+                    bits &= bits - 1;
+                    const uint32_t kst = ring.st, kph = ring.ph;
+                    ring.next(NS);
+                    const uint32_t vst = ring.st, vph = ring.ph;
+                    ring.next(NS);
+                    // Wait for every fill in order, like the MMA issuers: a parity
+                    // wait is only meaningful when the waiter is never a whole ring
+                    // cycle ahead of the fills it waits for.
+                    if (!(ok = wait_warp(BAR(BI.kv_full(kst)), kph, abort_flag, P.status))) break;
+                    if (!(ok = wait_warp(BAR(BI.kv_full(vst)), vph, abort_flag, P.status))) break;
+                    const int nj = __ldg(P.block_sizes + j);
+                    if ((nj & 15) == 0) continue;
+                    uint4 *vs = reinterpret_cast<uint4 *>(gbase + L.ring + vst * C::kStageBytes);
+                    const int n16 = (16 - (nj & 15)) * 8;
+#pragma unroll
+                    for (int c = 0; c < C::kChunks; ++c)
+                        for (int i = lane; i < n16; i += 32)
+                            vs[(c * C::kKVChunk + nj * 128) / 16 + i] = make_uint4(0u, 0u, 0u, 0u);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    mbar_arrive(BAR(BI.vz(vst)));
+                }
+            }
+            if (!ok) break;
+            __syncwarp();
+            mbar_arrive(BAR(BI.bm_empty(p)));
+        }
+      } else {
+        // ------------------------------------------------------------ MMA issuers
+        // Warp kMmaWarp0 + u issues every MMA of unit u: S_u = Q_u K_j^T and
+        // O_u += P_u V_j.  Two issuers let one warp's barrier waits overlap the
+        // other's MMA issue (tcgen05.mma issue runs only ~2 instructions ahead).
+        const int u = warp - kMmaWarp0;
+        Ring ring;
+        uint32_t pcnt = 0;
+        uint32_t vz_par = 0;  // per stage: parity of its next tail-zeroing phase
+        const uint64_t dq = sdesc_sw128(sQ + u * C::kQBytes, 16, 1024);  // Q_u, K-major
+        const uint64_t dk = sdesc_sw128(sRing, 16, 1024);                // stage 0 as K-major B
+        const uint64_t dv = sdesc_sw128(sRing, C::kKVChunk, 1024);       // stage 0 as MN-major B
+        constexpr uint32_t kStage16 = C::kStageBytes >> 4;
+        const uint32_t tS = tmem + (u ? C::kTmemS1 : C::kTmemS0);
+        const uint32_t tO = tmem + (u ? C::kTmemO1 : C::kTmemO0);
         bool ok = true;
         for (uint32_t it = 0; ok; ++it) {
             const int p = it & 1;
-            if (!(ok = wait_warp(BAR(C::kBmFull + p), (it >> 1) & 1u, abort_flag, P.status))) break;
-            const int item = hdr[p * 4];
-            if (item < 0) break;
+            if (!(ok = wait_warp(BAR(BI.bm_full(p)), (it >> 1) & 1u, abort_flag, P.status))) break;
+            if (hdr[p * 4] < 0) break;
             const uint32_t *bmp = bm + p * 4 * W;
-            ok = wait_warp(BAR(C::kQFull + 0), it & 1u, abort_flag, P.status) &&
-                 wait_warp(BAR(C::kQFull + 1), it & 1u, abort_flag, P.status);
-            if (!ok) break;
+            const uint32_t *pa = bmp + (2 * u) * W, *pb = pa + W;
+            // member entries of this unit, so Q can be released right after its last S
+            uint32_t n_mine = 0;
+            for (int w = lane; w < W; w += 32) n_mine += __popc(pa[w] | pb[w]);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) n_mine += __shfl_xor_sync(0xffffffffu, n_mine, o);
+            if (!(ok = wait_warp(BAR(BI.q_full(u)), it & 1u, abort_flag, P.status))) break;
             tc_fence_after();
-            bool pending[2] = {false, false};
-            bool first[2] = {true, true};
-            uint32_t pend_v[2] = {0u, 0u};
+            bool pending = false, first = true;
+            uint32_t pend_v = 0, pend_ph = 0;
+            int pend_kb = 0;
+            bool pend_tail = false;
+            uint32_t seen = 0;
 
-            // O_u += P_u V (the V stage of u's previous member entry).
-            auto flush = [&](int u) -> bool {
-                if (!wait_warp(BAR(C::kPFull + u), pcnt[u] & 1u, abort_flag, P.status)) return false;
-                ++pcnt[u];
+            // O_u += P_u V over the 16-key blocks of the previous member entry;
+            // then this issuer's release of that V stage.
+            auto flush = [&]() -> bool {
+                if (!wait_warp(BAR(BI.p_full(u)), pcnt & 1u, abort_flag, P.status)) return false;
+                ++pcnt;
+                if (!wait_warp(BAR(pend_tail ? BI.vz(pend_v) : BI.kv_full(pend_v)), pend_ph, abort_flag, P.status))
+                    return false;
                 tc_fence_after();
                 if (lane == 0) {
-                    const uint32_t d = tmem + (u ? C::kTmemO1 : C::kTmemO0);
-                    const uint32_t a = tmem + (u ? C::kTmemS1 : C::kTmemS0);
-                    const uint32_t vb = sRing + pend_v[u] * C::kStageBytes;
+                    const uint64_t b = dv + pend_v * kStage16;
+                    mma_ts(tO, tS, b, C::kIdescPV, first ? 0u : 1u);
 #pragma unroll
-                    for (int kk = 0; kk < T / 16; ++kk) {
-                        const uint64_t bdesc = sdesc_sw128(vb + kk * 16 * 128, C::kKVChunk, 1024);
-                        mma_ts(d, a + kk * 8, bdesc, C::kIdescPV, (first[u] && kk == 0) ? 0u : 1u);
-                    }
-                    mma_commit(BAR(C::kODone + u));
-                    const int o = 1 - u;
-                    if (!(pending[o] && pend_v[o] == pend_v[u])) mma_commit(BAR(C::kKvEmpty + pend_v[u]));
+                    for (int kk = 1; kk < T / 16; ++kk)
+                        if (kk < pend_kb) mma_ts(tO, tS + kk * 8, b + kk * 128, C::kIdescPV, 1u);
+                    mma_commit(BAR(BI.o_done(u)));
+                    mma_commit(BAR(BI.kv_empty(pend_v)));
                 }
                 __syncwarp();
-                first[u] = false;
-                pending[u] = false;
+                first = false;
+                pending = false;
                 return true;
             };
 
             for (int w = 0; w < W && ok; ++w) {
-                const uint32_t m0w = bmp[w] | bmp[W + w];
-                const uint32_t m1w = bmp[2 * W + w] | bmp[3 * W + w];
-                uint32_t bits = m0w | m1w;
+                const uint32_t mw = pa[w] | pb[w];
+                uint32_t bits = bmp[w] | bmp[W + w] | bmp[2 * W + w] | bmp[3 * W + w];
                 while (bits && ok) {
                     const int b = __ffs(bits) - 1;
                     bits &= bits - 1;
                     const int j = w * 32 + b;
-                    const bool mem[2] = {((m0w >> b) & 1u) != 0u, ((m1w >> b) & 1u) != 0u};
-                    const uint32_t kst = fills % NS, kph = (fills / NS) & 1u;
-                    ++fills;
-                    const uint32_t vst = fills % NS, vph = (fills / NS) & 1u;
-                    ++fills;
-                    if (!(ok = wait_warp(BAR(C::kKvFull + kst), kph, abort_flag, P.status))) break;
-                    tc_fence_after();
-                    for (int u = 0; u < 2 && ok; ++u) {
-                        if (!mem[u]) continue;
-                        if (pending[u] && !(ok = flush(u))) break;
+                    const uint32_t kst = ring.st, kph = ring.ph;
+                    ring.next(NS);
+                    const uint32_t vst = ring.st, vph = ring.ph;
+                    ring.next(NS);
+                    const int nj = __ldg(P.block_sizes + j);
+                    const bool tail = (nj & 15) != 0;
+                    const uint32_t vzp = (vz_par >> vst) & 1u;
+                    if (tail) vz_par ^= 1u << vst;
+                    // the previous PV frees a V stage: issue it first, member or not
+                    if (pending && !(ok = flush())) break;
+                    if (!(ok = wait_warp(BAR(BI.kv_full(kst)), kph, abort_flag, P.status))) break;
+                    if ((mw >> b) & 1u) {
+                        tc_fence_after();
                         if (lane == 0) {
-                            const uint32_t d = tmem + (u ? C::kTmemS1 : C::kTmemS0);
-                            const uint32_t qb = sQ + u * C::kQBytes;
-                            const uint32_t kb = sRing + kst * C::kStageBytes;
 #pragma unroll
-                            for (int kk = 0; kk < D / 16; ++kk) {
-                                const uint32_t off = (kk & 3) * 32u;  // K16 slice inside the 128-byte row
-                                const uint64_t ad = sdesc_sw128(qb + (kk >> 2) * C::kQChunk + off, 16, 1024);
-                                const uint64_t bd = sdesc_sw128(kb + (kk >> 2) * C::kKVChunk + off, 16, 1024);
-                                mma_ss(d, ad, bd, C::kIdescQK, kk > 0 ? 1u : 0u);
-                            }
-                            mma_commit(BAR(C::kSFull + u));
+                            for (int kk = 0; kk < D / 16; ++kk)
+                                mma_ss(tS, dq + (kk >> 2) * (C::kQChunk >> 4) + (kk & 3) * 2,
+                                       dk + kst * kStage16 + (kk >> 2) * (C::kKVChunk >> 4) + (kk & 3) * 2,
+                                       C::kIdescQK, kk > 0 ? 1u : 0u);
+                            mma_commit(BAR(BI.s_full(u)));
+                            if (++seen == n_mine) mma_commit(BAR(BI.q_empty(u)));
+                            mma_commit(BAR(BI.kv_empty(kst)));
                         }
                         __syncwarp();
+                        pending = true;
+                        pend_v = vst;
+                        pend_ph = tail ? vzp : vph;
+                        pend_kb = (nj + 15) >> 4;
+                        pend_tail = tail;
+                    } else {
+                        // not selected by this unit: release both stages of the entry
+                        if (lane == 0) mbar_arrive(BAR(BI.kv_empty(kst)));
+                        if (!(ok = wait_warp(BAR(BI.kv_full(vst)), vph, abort_flag, P.status))) break;
+                        if (lane == 0) mbar_arrive(BAR(BI.kv_empty(vst)));
+                        __syncwarp();
                     }
-                    for (int u = 0; u < 2 && ok; ++u)
-                        if (!mem[u] && pending[u]) ok = flush(u);
-                    if (!ok) break;
-                    if (lane == 0) mma_commit(BAR(C::kKvEmpty + kst));
-                    __syncwarp();
-                    if (!(ok = wait_warp(BAR(C::kKvFull + vst), vph, abort_flag, P.status))) break;
-                    const int nj = __ldg(P.block_sizes + j);
-                    if (nj < T) {
-                        // Zero the V rows past the valid count so 0 * NaN never
-                        // enters P V (rows of 128 bytes; the swizzle stays in-row).
-                        uint4 *vs = reinterpret_cast<uint4 *>(gbase + L.ring + vst * C::kStageBytes);
-                        const int n16 = (T - nj) * 8;
-                        for (int c = 0; c < C::kChunks; ++c)
-                            for (int i = lane; i < n16; i += 32)
-                                vs[(c * C::kKVChunk + nj * 128) / 16 + i] = make_uint4(0u, 0u, 0u, 0u);
-                        fence_proxy_async_smem();
-                    }
-                    __syncwarp();
-                    for (int u = 0; u < 2; ++u)
-                        if (mem[u]) {
-                            pending[u] = true;
-                            pend_v[u] = vst;
-                        }
                 }
             }
-            for (int u = 0; u < 2 && ok; ++u)
-                if (pending[u]) ok = flush(u);
+            if (ok && pending) ok = flush();
             if (!ok) break;
-            if (lane == 0) {
-                mma_commit(BAR(C::kQEmpty + 0));
-                mma_commit(BAR(C::kQEmpty + 1));
-            }
+            if (lane == 0 && n_mine == 0) mma_commit(BAR(BI.q_empty(u)));  // no S issued: release Q
             __syncwarp();
-            mbar_arrive(BAR(C::kBmEmpty + p));
+            mbar_arrive(BAR(BI.bm_empty(p)));
         }
-        // All MMAs of this CTA complete before TMEM is released.
+        // All MMAs of this issuer complete before TMEM is released.
         if (lane == 0) {
-            mma_commit(BAR(C::kDone));
-            drain_wait(BAR(C::kDone), 0u);
+            mma_commit(BAR(BI.done(u)));
+            drain_wait(BAR(BI.done(u)), 0u);
         }
         __syncwarp();
+      }
     } else {
+        regs_inc<RegSplit<T>::kSoftmax>();
         // ------------------------------------------------------------ softmax
         const int u = warp >> 2;
         const int q4 = warp & 3;
@@ -432,7 +542,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         uint32_t cnt = 0;  // member entries of this unit seen so far (all items)
         for (uint32_t it = 0;; ++it) {
             const int p = it & 1;
-            if (!wait_warp(BAR(C::kBmFull + p), (it >> 1) & 1u, abort_flag, P.status)) break;
+            if (!wait_warp(BAR(BI.bm_full(p)), (it >> 1) & 1u, abort_flag, P.status)) break;
             const int item = hdr[p * 4];
             if (item < 0) break;
             const uint32_t *bmp = bm + p * 4 * W;
@@ -440,7 +550,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             const int t = (T == 128) ? 2 * g + u : 4 * g + 2 * u + half;
             const int r = (T == 128) ? row : (row & 63);
             const int n_t = (t < NT) ? __ldg(P.block_sizes + t) : 0;
-            float m = -INFINITY, l = 0.f;
+            float m = -INFINITY, l0 = 0.f, l1 = 0.f;
             uint32_t n_mine = 0;
             bool ok = true;
             const uint32_t *pa = bmp + (2 * u) * W, *pb = bmp + (2 * u + 1) * W;
@@ -452,7 +562,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     const int b = __ffs(bits) - 1;
                     bits &= bits - 1;
                     const int j = w * 32 + b;
-                    if (!(ok = wait_warp(BAR(C::kSFull + u), cnt & 1u, abort_flag, P.status))) break;
+                    if (!(ok = wait_warp(BAR(BI.s_full(u)), cnt & 1u, abort_flag, P.status))) break;
                     tc_fence_after();
                     if ((mine >> b) & 1u) {
                         const int nj = __ldg(P.block_sizes + j);
@@ -464,22 +574,22 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                             for (int i = 0; i < T; ++i)
                                 if (i >= nj) s[i] = -INFINITY;
                         }
-                        float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+                        float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
 #pragma unroll
-                        for (int i = 4; i < T; i += 4) {
-                            mx0 = fmaxf(mx0, s[i]);
-                            mx1 = fmaxf(mx1, s[i + 1]);
-                            mx2 = fmaxf(mx2, s[i + 2]);
-                            mx3 = fmaxf(mx3, s[i + 3]);
+                        for (int i = 0; i < T; i += 8) {
+                            a0 = max3(a0, s[i], s[i + 1]);
+                            a1 = max3(a1, s[i + 2], s[i + 3]);
+                            a2 = max3(a2, s[i + 4], s[i + 5]);
+                            a3 = max3(a3, s[i + 6], s[i + 7]);
                         }
-                        const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c;
+                        const float mx = max3(a0, a1, fmaxf(a2, a3)) * c;
                         const float m_new = fmaxf(m, mx);
                         const bool fresh = (m == -INFINITY);
                         const bool resc = !fresh && (m_new > m + kRescaleThreshold);
                         if (__any_sync(0xffffffffu, resc)) {
                             // O of this unit holds the sum up to the previous
                             // entry once that PV completes.
-                            if (!(ok = wait_warp(BAR(C::kODone + u), (cnt - 1u) & 1u, abort_flag, P.status)))
+                            if (!(ok = wait_warp(BAR(BI.o_done(u)), (cnt - 1u) & 1u, abort_flag, P.status)))
                                 break;
                             tc_fence_after();
                             const float alpha = resc ? ex2(m - m_new) : 1.f;
@@ -492,27 +602,25 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                                 tmem_st32(tO + ch * 32, o);
                             }
                             tmem_wait_st();
-                            l *= alpha;
+                            l0 *= alpha;
+                            l1 *= alpha;
                         }
                         if (fresh || resc) m = m_new;
                         const float neg_m = -m;
-                        float l0 = 0.f, l1 = 0.f;
 #pragma unroll
                         for (int ch = 0; ch < T / 32; ++ch) {
                             uint32_t pk[16];
 #pragma unroll
                             for (int i = 0; i < 16; ++i) {
-                                const float p0 = ex2(fmaf(s[ch * 32 + 2 * i], c, neg_m));
-                                const float p1 = ex2(fmaf(s[ch * 32 + 2 * i + 1], c, neg_m));
-                                pk[i] = pack_bf16x2(p0, p1);
-                                // l sums the bf16 values P V actually uses, so the
-                                // weights P / l stay exactly normalised.
-                                l0 += __uint_as_float(pk[i] << 16);
-                                l1 += __uint_as_float(pk[i] & 0xffff0000u);
+                                float x0, x1;
+                                fma2_scalar(x0, x1, s[ch * 32 + 2 * i], s[ch * 32 + 2 * i + 1], c, neg_m);
+                                pk[i] = pack_bf16x2(ex2(x0), ex2(x1));
+                                // l sums the bf16 values P V actually uses, so
+                                // the weights P / l stay exactly normalised.
+                                add_bf16x2_f32(l0, l1, pk[i]);
                             }
                             tmem_st16(tS + ch * 16, pk);
                         }
-                        l += l0 + l1;
                     } else {
                         // This half of the unit does not select tile j: its P
                         // rows are zero so O is left unchanged.
@@ -523,7 +631,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     }
                     tmem_wait_st();
                     tc_fence_before();
-                    mbar_arrive(BAR(C::kPFull + u));
+                    mbar_arrive(BAR(BI.p_full(u)));
                     ++cnt;
                     ++n_mine;
                 }
@@ -531,9 +639,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             if (!ok) break;
             // -------------------------------------------------------- epilogue
             if (n_mine > 0) {
-                if (!wait_warp(BAR(C::kODone + u), (cnt - 1u) & 1u, abort_flag, P.status)) break;
+                if (!wait_warp(BAR(BI.o_done(u)), (cnt - 1u) & 1u, abort_flag, P.status)) break;
                 tc_fence_after();
             }
+            const float l = l0 + l1;
             const bool write_row = t < NT;
             const bool valid = r < n_t;
             const bool use_o = (n_mine > 0) && valid && (l != 0.f);  // NaN l keeps use_o: NaN row
@@ -565,34 +674,35 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 P.lse[orow] = v;
             }
             tc_fence_before();
-            mbar_arrive(BAR(C::kBmEmpty + p));
+            mbar_arrive(BAR(BI.bm_empty(p)));
         }
     }
 
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == kMmaWarp) tmem_dealloc(tmem, C::kTmemCols);
+    if (warp == kMmaWarp0) tmem_dealloc(tmem, C::kTmemCols);
 }
 
 template <int T, int D>
-cudaError_t launch_t(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v, const AttnParams &p,
-                     int grid, cudaStream_t stream) {
-    const SmemPlan L = smem_plan<T, D>(p.bm_words);
+cudaError_t launch_t(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v, AttnParams p, int grid,
+                     cudaStream_t stream) {
+    p.stages = stages_for<T, D>(p.bm_words);
+    const SmemPlan L = smem_plan<T, D>(p.bm_words, p.stages);
     attn_fwd_kernel<T, D><<<grid, kAttnThreads, L.total, stream>>>(q, k, v, p);
     return cudaGetLastError();
 }
 
 template <int T, int D>
 AttnLaunchInfo info_t(int bm_words) {
-    return AttnLaunchInfo{Cfg<T, D>::kStages, (int)smem_plan<T, D>(bm_words).total};
+    const int ns = stages_for<T, D>(bm_words);
+    return AttnLaunchInfo{ns, (int)smem_plan<T, D>(bm_words, ns).total};
 }
 
 template <int T, int D>
 cudaError_t prepare_t() {
-    const SmemPlan L = smem_plan<T, D>((kMaxTiles + 31) / 32);
     return cudaFuncSetAttribute(attn_fwd_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)L.total);
+                                (int)kSmemLimit);
 }
 
 }  // namespace
@@ -611,8 +721,8 @@ cudaError_t attn_prepare(int tile, int head_dim, int) {
     return prepare_t<64, 64>();
 }
 
-cudaError_t launch_attn(int tile, int head_dim, const CUtensorMap &q, const CUtensorMap &k,
-                        const CUtensorMap &v, const AttnParams &p, int grid, cudaStream_t stream) {
+cudaError_t launch_attn(int tile, int head_dim, const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
+                        AttnParams p, int grid, cudaStream_t stream) {
     if (tile == 128 && head_dim == 128) return launch_t<128, 128>(q, k, v, p, grid, stream);
     if (tile == 128 && head_dim == 64) return launch_t<128, 64>(q, k, v, p, grid, stream);
     if (tile == 64 && head_dim == 128) return launch_t<64, 128>(q, k, v, p, grid, stream);

@@ -14,7 +14,7 @@ enum : int32_t { kFlagIndex = 1, kFlagTimeout = 2 };
 // Query rows of one work item: two 128-row units, each one MMA M=128.
 constexpr int kUnitRows = 128;
 constexpr int kItemRows = 256;
-constexpr int kAttnThreads = 320;  // 8 softmax warps, 1 MMA warp, 1 producer warp
+constexpr int kAttnThreads = 384;  // 8 softmax warps, 2 MMA issuers, 1 producer, 1 fix-up warp
 constexpr int kMaxTiles = 8192;     // VSA_MAX_TILES
 
 struct AttnParams {
@@ -31,6 +31,7 @@ struct AttnParams {
     int32_t G;                   // work items per (b, h)
     int32_t bm_words;            // 32-bit words of one selection bitmap
     int32_t n_items;
+    int32_t stages;              // K/V ring depth (set by launch_attn)
     int64_t Sp;                  // NT * tile
     float scale_log2;            // softmax scale * log2(e)
 };
@@ -40,14 +41,17 @@ struct AttnLaunchInfo {
     int smem_bytes;
 };
 
-// Dynamic shared memory and ring depth of the attention kernel variant.
+// Ring depth and dynamic shared memory of the attention kernel variant: the
+// deepest K/V ring that fits the 227 KB per-CTA limit next to the Q tiles and
+// the selection bitmaps.
 AttnLaunchInfo attn_launch_info(int tile, int head_dim, int bm_words);
 
 // Enables the variant's shared-memory size on the current device (once).
 cudaError_t attn_prepare(int tile, int head_dim, int device);
 
+// Launches with p.stages taken from attn_launch_info (the caller's value is ignored).
 cudaError_t launch_attn(int tile, int head_dim, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
-                        const CUtensorMap &tm_v, const AttnParams &p, int grid, cudaStream_t stream);
+                        const CUtensorMap &tm_v, AttnParams p, int grid, cudaStream_t stream);
 
 struct LayoutParams {
     const void *src[3];
