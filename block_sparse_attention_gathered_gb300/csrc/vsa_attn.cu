@@ -88,6 +88,8 @@ struct Cfg {
     static constexpr int kChunks = D / 64;                    // 128-byte column chunks per row
     static constexpr uint32_t kQChunk = kUnitRows * 128;      // bytes of one Q column chunk
     static constexpr uint32_t kQBytes = kUnitRows * D * 2;    // one unit's Q
+    static constexpr uint32_t kPChunk = kUnitRows * 128;      // bytes of one P column chunk (64 keys)
+    static constexpr uint32_t kPBytes = kUnitRows * T * 2;    // one unit's P (bf16 softmax weights)
     static constexpr uint32_t kKVChunk = T * 128;             // bytes of one K/V column chunk
     static constexpr uint32_t kStageBytes = T * D * 2;        // one K or V tile
     static constexpr uint32_t kTmemO0 = 0, kTmemO1 = D, kTmemS0 = 2 * D, kTmemS1 = 2 * D + T;
@@ -110,11 +112,12 @@ struct Bars {
     __host__ __device__ int bm_full(int p) const { return 3 * NS + 10 + p; }
     __host__ __device__ int bm_empty(int p) const { return 3 * NS + 12 + p; }
     __host__ __device__ int done(int u) const { return 3 * NS + 14 + u; }
-    __host__ __device__ int count() const { return 3 * NS + 16; }
+    __host__ __device__ int s_free(int u) const { return 3 * NS + 16 + u; }  // S loaded by the softmax
+    __host__ __device__ int count() const { return 3 * NS + 18; }
 };
 
 struct SmemPlan {
-    uint32_t q, ring, bm, hdr, bars, tslot, flag, total;
+    uint32_t q, pbuf, ring, bm, hdr, bars, tslot, flag, total;
 };
 
 template <int T, int D>
@@ -122,7 +125,8 @@ __host__ __device__ inline SmemPlan smem_plan(int bm_words, int NS) {
     using C = Cfg<T, D>;
     SmemPlan s;
     s.q = 0;
-    s.ring = 2 * C::kQBytes;
+    s.pbuf = 2 * C::kQBytes;
+    s.ring = s.pbuf + 2 * C::kPBytes;
     s.bm = s.ring + (uint32_t)NS * C::kStageBytes;
     s.hdr = s.bm + 2u * 4u * 4u * (uint32_t)bm_words;
     s.bars = s.hdr + 32;
@@ -210,6 +214,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const int W = P.bm_words;
     const SmemPlan L = smem_plan<T, D>(W, NS);
     const uint32_t sQ = base + L.q;
+    const uint32_t sP = base + L.pbuf;
     const uint32_t sRing = base + L.ring;
     uint32_t *bm = reinterpret_cast<uint32_t *>(gbase + L.bm);           // [2][4][W]
     volatile int32_t *hdr = reinterpret_cast<int32_t *>(gbase + L.hdr);  // [2][4]
@@ -235,8 +240,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             mbar_init(BAR(BI.p_full(u)), 128);
             mbar_init(BAR(BI.o_done(u)), 1);
             mbar_init(BAR(BI.bm_full(u)), 32);
-            mbar_init(BAR(BI.bm_empty(u)), 3 * 32 + 32 * kSoftmaxWarps);
+            mbar_init(BAR(BI.bm_empty(u)), 2 + 32 + 32 * kSoftmaxWarps);  // issuers' lane 0, fix-up, softmax
             mbar_init(BAR(BI.done(u)), 1);
+            mbar_init(BAR(BI.s_free(u)), 128);
         }
         *abort_flag = 0;
         fence_mbar_init();
@@ -414,115 +420,118 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
       } else {
         // ------------------------------------------------------------ MMA issuers
-        // Warp kMmaWarp0 + u issues every MMA of unit u: S_u = Q_u K_j^T and
-        // O_u += P_u V_j.  Two issuers let one warp's barrier waits overlap the
-        // other's MMA issue (tcgen05.mma issue runs only ~2 instructions ahead).
-        const int u = warp - kMmaWarp0;
-        Ring ring;
-        uint32_t pcnt = 0;
-        uint32_t vz_par = 0;  // per stage: parity of its next tail-zeroing phase
-        const uint64_t dq = sdesc_sw128(sQ + u * C::kQBytes, 16, 1024);  // Q_u, K-major
-        const uint64_t dk = sdesc_sw128(sRing, 16, 1024);                // stage 0 as K-major B
-        const uint64_t dv = sdesc_sw128(sRing, C::kKVChunk, 1024);       // stage 0 as MN-major B
-        constexpr uint32_t kStage16 = C::kStageBytes >> 4;
-        const uint32_t tS = tmem + (u ? C::kTmemS1 : C::kTmemS0);
-        const uint32_t tO = tmem + (u ? C::kTmemO1 : C::kTmemO0);
-        bool ok = true;
-        for (uint32_t it = 0; ok; ++it) {
-            const int p = it & 1;
-            if (!(ok = wait_warp(BAR(BI.bm_full(p)), (it >> 1) & 1u, abort_flag, P.status))) break;
-            if (hdr[p * 4] < 0) break;
-            const uint32_t *bmp = bm + p * 4 * W;
-            const uint32_t *pa = bmp + (2 * u) * W, *pb = pa + W;
-            // member entries of this unit, so Q can be released right after its last S
-            uint32_t n_mine = 0;
-            for (int w = lane; w < W; w += 32) n_mine += __popc(pa[w] | pb[w]);
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) n_mine += __shfl_xor_sync(0xffffffffu, n_mine, o);
-            if (!(ok = wait_warp(BAR(BI.q_full(u)), it & 1u, abort_flag, P.status))) break;
-            tc_fence_after();
-            bool pending = false, first = true;
-            uint32_t pend_v = 0, pend_ph = 0;
-            int pend_kb = 0;
-            bool pend_tail = false;
-            uint32_t seen = 0;
-
-            // O_u += P_u V over the 16-key blocks of the previous member entry;
-            // then this issuer's release of that V stage.
-            auto flush = [&]() -> bool {
-                if (!wait_warp(BAR(BI.p_full(u)), pcnt & 1u, abort_flag, P.status)) return false;
-                ++pcnt;
-                if (!wait_warp(BAR(pend_tail ? BI.vz(pend_v) : BI.kv_full(pend_v)), pend_ph, abort_flag, P.status))
-                    return false;
+        // Lane 0 of warp kMmaWarp0 + u issues every MMA of unit u: S_u = Q_u
+        // K_j^T and O_u += P_u V_j.  tcgen05.mma issue runs only ~2
+        // instructions ahead of execution and each barrier wait costs the
+        // issuing thread ~100 cycles, so (a) two issuers let one unit's waits
+        // overlap the other's issue, and (b) all waits of an entry come before
+        // its MMAs, leaving nothing between a unit's P V and its next S.
+        if (lane == 0) {
+            const int u = warp - kMmaWarp0;
+            Ring ring;
+            uint32_t pcnt = 0;    // P V issued (= p_full phases consumed)
+            uint32_t scnt = 0;    // S issued (= s_full phases produced)
+            uint32_t vz_par = 0;  // per stage: parity of its next tail-zeroing phase
+            const uint64_t dq = sdesc_sw128(sQ + u * C::kQBytes, 16, 1024);  // Q_u, K-major
+            const uint64_t dk = sdesc_sw128(sRing, 16, 1024);                // stage 0 as K-major B
+            const uint64_t dv = sdesc_sw128(sRing, C::kKVChunk, 1024);       // stage 0 as MN-major B
+            const uint64_t dp = sdesc_sw128(sP + u * C::kPBytes, 16, 1024);  // P_u, K-major A
+            constexpr uint32_t kStage16 = C::kStageBytes >> 4;
+            const uint32_t tS = tmem + (u ? C::kTmemS1 : C::kTmemS0);
+            const uint32_t tO = tmem + (u ? C::kTmemO1 : C::kTmemO0);
+            bool ok = true;
+            for (uint32_t it = 0; ok; ++it) {
+                const int p = it & 1;
+                if (!(ok = wait_bar(BAR(BI.bm_full(p)), (it >> 1) & 1u, abort_flag, P.status))) break;
+                if (hdr[p * 4] < 0) break;
+                const uint32_t *bmp = bm + p * 4 * W;
+                const uint32_t *pa = bmp + (2 * u) * W, *pb = pa + W;
+                // member entries of this unit, so Q can be released right after its last S
+                uint32_t n_mine = 0;
+                for (int w = 0; w < W; ++w) n_mine += __popc(pa[w] | pb[w]);
+                if (!(ok = wait_bar(BAR(BI.q_full(u)), it & 1u, abort_flag, P.status))) break;
                 tc_fence_after();
-                if (lane == 0) {
+                bool pending = false, first = true;
+                uint32_t pend_v = 0, pend_ph = 0;
+                int pend_kb = 0;
+                bool pend_tail = false;
+                uint32_t seen = 0;
+
+                // O_u += P_u V of the pending entry (P from shared memory), then
+                // this issuer's release of that V stage.
+                auto pv = [&]() -> bool {
+                    if (!wait_bar(BAR(pend_tail ? BI.vz(pend_v) : BI.kv_full(pend_v)), pend_ph, abort_flag, P.status))
+                        return false;
+                    if (!wait_bar(BAR(BI.p_full(u)), pcnt & 1u, abort_flag, P.status)) return false;
+                    ++pcnt;
+                    tc_fence_after();
                     const uint64_t b = dv + pend_v * kStage16;
-                    mma_ts(tO, tS, b, C::kIdescPV, first ? 0u : 1u);
+                    mma_ss(tO, dp, b, C::kIdescPV, first ? 0u : 1u);
 #pragma unroll
                     for (int kk = 1; kk < T / 16; ++kk)
-                        if (kk < pend_kb) mma_ts(tO, tS + kk * 8, b + kk * 128, C::kIdescPV, 1u);
+                        if (kk < pend_kb)
+                            mma_ss(tO, dp + (kk >> 2) * (C::kPChunk >> 4) + (kk & 3) * 2, b + kk * 128,
+                                   C::kIdescPV, 1u);
                     mma_commit(BAR(BI.o_done(u)));
                     mma_commit(BAR(BI.kv_empty(pend_v)));
-                }
-                __syncwarp();
-                first = false;
-                pending = false;
-                return true;
-            };
+                    first = false;
+                    pending = false;
+                    return true;
+                };
 
-            for (int w = 0; w < W && ok; ++w) {
-                const uint32_t mw = pa[w] | pb[w];
-                uint32_t bits = bmp[w] | bmp[W + w] | bmp[2 * W + w] | bmp[3 * W + w];
-                while (bits && ok) {
-                    const int b = __ffs(bits) - 1;
-                    bits &= bits - 1;
-                    const int j = w * 32 + b;
-                    const uint32_t kst = ring.st, kph = ring.ph;
-                    ring.next(NS);
-                    const uint32_t vst = ring.st, vph = ring.ph;
-                    ring.next(NS);
-                    const int nj = __ldg(P.block_sizes + j);
-                    const bool tail = (nj & 15) != 0;
-                    const uint32_t vzp = (vz_par >> vst) & 1u;
-                    if (tail) vz_par ^= 1u << vst;
-                    // the previous PV frees a V stage: issue it first, member or not
-                    if (pending && !(ok = flush())) break;
-                    if (!(ok = wait_warp(BAR(BI.kv_full(kst)), kph, abort_flag, P.status))) break;
-                    if ((mw >> b) & 1u) {
-                        tc_fence_after();
-                        if (lane == 0) {
+                for (int w = 0; w < W && ok; ++w) {
+                    const uint32_t mw = pa[w] | pb[w];
+                    uint32_t bits = bmp[w] | bmp[W + w] | bmp[2 * W + w] | bmp[3 * W + w];
+                    while (bits && ok) {
+                        const int b = __ffs(bits) - 1;
+                        bits &= bits - 1;
+                        const int j = w * 32 + b;
+                        const uint32_t kst = ring.st, kph = ring.ph;
+                        ring.next(NS);
+                        const uint32_t vst = ring.st, vph = ring.ph;
+                        ring.next(NS);
+                        const int nj = __ldg(P.block_sizes + j);
+                        const bool tail = (nj & 15) != 0;
+                        const uint32_t vzp = (vz_par >> vst) & 1u;
+                        if (tail) vz_par ^= 1u << vst;
+                        if ((mw >> b) & 1u) {
+                            // S first: it needs only K and the softmax having loaded
+                            // the previous S; then the pending P V.
+                            if (!(ok = wait_bar(BAR(BI.kv_full(kst)), kph, abort_flag, P.status))) break;
+                            if (!(ok = wait_bar(BAR(BI.s_free(u)), (scnt & 1u) ^ 1u, abort_flag, P.status))) break;
+                            tc_fence_after();
 #pragma unroll
                             for (int kk = 0; kk < D / 16; ++kk)
                                 mma_ss(tS, dq + (kk >> 2) * (C::kQChunk >> 4) + (kk & 3) * 2,
                                        dk + kst * kStage16 + (kk >> 2) * (C::kKVChunk >> 4) + (kk & 3) * 2,
                                        C::kIdescQK, kk > 0 ? 1u : 0u);
                             mma_commit(BAR(BI.s_full(u)));
+                            ++scnt;
                             if (++seen == n_mine) mma_commit(BAR(BI.q_empty(u)));
                             mma_commit(BAR(BI.kv_empty(kst)));
+                            if (pending && !(ok = pv())) break;
+                            pending = true;
+                            pend_v = vst;
+                            pend_ph = tail ? vzp : vph;
+                            pend_kb = (nj + 15) >> 4;
+                            pend_tail = tail;
+                        } else {
+                            // not selected by this unit: issue the pending P V (it
+                            // frees a V stage), then release both stages of the entry
+                            if (pending && !(ok = pv())) break;
+                            if (!(ok = wait_bar(BAR(BI.kv_full(kst)), kph, abort_flag, P.status))) break;
+                            mbar_arrive(BAR(BI.kv_empty(kst)));
+                            if (!(ok = wait_bar(BAR(BI.kv_full(vst)), vph, abort_flag, P.status))) break;
+                            mbar_arrive(BAR(BI.kv_empty(vst)));
                         }
-                        __syncwarp();
-                        pending = true;
-                        pend_v = vst;
-                        pend_ph = tail ? vzp : vph;
-                        pend_kb = (nj + 15) >> 4;
-                        pend_tail = tail;
-                    } else {
-                        // not selected by this unit: release both stages of the entry
-                        if (lane == 0) mbar_arrive(BAR(BI.kv_empty(kst)));
-                        if (!(ok = wait_warp(BAR(BI.kv_full(vst)), vph, abort_flag, P.status))) break;
-                        if (lane == 0) mbar_arrive(BAR(BI.kv_empty(vst)));
-                        __syncwarp();
                     }
                 }
+                if (ok && pending) ok = pv();
+                if (!ok) break;
+                if (n_mine == 0) mma_commit(BAR(BI.q_empty(u)));  // no S issued: release Q
+                mbar_arrive(BAR(BI.bm_empty(p)));
             }
-            if (ok && pending) ok = flush();
-            if (!ok) break;
-            if (lane == 0 && n_mine == 0) mma_commit(BAR(BI.q_empty(u)));  // no S issued: release Q
-            __syncwarp();
-            mbar_arrive(BAR(BI.bm_empty(p)));
-        }
-        // All MMAs of this issuer complete before TMEM is released.
-        if (lane == 0) {
+            // All MMAs of this issuer complete before TMEM is released.
             mma_commit(BAR(BI.done(u)));
             drain_wait(BAR(BI.done(u)), 0u);
         }
@@ -538,6 +547,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const uint32_t tl = (uint32_t)(q4 * 32) << 16;
         const uint32_t tS = tmem + tl + (u ? C::kTmemS1 : C::kTmemS0);
         const uint32_t tO = tmem + tl + (u ? C::kTmemO1 : C::kTmemO0);
+        uint8_t *pbuf_row = gbase + L.pbuf + u * C::kPBytes + row * 128;  // row `row` of P_u, chunk 0
         const float c = P.scale_log2;
         uint32_t cnt = 0;  // member entries of this unit seen so far (all items)
         for (uint32_t it = 0;; ++it) {
@@ -564,11 +574,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     const int j = w * 32 + b;
                     if (!(ok = wait_warp(BAR(BI.s_full(u)), cnt & 1u, abort_flag, P.status))) break;
                     tc_fence_after();
-                    if ((mine >> b) & 1u) {
-                        const int nj = __ldg(P.block_sizes + j);
-                        float s[T];
+                    const bool member_row = ((mine >> b) & 1u) != 0u;  // warp-uniform
+                    float s[T];
+                    if (member_row) {
                         if constexpr (T == 128) tmem_ld128(tS, s);
                         else tmem_ld64(tS, s);
+                    }
+                    // S is in registers: the MMA issuer may overwrite it with the next S.
+                    tc_fence_before();
+                    mbar_arrive(BAR(BI.s_free(u)));
+                    float m_new = m;
+                    bool fresh = false, resc = false;
+                    if (member_row) {
+                        const int nj = __ldg(P.block_sizes + j);
                         if (nj < T) {
 #pragma unroll
                             for (int i = 0; i < T; ++i)
@@ -583,53 +601,63 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                             a3 = max3(a3, s[i + 6], s[i + 7]);
                         }
                         const float mx = max3(a0, a1, fmaxf(a2, a3)) * c;
-                        const float m_new = fmaxf(m, mx);
-                        const bool fresh = (m == -INFINITY);
-                        const bool resc = !fresh && (m_new > m + kRescaleThreshold);
-                        if (__any_sync(0xffffffffu, resc)) {
-                            // O of this unit holds the sum up to the previous
-                            // entry once that PV completes.
-                            if (!(ok = wait_warp(BAR(BI.o_done(u)), (cnt - 1u) & 1u, abort_flag, P.status)))
-                                break;
-                            tc_fence_after();
-                            const float alpha = resc ? ex2(m - m_new) : 1.f;
+                        m_new = fmaxf(m, mx);
+                        fresh = (m == -INFINITY);
+                        resc = !fresh && (m_new > m + kRescaleThreshold);
+                    }
+                    // The previous P V of this unit must be done: it reads the P
+                    // buffer about to be overwritten and accumulates into O.
+                    if (n_mine > 0) {
+                        if (!(ok = wait_warp(BAR(BI.o_done(u)), (cnt - 1u) & 1u, abort_flag, P.status))) break;
+                        tc_fence_after();
+                    }
+                    if (__any_sync(0xffffffffu, resc)) {
+                        const float alpha = resc ? ex2(m - m_new) : 1.f;
 #pragma unroll
-                            for (int ch = 0; ch < D / 32; ++ch) {
-                                float o[32];
-                                tmem_ld32(tO + ch * 32, o);
+                        for (int ch = 0; ch < D / 32; ++ch) {
+                            float o[32];
+                            tmem_ld32(tO + ch * 32, o);
 #pragma unroll
-                                for (int i = 0; i < 32; ++i) o[i] *= alpha;
-                                tmem_st32(tO + ch * 32, o);
-                            }
-                            tmem_wait_st();
-                            l0 *= alpha;
-                            l1 *= alpha;
+                            for (int i = 0; i < 32; ++i) o[i] *= alpha;
+                            tmem_st32(tO + ch * 32, o);
                         }
-                        if (fresh || resc) m = m_new;
-                        const float neg_m = -m;
+                        tmem_wait_st();
+                        l0 *= alpha;
+                        l1 *= alpha;
+                    }
+                    if (fresh || resc) m = m_new;
+                    const float neg_m = -m;
 #pragma unroll
-                        for (int ch = 0; ch < T / 32; ++ch) {
-                            uint32_t pk[16];
+                    for (int ch = 0; ch < T / 32; ++ch) {
+                        uint32_t pk[16];
+                        if (member_row) {
 #pragma unroll
                             for (int i = 0; i < 16; ++i) {
                                 float x0, x1;
                                 fma2_scalar(x0, x1, s[ch * 32 + 2 * i], s[ch * 32 + 2 * i + 1], c, neg_m);
                                 pk[i] = pack_bf16x2(ex2(x0), ex2(x1));
-                                // l sums the bf16 values P V actually uses, so
-                                // the weights P / l stay exactly normalised.
+                                // l sums the bf16 values P V actually uses, so the
+                                // weights P / l stay exactly normalised.
                                 add_bf16x2_f32(l0, l1, pk[i]);
                             }
-                            tmem_st16(tS + ch * 16, pk);
-                        }
-                    } else {
-                        // This half of the unit does not select tile j: its P
-                        // rows are zero so O is left unchanged.
-                        const uint32_t z[16] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u,
-                                                0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+                        } else {
+                            // this half of the unit does not select tile j: zero P rows
 #pragma unroll
-                        for (int ch = 0; ch < T / 32; ++ch) tmem_st16(tS + ch * 16, z);
+                            for (int i = 0; i < 16; ++i) pk[i] = 0u;
+                        }
+                        // P row `row`, 64-key chunk ch/2, 16-byte units (ch%2)*4..+3,
+                        // 128-byte swizzle: unit index XOR (row & 7).
+                        uint8_t *prow = pbuf_row + (ch >> 1) * C::kPChunk;
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const int unit = (ch & 1) * 4 + q;
+                            *reinterpret_cast<uint4 *>(prow + ((unit ^ (row & 7)) << 4)) =
+                                make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+                        }
                     }
-                    tmem_wait_st();
+                    // P is read by tcgen05.mma (async proxy); O may have been
+                    // rewritten with tcgen05.st above.
+                    fence_proxy_async_smem();
                     tc_fence_before();
                     mbar_arrive(BAR(BI.p_full(u)));
                     ++cnt;
