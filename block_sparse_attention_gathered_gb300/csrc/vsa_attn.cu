@@ -88,11 +88,12 @@ struct Cfg {
     static constexpr int kChunks = D / 64;                    // 128-byte column chunks per row
     static constexpr uint32_t kQChunk = kUnitRows * 128;      // bytes of one Q column chunk
     static constexpr uint32_t kQBytes = kUnitRows * D * 2;    // one unit's Q
-    static constexpr uint32_t kPChunk = kUnitRows * 128;      // bytes of one P column chunk (64 keys)
-    static constexpr uint32_t kPBytes = kUnitRows * T * 2;    // one unit's P (bf16 softmax weights)
     static constexpr uint32_t kKVChunk = T * 128;             // bytes of one K/V column chunk
     static constexpr uint32_t kStageBytes = T * D * 2;        // one K or V tile
-    static constexpr uint32_t kTmemO0 = 0, kTmemO1 = D, kTmemS0 = 2 * D, kTmemS1 = 2 * D + T;
+    // TMEM columns: O of each unit (fp32), one S buffer the units take turns
+    // on (fp32), and P of each unit (bf16 pairs).
+    static constexpr uint32_t kTmemO0 = 0, kTmemO1 = D, kTmemS = 2 * D, kTmemP0 = 2 * D + T,
+                              kTmemP1 = 2 * D + T + T / 2;
     static constexpr uint32_t kTmemCols = (2 * D + 2 * T <= 256) ? 256 : 512;
     static constexpr uint32_t kIdescQK = idesc_bf16(128, T, false);
     static constexpr uint32_t kIdescPV = idesc_bf16(128, D, true);
@@ -112,12 +113,11 @@ struct Bars {
     __host__ __device__ int bm_full(int p) const { return 3 * NS + 10 + p; }
     __host__ __device__ int bm_empty(int p) const { return 3 * NS + 12 + p; }
     __host__ __device__ int done(int u) const { return 3 * NS + 14 + u; }
-    __host__ __device__ int s_free(int u) const { return 3 * NS + 16 + u; }  // S loaded by the softmax
-    __host__ __device__ int count() const { return 3 * NS + 18; }
+    __host__ __device__ int count() const { return 3 * NS + 16; }
 };
 
 struct SmemPlan {
-    uint32_t q, pbuf, ring, bm, hdr, bars, tslot, flag, total;
+    uint32_t q, ring, bm, hdr, bars, tslot, flag, sfree, total;
 };
 
 template <int T, int D>
@@ -125,14 +125,14 @@ __host__ __device__ inline SmemPlan smem_plan(int bm_words, int NS) {
     using C = Cfg<T, D>;
     SmemPlan s;
     s.q = 0;
-    s.pbuf = 2 * C::kQBytes;
-    s.ring = s.pbuf + 2 * C::kPBytes;
+    s.ring = 2 * C::kQBytes;
     s.bm = s.ring + (uint32_t)NS * C::kStageBytes;
     s.hdr = s.bm + 2u * 4u * 4u * (uint32_t)bm_words;
     s.bars = s.hdr + 32;
     s.tslot = s.bars + 8u * (uint32_t)Bars{NS}.count();
     s.flag = s.tslot + 4;
-    s.total = ((s.flag + 4 + 15) & ~15u) + 1024;  // + slack to align the base to 1024
+    s.sfree = s.flag + 4;
+    s.total = ((s.sfree + 4 + 15) & ~15u) + 1024;  // + slack to align the base to 1024
     return s;
 }
 
@@ -193,6 +193,26 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
     }
 }
 
+// Bounded wait until a monotonic shared-memory counter reaches `target`.
+__device__ __forceinline__ bool wait_count(uint32_t addr, uint32_t target, volatile int *abort_flag,
+                                           int32_t *status) {
+    uint64_t t0 = 0;
+    for (uint32_t it = 0;; ++it) {
+        if ((int32_t)(ld_acquire(addr) - target) >= 0) return true;
+        if ((it & 63u) == 63u) {
+            if (*abort_flag) return false;
+            const uint64_t now = globaltimer_ns();
+            if (t0 == 0) {
+                t0 = now;
+            } else if (now - t0 > kWaitLimitNs) {
+                *abort_flag = 1;
+                atomicOr(status, kFlagTimeout);
+                return false;
+            }
+        }
+    }
+}
+
 // Tile index held by bitmap slot s (unit = s/2, half = s%2) of item g.
 template <int T>
 __device__ __forceinline__ int tile_of_slot(int g, int s) {
@@ -214,7 +234,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const int W = P.bm_words;
     const SmemPlan L = smem_plan<T, D>(W, NS);
     const uint32_t sQ = base + L.q;
-    const uint32_t sP = base + L.pbuf;
+    // Count of S tiles the softmax warps have copied out of the shared S buffer
+    // (each of the four warps of a unit adds 1 per S).
+    const uint32_t sFree = base + L.sfree;
     const uint32_t sRing = base + L.ring;
     uint32_t *bm = reinterpret_cast<uint32_t *>(gbase + L.bm);           // [2][4][W]
     volatile int32_t *hdr = reinterpret_cast<int32_t *>(gbase + L.hdr);  // [2][4]
@@ -242,9 +264,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             mbar_init(BAR(BI.bm_full(u)), 32);
             mbar_init(BAR(BI.bm_empty(u)), 2 + 32 + 32 * kSoftmaxWarps);  // issuers' lane 0, fix-up, softmax
             mbar_init(BAR(BI.done(u)), 1);
-            mbar_init(BAR(BI.s_free(u)), 128);
         }
         *abort_flag = 0;
+        *reinterpret_cast<volatile uint32_t *>(gbase + L.sfree) = 0u;
         fence_mbar_init();
         fence_proxy_async_smem();
     }
@@ -430,14 +452,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             const int u = warp - kMmaWarp0;
             Ring ring;
             uint32_t pcnt = 0;    // P V issued (= p_full phases consumed)
-            uint32_t scnt = 0;    // S issued (= s_full phases produced)
+            uint32_t gcnt = 0;    // S tiles of both units before this entry (union order, unit 0 first)
             uint32_t vz_par = 0;  // per stage: parity of its next tail-zeroing phase
             const uint64_t dq = sdesc_sw128(sQ + u * C::kQBytes, 16, 1024);  // Q_u, K-major
             const uint64_t dk = sdesc_sw128(sRing, 16, 1024);                // stage 0 as K-major B
             const uint64_t dv = sdesc_sw128(sRing, C::kKVChunk, 1024);       // stage 0 as MN-major B
-            const uint64_t dp = sdesc_sw128(sP + u * C::kPBytes, 16, 1024);  // P_u, K-major A
             constexpr uint32_t kStage16 = C::kStageBytes >> 4;
-            const uint32_t tS = tmem + (u ? C::kTmemS1 : C::kTmemS0);
+            const uint32_t tS = tmem + C::kTmemS;
+            const uint32_t tP = tmem + (u ? C::kTmemP1 : C::kTmemP0);
             const uint32_t tO = tmem + (u ? C::kTmemO1 : C::kTmemO0);
             bool ok = true;
             for (uint32_t it = 0; ok; ++it) {
@@ -466,12 +488,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     ++pcnt;
                     tc_fence_after();
                     const uint64_t b = dv + pend_v * kStage16;
-                    mma_ss(tO, dp, b, C::kIdescPV, first ? 0u : 1u);
+                    mma_ts(tO, tP, b, C::kIdescPV, first ? 0u : 1u);
 #pragma unroll
                     for (int kk = 1; kk < T / 16; ++kk)
-                        if (kk < pend_kb)
-                            mma_ss(tO, dp + (kk >> 2) * (C::kPChunk >> 4) + (kk & 3) * 2, b + kk * 128,
-                                   C::kIdescPV, 1u);
+                        if (kk < pend_kb) mma_ts(tO, tP + kk * 8, b + kk * 128, C::kIdescPV, 1u);
                     mma_commit(BAR(BI.o_done(u)));
                     mma_commit(BAR(BI.kv_empty(pend_v)));
                     first = false;
@@ -494,11 +514,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         const bool tail = (nj & 15) != 0;
                         const uint32_t vzp = (vz_par >> vst) & 1u;
                         if (tail) vz_par ^= 1u << vst;
+                        const uint32_t m0 = ((bmp[w] | bmp[W + w]) >> b) & 1u;
+                        const uint32_t m1 = ((bmp[2 * W + w] | bmp[3 * W + w]) >> b) & 1u;
+                        const uint32_t g = gcnt + (u ? m0 : 0u);  // this S in the shared-buffer order
+                        gcnt += m0 + m1;
                         if ((mw >> b) & 1u) {
                             // S first: it needs only K and the softmax having loaded
                             // the previous S; then the pending P V.
                             if (!(ok = wait_bar(BAR(BI.kv_full(kst)), kph, abort_flag, P.status))) break;
-                            if (!(ok = wait_bar(BAR(BI.s_free(u)), (scnt & 1u) ^ 1u, abort_flag, P.status))) break;
+                            // every earlier S tile has left the shared S buffer
+                            if (!(ok = wait_count(sFree, 4u * g, abort_flag, P.status))) break;
                             tc_fence_after();
 #pragma unroll
                             for (int kk = 0; kk < D / 16; ++kk)
@@ -506,7 +531,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                                        dk + kst * kStage16 + (kk >> 2) * (C::kKVChunk >> 4) + (kk & 3) * 2,
                                        C::kIdescQK, kk > 0 ? 1u : 0u);
                             mma_commit(BAR(BI.s_full(u)));
-                            ++scnt;
                             if (++seen == n_mine) mma_commit(BAR(BI.q_empty(u)));
                             mma_commit(BAR(BI.kv_empty(kst)));
                             if (pending && !(ok = pv())) break;
@@ -545,9 +569,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const int row = q4 * 32 + lane;  // query row within the unit
         const int half = (T == 64) ? (row >> 6) : 0;
         const uint32_t tl = (uint32_t)(q4 * 32) << 16;
-        const uint32_t tS = tmem + tl + (u ? C::kTmemS1 : C::kTmemS0);
+        const uint32_t tS = tmem + tl + C::kTmemS;
+        const uint32_t tP = tmem + tl + (u ? C::kTmemP1 : C::kTmemP0);
         const uint32_t tO = tmem + tl + (u ? C::kTmemO1 : C::kTmemO0);
-        uint8_t *pbuf_row = gbase + L.pbuf + u * C::kPBytes + row * 128;  // row `row` of P_u, chunk 0
         const float c = P.scale_log2;
         uint32_t cnt = 0;  // member entries of this unit seen so far (all items)
         for (uint32_t it = 0;; ++it) {
@@ -580,9 +604,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         if constexpr (T == 128) tmem_ld128(tS, s);
                         else tmem_ld64(tS, s);
                     }
-                    // S is in registers: the MMA issuer may overwrite it with the next S.
+                    // S is in registers: the shared S buffer may take the next S.
                     tc_fence_before();
-                    mbar_arrive(BAR(BI.s_free(u)));
+                    __syncwarp();
+                    if (lane == 0) red_add_release(sFree, 1u);
                     float m_new = m;
                     bool fresh = false, resc = false;
                     if (member_row) {
@@ -606,7 +631,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         resc = !fresh && (m_new > m + kRescaleThreshold);
                     }
                     // The previous P V of this unit must be done: it reads the P
-                    // buffer about to be overwritten and accumulates into O.
+                    // columns about to be overwritten and accumulates into O.
                     if (n_mine > 0) {
                         if (!(ok = wait_warp(BAR(BI.o_done(u)), (cnt - 1u) & 1u, abort_flag, P.status))) break;
                         tc_fence_after();
@@ -645,19 +670,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
                             for (int i = 0; i < 16; ++i) pk[i] = 0u;
                         }
-                        // P row `row`, 64-key chunk ch/2, 16-byte units (ch%2)*4..+3,
-                        // 128-byte swizzle: unit index XOR (row & 7).
-                        uint8_t *prow = pbuf_row + (ch >> 1) * C::kPChunk;
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const int unit = (ch & 1) * 4 + q;
-                            *reinterpret_cast<uint4 *>(prow + ((unit ^ (row & 7)) << 4)) =
-                                make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-                        }
+                        tmem_st16(tP + ch * 16, pk);
                     }
-                    // P is read by tcgen05.mma (async proxy); O may have been
-                    // rewritten with tcgen05.st above.
-                    fence_proxy_async_smem();
+                    tmem_wait_st();
                     tc_fence_before();
                     mbar_arrive(BAR(BI.p_full(u)));
                     ++cnt;
