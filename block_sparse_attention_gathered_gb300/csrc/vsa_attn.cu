@@ -63,6 +63,7 @@ template <int T> struct RegSplit {
 };
 constexpr uint32_t kSmemLimit = 232448;  // 227 KB opt-in per CTA
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr uint32_t kSleepHintNs = 20000;  // upper bound of one sleeping try_wait
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when the max grows by > 2^8
 
 // Instruction descriptor, tcgen05.mma kind::f16: bf16 A and B, fp32 D,
@@ -161,8 +162,10 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
     if (mbar_try_wait(bar, parity)) return true;
     uint64_t t0 = 0;
     for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 63u) == 0) {
+        // sleep in the barrier instead of spinning: spinning warps take issue
+        // slots from the softmax warps that share their SM sub-partition
+        if (mbar_try_wait_sleep(bar, parity, kSleepHintNs)) return true;
+        if ((it & 7u) == 0) {
             if (*abort_flag) return false;
             const uint64_t now = globaltimer_ns();
             if (t0 == 0) {
@@ -199,6 +202,7 @@ __device__ __forceinline__ bool wait_count(uint32_t addr, uint32_t target, volat
     uint64_t t0 = 0;
     for (uint32_t it = 0;; ++it) {
         if ((int32_t)(ld_acquire(addr) - target) >= 0) return true;
+        __nanosleep(32);
         if ((it & 63u) == 63u) {
             if (*abort_flag) return false;
             const uint64_t now = globaltimer_ns();
