@@ -656,6 +656,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     }
                     if (fresh || resc) m = m_new;
                     const float neg_m = -m;
+                    // This tile's part of l in 8 independent sums: one running sum
+                    // would chain 128 dependent adds through the row.
+                    float la[8];
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) la[q] = 0.f;
 #pragma unroll
                     for (int ch = 0; ch < T / 32; ++ch) {
                         uint32_t pk[16];
@@ -667,7 +672,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                                 pk[i] = pack_bf16x2(ex2(x0), ex2(x1));
                                 // l sums the bf16 values P V actually uses, so the
                                 // weights P / l stay exactly normalised.
-                                add_bf16x2_f32(l0, l1, pk[i]);
+                                add_bf16x2_f32(la[2 * (i & 3)], la[2 * (i & 3) + 1], pk[i]);
                             }
                         } else {
                             // this half of the unit does not select tile j: zero P rows
@@ -676,6 +681,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         }
                         tmem_st16(tP + ch * 16, pk);
                     }
+                    l0 += (la[0] + la[2]) + (la[4] + la[6]);
+                    l1 += (la[1] + la[3]) + (la[5] + la[7]);
                     tmem_wait_st();
                     tc_fence_before();
                     mbar_arrive(BAR(BI.p_full(u)));
