@@ -43,8 +43,8 @@ FALLBACK_HBM_GBS = 6800.0
 # the SHA-256 of the attention kernel source the capture was taken with; a
 # changed kernel reports null until it is captured again.
 ATTN_TRAFFIC = {
-    # profiles/attn_fwd_t128d128_dense_b1h6_s31200.md: 345.5 MB read + 38.8 MB written
-    ("dense_b1h6d128_s31200_t128x244_lse", "6b166f4f356a13be"): 384.27e6,
+    # profiles/attn_fwd_t128d128_dense_b1h6_s31200.md: 313.0 MB read + 36.8 MB written
+    ("dense_b1h6d128_s31200_t128x244_lse", "3461624eb2703e31"): 349.78e6,
 }
 
 
@@ -73,18 +73,25 @@ class ClockSampler:
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index: int):
+    def __init__(self, index: int, period_ms: int = 20):
         self.index = index
+        self.period_ms = period_ms
         self.proc = None
         self.lines = []
+        self.start = 0
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                          "--format=csv,noheader,nounits", "-lms", str(self.period_ms)],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
+            # start timing only once the sampler is producing lines
+            t0 = time.monotonic()
+            while not self.lines and self.proc.poll() is None and time.monotonic() - t0 < 5.0:
+                time.sleep(0.01)
+            self.start = len(self.lines)
         except OSError:
             self.proc = None
         return self
@@ -105,7 +112,7 @@ class ClockSampler:
     def summary(self):
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.lines:
+        for line in self.lines[self.start:]:
             f = [x.strip() for x in line.split(",")]
             if len(f) < 9:
                 continue
@@ -175,7 +182,9 @@ def run_reference(args, cfg):
     import oracle
     oracle.build()
     nthreads = oracle.default_threads()
-    refs, units = _cpu_sample_units(w, 4.0, nthreads)
+    # each step times the oracle on a sample sized so that the whole run stays
+    # within a few minutes
+    refs, units = _cpu_sample_units(w, min(4.0, 150.0 / max(1, args.steps + args.warmup)), nthreads)
     fl = _unit_flops(w, units)
     times = []
     for i in range(args.warmup + args.steps):
@@ -192,11 +201,38 @@ def run_reference(args, cfg):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "S": w.S or w.Sp, "head_dim": w.D, "tile": w.T,
-                   "num_tiles": w.NT, "density": "100%" if cfg == 5 else "per workload",
-                   "lse": w.want_lse},
+                   "num_tiles": w.NT, "density": round(density(w), 4), "lse": w.want_lse},
         "cpu_baseline": {"value": val, "unit": UNIT, "cores": nthreads, "kind": "oracle", "sample": sample},
         "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
+
+
+def density(w) -> float:
+    """Fraction of (query tile, key tile) pairs selected."""
+    return float(w.q2k_num.sum()) / float(w.B * w.H * w.NT * w.NT)
+
+
+def layout_bytes(w) -> int:
+    """Algorithmic bytes of one tile-layout launch: every token's q/k/v head
+    vectors read once, every tile-major row (padding included) written once,
+    plus the 4-byte row map."""
+    return 3 * 2 * w.B * w.H * w.D * (w.S + w.Sp) + 4 * w.Sp
+
+
+def max_over_ranks(x: float, device) -> float:
+    """The largest value of ``x`` over all ranks (``x`` itself on one rank)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(eff_flops_per_rank: float, world: int, ms_max: float) -> float:
+    """Whole-job effective TFLOP/s: every rank runs one full problem (weak
+    scaling, independent replicas), timed by the slowest rank."""
+    return world * eff_flops_per_rank / (ms_max / 1e3) / 1e12
 
 
 def run_ours(args, cfg):
@@ -225,14 +261,19 @@ def run_ours(args, cfg):
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)  # > 129 MB L2
     stream = torch.cuda.current_stream()
 
+    def ev():
+        return torch.cuda.Event(enable_timing=True)
+
     def step(qt, kt, vt):
+        """One pass of the hot path; returns events around the layout and the
+        attention call (recorded on the launching stream)."""
+        l0, l1, a1 = ev(), ev(), ev()
+        l0.record(stream)
         vsa.vsa_tile_layout(qt, kt, vt, tiles[0], tiles[1], tiles[2], r2t, B, S, H, D, NT, T, stream)
-        a0 = torch.cuda.Event(enable_timing=True)
-        a1 = torch.cuda.Event(enable_timing=True)
-        a0.record(stream)
+        l1.record(stream)
         vsa.vsa_block_sparse_fwd(tiles[0], tiles[1], tiles[2], idx, num, bs, out, lse, dims, ws, stream)
         a1.record(stream)
-        return a0, a1
+        return l0, l1, a1
 
     def barrier():
         if world > 1:
@@ -247,27 +288,17 @@ def run_ours(args, cfg):
         raise RuntimeError("device status error during warm-up")
 
     # ---------------------------------------------------------------- device-timed steps
-    pairs, attn = [], []
+    marks = []
     with ClockSampler(torch.cuda.current_device()) as clk:
         barrier()
         for _ in range(args.steps):
             flush.zero_()  # L2 flush, outside the timed events
-            s0 = torch.cuda.Event(enable_timing=True)
-            s1 = torch.cuda.Event(enable_timing=True)
-            s0.record(stream)
-            a0, a1 = step(q_tok, k_tok, v_tok)
-            s1.record(stream)
-            pairs.append((s0, s1))
-            attn.append((a0, a1))
+            marks.append(step(q_tok, k_tok, v_tok))
         barrier()
-    step_ms = [a.elapsed_time(b) for a, b in pairs]
-    attn_ms = [a.elapsed_time(b) for a, b in attn]
-    ms = sum(step_ms) / len(step_ms)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    step_ms = [a.elapsed_time(c) for a, b, c in marks]
+    layout_ms = [a.elapsed_time(b) for a, b, c in marks]
+    attn_ms = [b.elapsed_time(c) for a, b, c in marks]
+    ms = max_over_ranks(sum(step_ms) / len(step_ms), dev)
     if vsa.vsa_check_device_status() != 0:
         raise RuntimeError("device status error in the timed region")
 
@@ -293,41 +324,40 @@ def run_ours(args, cfg):
     e_ms = []
     for _ in range(args.steps):
         flush.zero_()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
+        e0, e1 = ev(), ev()
         e0.record(stream)
         e2e_step()
         e1.record(stream)
         e_ms.append((e0, e1))
     barrier()
-    e2e_ms = sum(a.elapsed_time(b) for a, b in e_ms) / len(e_ms)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in e_ms) / len(e_ms), dev)
 
     route = vsa.vsa_last_route()
     peak, hbm, src = _peaks()
     attn_avg = sum(attn_ms) / len(attn_ms)
+    lay_avg = sum(layout_ms) / len(layout_ms)
     achieved = eff / (attn_avg / 1e3) / 1e12
-    h = _attn_source_hash()
-    traffic = ATTN_TRAFFIC.get((w.name, h))
+    lay_gbs = layout_bytes(w) / (lay_avg / 1e3) / 1e9
+    traffic = ATTN_TRAFFIC.get((w.name, _attn_source_hash()))
     if rank == 0:
         line = {
-            "metric": METRIC, "value": world * eff / (ms / 1e3) / 1e12, "unit": UNIT, "n_gpus": world,
+            "metric": METRIC, "value": aggregate(eff, world, ms), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": w.name, "B": B, "H": H, "S": S, "head_dim": D, "tile": T, "num_tiles": NT,
-                       "density": "100%", "lse": True, "effective_flops": eff,
+                       "density": round(density(w), 4), "lse": w.want_lse, "effective_flops": eff,
                        "padded_flops": W.padded_flops(w), "l2": "flushed (256 MB write) between steps",
                        "step": "tile layout (q,k,v) + work ordering + tcgen05 attention"},
-            "attn_ms": attn_avg, "layout_plus_sched_ms": ms - attn_avg,
+            "attn_ms": attn_avg, "layout_ms": lay_avg,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                          "frac": achieved / peak, "traffic": traffic,
-                         "peak_source": f"{src} bf16 burst (cuBLAS)", "kernel": "attn_fwd_kernel<128,128>"},
-            "e2e": {"value": world * eff / (e2e_ms / 1e3) / 1e12, "unit": UNIT, "ms_per_step": e2e_ms,
+                         "peak_source": f"{src} bf16 burst (cuBLAS)", "kernel": f"attn_fwd_kernel<{T},{D}>"},
+            "layout_roofline": {"bound": "hbm", "achieved": lay_gbs, "peak": hbm, "unit": "GB/s",
+                                "frac": lay_gbs / hbm, "bytes": layout_bytes(w),
+                                "peak_source": f"{src} HBM copy", "kernel": "layout_kernel"},
+            "e2e": {"value": aggregate(eff, world, e2e_ms), "unit": UNIT, "ms_per_step": e2e_ms,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            # per step: tile layout, work-ordering sort, attention
             "gpu_launches": 3 * args.steps,
             "clocks": clk.summary(),
             "route": route,
@@ -343,8 +373,8 @@ def run_ours(args, cfg):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", type=int, default=5, choices=[2, 4, 5])
     ap.add_argument("--no-cpu-baseline", action="store_true")
