@@ -52,6 +52,8 @@ def _load():
         lib.oracle_block_sparse_fwd.restype = i32
         lib.oracle_tile_layout.argtypes = [P, P, P, i32, i32, i32, i32, i32, i32]
         lib.oracle_tile_layout.restype = i32
+        lib.oracle_coarse_select.argtypes = [P, P, P, i32, i32, i32, i32, i32, i32, P, P, P]
+        lib.oracle_coarse_select.restype = i32
         _lib = lib
     return _lib
 
@@ -122,6 +124,31 @@ def tile_layout(x_tok, row_to_token, NT: int, T: int) -> np.ndarray:
     if rc != 0:
         raise ValueError(f"oracle_tile_layout: {ERRORS.get(rc, rc)}")
     return dst
+
+
+def coarse_select(q, k, block_sizes, T: int, topk: int, want_scores: bool = True):
+    """Coarse key-tile selection (see ``oracle_coarse_select`` in vsa_oracle.c):
+    tile means of the valid rows, tile-level q.k scores, the ``topk`` best key
+    tiles per query tile (ties to the smaller index), all in fp32 with sums in
+    index order.  ``q, k``: tile-major bf16 ``[B, H, NT*T, D]``.
+
+    Returns ``(q2k_idx [B,H,NT,topk] int32 ascending, -1 padded;
+    q2k_num [B,H,NT] int32; scores [B,H,NT,NT] float32 or None)``.
+    """
+    qb, kb = _bf16_bits(q), _bf16_bits(k)
+    B, H, Sp, D = qb.shape
+    assert kb.shape == qb.shape and Sp % T == 0
+    NT = Sp // T
+    bs = _i32(block_sizes)
+    assert bs.shape == (NT,)
+    idx = np.empty((B, H, NT, topk), dtype=np.int32)
+    num = np.empty((B, H, NT), dtype=np.int32)
+    sc = np.empty((B, H, NT, NT), dtype=np.float32) if want_scores else None
+    rc = _load().oracle_coarse_select(_ptr(qb), _ptr(kb), _ptr(bs), B, H, NT, T, D, int(topk), _ptr(idx),
+                                      _ptr(num), _ptr(sc) if sc is not None else None)
+    if rc != 0:
+        raise ValueError(f"oracle_coarse_select: {ERRORS.get(rc, rc)}")
+    return idx, num, sc
 
 
 def bits_to_float(bits: np.ndarray) -> np.ndarray:

@@ -1,5 +1,6 @@
 /*
- * CPU oracle for the block-sparse attention forward pass and the tile layout.
+ * CPU oracle for the block-sparse attention forward pass, the tile layout and
+ * the coarse key-tile selection that produces the block-sparse selection.
  *
  * TEST INFRASTRUCTURE ONLY.  This file is the plain, slow, obviously correct
  * FP64 statement of what the GPU library computes.  Only the tests, the smoke
@@ -234,5 +235,105 @@ int oracle_tile_layout(const uint16_t *src, const int32_t *row_to_token, uint16_
                 for (int d = 0; d < D; ++d)
                     o[d] = (s < 0) ? (uint16_t)0 : src[(((int64_t)b * S + s) * H + h) * D + d];
             }
+    return ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------------
+ * Coarse key-tile selection of video sparse attention: the step that produces
+ * q2k_idx / q2k_num for the block-sparse forward.
+ *
+ * The page names video sparse attention (VSA) and its block-sparse fine stage
+ * (commit adding the sm_121a tile-128 forward; fused tile_to_bhsd commit:
+ * "Wan VSA inference"), but not the coarse stage's arithmetic.  Plain reading,
+ * stated here and used below:
+ *   1. every non-empty tile t (n_t = block_sizes[t] > 0) is pooled to the mean
+ *      of its valid rows: qm[t] = (sum_{r < n_t} q[t*T + r]) / n_t, and km[t]
+ *      likewise from k; padding rows are never read;
+ *   2. the tile-level score is the dot product score[t][j] = sum_d qm[t][d] *
+ *      km[j][d] (a positive softmax scale would not change the ranking);
+ *   3. query tile t keeps the topk key tiles j with the largest score among
+ *      the candidates (n_j > 0 and the score is not NaN), ties going to the
+ *      smaller j; with fewer candidates it keeps all of them; an empty query
+ *      tile keeps none;
+ *   4. the kept tiles are written in ascending order to q2k_idx[b,h,t,0:kk],
+ *      the rest of the row is -1, and q2k_num[b,h,t] = kk.
+ * The selection is an integer result decided by floating point, so this
+ * oracle takes the decision in the precision of the GPU kernel (fp32), with
+ * every sum in index order and no fused multiply-add (-ffp-contract=off).
+ * scores (nullable) receives the fp32 score matrix [B,H,NT,NT] (NaN for a
+ * non-candidate pair) so that tests can tell exact ties from clear gaps.
+ * ------------------------------------------------------------------------ */
+int oracle_coarse_select(const uint16_t *q, const uint16_t *k, const int32_t *block_sizes, int B, int H,
+                         int NT, int T, int D, int topk, int32_t *q2k_idx, int32_t *q2k_num, float *scores) {
+    if (!q || !k || !block_sizes || !q2k_idx || !q2k_num || B <= 0 || H <= 0 || NT <= 0 || T <= 0 ||
+        D <= 0 || topk < 0)
+        return ORACLE_ERR_ARG;
+    for (int t = 0; t < NT; ++t)
+        if (block_sizes[t] < 0 || block_sizes[t] > T) return ORACLE_ERR_ARG;
+    const int64_t Sp = (int64_t)NT * T;
+    float *qm = (float *)malloc(sizeof(float) * (size_t)NT * D);
+    float *km = (float *)malloc(sizeof(float) * (size_t)NT * D);
+    float *row = (float *)malloc(sizeof(float) * (size_t)NT);
+    unsigned char *taken = (unsigned char *)malloc((size_t)NT);
+    if (!qm || !km || !row || !taken) {
+        free(qm);
+        free(km);
+        free(row);
+        free(taken);
+        return ORACLE_ERR_NOMEM;
+    }
+    for (int b = 0; b < B; ++b)
+        for (int h = 0; h < H; ++h) {
+            const int64_t bh = (int64_t)b * H + h;
+            /* 1. tile means, fp32, rows in order */
+            for (int t = 0; t < NT; ++t) {
+                const int n = block_sizes[t];
+                for (int d = 0; d < D; ++d) {
+                    float sq = 0.f, sk = 0.f;
+                    for (int r = 0; r < n; ++r) {
+                        const int64_t at = (bh * Sp + (int64_t)t * T + r) * D + d;
+                        sq += (float)bf16_to_double(q[at]);
+                        sk += (float)bf16_to_double(k[at]);
+                    }
+                    qm[(int64_t)t * D + d] = n > 0 ? sq / (float)n : 0.f;
+                    km[(int64_t)t * D + d] = n > 0 ? sk / (float)n : 0.f;
+                }
+            }
+            for (int t = 0; t < NT; ++t) {
+                /* 2. scores of query tile t against every candidate key tile */
+                int n_cand = 0;
+                for (int j = 0; j < NT; ++j) {
+                    float s = 0.f;
+                    for (int d = 0; d < D; ++d) s += qm[(int64_t)t * D + d] * km[(int64_t)j * D + d];
+                    const int cand = block_sizes[j] > 0 && !isnan(s);
+                    row[j] = cand ? s : NAN;
+                    taken[j] = 0;
+                    n_cand += cand;
+                }
+                if (scores) memcpy(scores + (bh * NT + t) * NT, row, sizeof(float) * (size_t)NT);
+                /* 3. the kk best candidates: repeatedly the largest score not yet
+                 *    taken, the smaller index on a tie */
+                int kk = block_sizes[t] > 0 ? (topk < n_cand ? topk : n_cand) : 0;
+                for (int i = 0; i < kk; ++i) {
+                    int best = -1;
+                    for (int j = 0; j < NT; ++j) {
+                        if (taken[j] || isnan(row[j])) continue;
+                        if (best < 0 || row[j] > row[best]) best = j;
+                    }
+                    taken[best] = 1;
+                }
+                /* 4. ascending order, -1 after */
+                int32_t *out = q2k_idx + (bh * NT + t) * (int64_t)topk;
+                int o = 0;
+                for (int j = 0; j < NT; ++j)
+                    if (taken[j]) out[o++] = j;
+                for (; o < topk; ++o) out[o] = -1;
+                q2k_num[bh * NT + t] = kk;
+            }
+        }
+    free(qm);
+    free(km);
+    free(row);
+    free(taken);
     return ORACLE_OK;
 }

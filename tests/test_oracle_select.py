@@ -1,0 +1,122 @@
+"""Pins for the oracle's coarse key-tile selection (no GPU).
+
+The selection (tile means of the valid rows, tile-level q.k scores, the top-k
+key tiles per query tile with ties to the smaller index) is the step before
+the block-sparse forward of video sparse attention on the FastVideo kernel
+page (hao-ai-lab/FastVideo commit 8503617, fastvideo-kernel/python).  Each test
+checks the oracle against something other than itself: planted rankings with
+exactly known scores, exact ties, the empty-tile and count rules, padding
+isolation, and a float64 library computation (torch mean, matmul, topk).
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+
+
+def _tiles(vals_per_tile, T, D, bs, fill=0.0):
+    """Tile-major [1, 1, NT*T, D] bf16 whose valid rows of tile t all equal
+    vals_per_tile[t] (a length-D vector); padding rows hold `fill`."""
+    NT = len(vals_per_tile)
+    x = torch.full((1, 1, NT * T, D), fill, dtype=torch.float32)
+    for t, v in enumerate(vals_per_tile):
+        x[0, 0, t * T: t * T + int(bs[t])] = torch.as_tensor(v, dtype=torch.float32)
+    return x.to(torch.bfloat16)
+
+
+def test_planted_ranking(oracle_mod):
+    # q tiles pool to e0 exactly; key tile j pools to c_j * e0 with distinct,
+    # exactly representable c_j, so score[t][j] = c_j and the top k are known.
+    NT, T, D, k = 12, 8, 16, 5
+    rng = np.random.default_rng(3)
+    perm = rng.permutation(NT)
+    bs = torch.tensor([T, 3, T, 1, T, 5, 7, T, 2, T, 6, 4], dtype=torch.int32)
+    e0 = np.eye(D)[0]
+    q = _tiles([e0] * NT, T, D, bs, fill=float("nan"))
+    kk = _tiles([(perm[j] + 1) / 16.0 * e0 for j in range(NT)], T, D, bs, fill=float("inf"))
+    idx, num, sc = oracle_mod.coarse_select(q, kk, bs, T, k)
+    want = sorted(np.argsort(-perm)[:k].tolist())
+    for t in range(NT):
+        assert num[0, 0, t] == k
+        assert idx[0, 0, t, :k].tolist() == want
+        np.testing.assert_array_equal(sc[0, 0, t], ((perm + 1) / 16.0).astype(np.float32))
+
+
+def test_ties_go_to_the_smaller_index(oracle_mod):
+    NT, T, D, k = 9, 4, 8, 4
+    bs = torch.full((NT,), T, dtype=torch.int32)
+    v = np.linspace(-1, 1, D)
+    q = _tiles([v] * NT, T, D, bs)
+    kk = _tiles([v] * NT, T, D, bs)  # every key tile identical: all scores equal
+    idx, num, _ = oracle_mod.coarse_select(q, kk, bs, T, k)
+    assert (num == k).all()
+    assert (idx[0, 0, :, :k] == np.arange(k)).all()
+
+
+def test_counts_empty_tiles_and_short_rows(oracle_mod):
+    NT, T, D = 6, 4, 8
+    bs = torch.tensor([4, 0, 2, 0, 3, 1], dtype=torch.int32)
+    g = torch.Generator().manual_seed(5)
+    q = torch.randn((1, 2, NT * T, D), generator=g).to(torch.bfloat16)
+    kk = torch.randn((1, 2, NT * T, D), generator=g).to(torch.bfloat16)
+    cand = [j for j in range(NT) if bs[j] > 0]
+    # topk larger than the candidates: every non-empty key tile, ascending, -1 after
+    idx, num, sc = oracle_mod.coarse_select(q, kk, bs, T, 5)
+    for h in range(2):
+        for t in range(NT):
+            if bs[t] == 0:
+                assert num[0, h, t] == 0 and (idx[0, h, t] == -1).all()
+            else:
+                assert num[0, h, t] == len(cand)
+                assert idx[0, h, t].tolist() == cand + [-1]
+            assert np.isnan(sc[0, h, t, [1, 3]]).all()
+    # topk = 0 keeps nothing
+    idx0, num0, _ = oracle_mod.coarse_select(q, kk, bs, T, 0, want_scores=False)
+    assert (num0 == 0).all() and idx0.shape == (1, 2, NT, 0)
+
+
+def test_padding_values_are_never_read(oracle_mod):
+    NT, T, D, k = 7, 8, 16, 3
+    g = torch.Generator().manual_seed(11)
+    bs = torch.tensor([8, 5, 1, 8, 3, 7, 2], dtype=torch.int32)
+    q = torch.randn((2, 2, NT * T, D), generator=g).to(torch.bfloat16)
+    kk = torch.randn((2, 2, NT * T, D), generator=g).to(torch.bfloat16)
+    qz, kz = (W.pad_tile_major(x, bs, T, "zero") for x in (q, kk))
+    qn, kn = (W.pad_tile_major(x, bs, T, "naninf") for x in (q, kk))
+    a = oracle_mod.coarse_select(qz, kz, bs, T, k)
+    b = oracle_mod.coarse_select(qn, kn, bs, T, k)
+    for x, y in zip(a, b):
+        np.testing.assert_array_equal(x, y)
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_matches_float64_library_topk(oracle_mod, seed):
+    # torch float64: mean over the valid rows, matmul, topk.  Where the k-th and
+    # (k+1)-th float64 scores are clearly apart the kept set is unique and the
+    # fp32 oracle must keep exactly that set.
+    B, H, NT, T, D, k = 1, 3, 20, 16, 32, 6
+    g = torch.Generator().manual_seed(seed)
+    bs = torch.randint(1, T + 1, (NT,), generator=g).to(torch.int32)
+    off = torch.randn((B, H, NT, 1, D), generator=g)
+    q = (torch.randn((B, H, NT, T, D), generator=g) + off).reshape(B, H, NT * T, D).to(torch.bfloat16)
+    kk = (torch.randn((B, H, NT, T, D), generator=g) + off).reshape(B, H, NT * T, D).to(torch.bfloat16)
+    idx, num, sc = oracle_mod.coarse_select(q, kk, bs, T, k)
+    qd = q.double().reshape(B, H, NT, T, D)
+    kd = kk.double().reshape(B, H, NT, T, D)
+    mask = (torch.arange(T)[None, :] < bs[:, None]).double()[None, None, :, :, None]
+    qm = (qd * mask).sum(3) / bs.double()[None, None, :, None]
+    km = (kd * mask).sum(3) / bs.double()[None, None, :, None]
+    s64 = qm @ km.transpose(-1, -2)
+    np.testing.assert_allclose(sc, s64.numpy(), rtol=1e-4, atol=1e-4)
+    checked = 0
+    for h in range(H):
+        for t in range(NT):
+            srt = torch.sort(s64[0, h, t], descending=True).values
+            if float(srt[k - 1] - srt[k]) < 1e-3:
+                continue
+            want = sorted(torch.topk(s64[0, h, t], k).indices.tolist())
+            assert num[0, h, t] == k
+            assert idx[0, h, t].tolist() == want
+            checked += 1
+    assert checked >= H * NT // 2
