@@ -250,7 +250,8 @@ int oracle_tile_layout(const uint16_t *src, const int32_t *row_to_token, uint16_
  *      of its valid rows: qm[t] = (sum_{r < n_t} q[t*T + r]) / n_t, and km[t]
  *      likewise from k; padding rows are never read;
  *   2. the tile-level score is the dot product score[t][j] = sum_d qm[t][d] *
- *      km[j][d] (a positive softmax scale would not change the ranking);
+ *      km[j][d], each term added with one fused multiply-add (a positive
+ *      softmax scale would not change the ranking);
  *   3. query tile t keeps the topk key tiles j with the largest score among
  *      the candidates (n_j > 0 and the score is not NaN), ties going to the
  *      smaller j; with fewer candidates it keeps all of them; an empty query
@@ -259,7 +260,8 @@ int oracle_tile_layout(const uint16_t *src, const int32_t *row_to_token, uint16_
  *      the rest of the row is -1, and q2k_num[b,h,t] = kk.
  * The selection is an integer result decided by floating point, so this
  * oracle takes the decision in the precision of the GPU kernel (fp32), with
- * every sum in index order and no fused multiply-add (-ffp-contract=off).
+ * every sum in index order: the means by plain adds, the scores by fmaf
+ * (-ffp-contract=off keeps every other operation unfused).
  * scores (nullable) receives the fp32 score matrix [B,H,NT,NT] (NaN for a
  * non-candidate pair) so that tests can tell exact ties from clear gaps.
  * ------------------------------------------------------------------------ */
@@ -304,7 +306,7 @@ int oracle_coarse_select(const uint16_t *q, const uint16_t *k, const int32_t *bl
                 int n_cand = 0;
                 for (int j = 0; j < NT; ++j) {
                     float s = 0.f;
-                    for (int d = 0; d < D; ++d) s += qm[(int64_t)t * D + d] * km[(int64_t)j * D + d];
+                    for (int d = 0; d < D; ++d) s = fmaf(qm[(int64_t)t * D + d], km[(int64_t)j * D + d], s);
                     const int cand = block_sizes[j] > 0 && !isnan(s);
                     row[j] = cand ? s : NAN;
                     taken[j] = 0;
