@@ -25,6 +25,7 @@ LIB_PATH = os.path.join(_HERE, "_build", "libvsa.so")
 VSA_OK, VSA_ERR_ARG, VSA_ERR_ALIGN, VSA_ERR_LIMITS, VSA_ERR_ARCH = 0, -1, -2, -3, -4
 VSA_ERR_CUDA, VSA_ERR_TIMEOUT, VSA_ERR_INDEX, VSA_ERR_WORKSPACE = -5, -6, -7, -8
 VSA_KERNEL_NONE, VSA_KERNEL_ATTN_TCGEN05, VSA_KERNEL_LAYOUT, VSA_KERNEL_VALIDATE = 0, 1, 2, 3
+VSA_KERNEL_SELECT = 4
 VSA_MAX_BATCH_HEADS, VSA_MAX_TILES = 65535, 8192
 
 
@@ -63,6 +64,8 @@ def _load() -> ctypes.CDLL:
         "vsa_block_sparse_fwd_noalloc": ([P, P, P, P, P, P, P, P, dims_p, P], i32),
         "vsa_tile_layout": ([P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, P], i32),
         "vsa_validate_indices": ([P, P, P, dims_p, P, P], i32),
+        "vsa_coarse_select_workspace_size": ([dims_p], sz),
+        "vsa_coarse_select": ([P, P, P, i32, P, P, dims_p, P, sz, P], i32),
         "vsa_check_device_status": ([P], i32),
         "vsa_last_route": ([ctypes.POINTER(VsaRoute)], i32),
         "vsa_status_string": ([i32], ctypes.c_char_p),
@@ -76,7 +79,7 @@ def _load() -> ctypes.CDLL:
 
 _lib = _load()
 EXPORTED = ("vsa_block_sparse_workspace_size", "vsa_block_sparse_fwd", "vsa_block_sparse_fwd_noalloc",
-            "vsa_tile_layout",
+            "vsa_tile_layout", "vsa_coarse_select_workspace_size", "vsa_coarse_select",
             "vsa_validate_indices", "vsa_check_device_status", "vsa_last_route",
             "vsa_status_string", "vsa_version")
 
@@ -147,6 +150,20 @@ def vsa_tile_layout(q_tok, k_tok, v_tok, q_tile, k_tile, v_tile, row_to_token, B
         raise VsaError(st, "vsa_tile_layout")
 
 
+def vsa_coarse_select_workspace_size(dims: VsaDims) -> int:
+    return int(_lib.vsa_coarse_select_workspace_size(ctypes.byref(dims)))
+
+
+def vsa_coarse_select(q, k, block_sizes, topk: int, q2k_idx, q2k_num, dims: VsaDims, workspace: torch.Tensor,
+                      stream=None) -> None:
+    st = _lib.vsa_coarse_select(_ptr(q), _ptr(k), _ptr(block_sizes), int(topk), _ptr(q2k_idx), _ptr(q2k_num),
+                                ctypes.byref(dims), _ptr(workspace),
+                                workspace.numel() * workspace.element_size() if workspace is not None else 0,
+                                _stream(stream))
+    if st != VSA_OK:
+        raise VsaError(st, "vsa_coarse_select")
+
+
 def vsa_validate_indices(q2k_idx, q2k_num, block_sizes, dims: VsaDims, dev_status: torch.Tensor,
                          stream=None) -> None:
     st = _lib.vsa_validate_indices(_ptr(q2k_idx), _ptr(q2k_num), _ptr(block_sizes),
@@ -203,6 +220,28 @@ def block_sparse_attention(q, k, v, q2k_idx, q2k_num, block_sizes, tile: int,
     vsa_block_sparse_fwd(q, k, v, q2k_idx, q2k_num.contiguous(), block_sizes.contiguous(), out, lse,
                          dims, workspace, stream)
     return (out, lse) if want_lse else out
+
+
+def coarse_select(q, k, block_sizes, tile: int, topk: int, workspace: Optional[torch.Tensor] = None,
+                  stream=None):
+    """Coarse key-tile selection on tile-major bf16 ``q, k`` ``[B, H, NT*tile, D]``:
+    returns ``(q2k_idx [B, H, NT, topk] int32, q2k_num [B, H, NT] int32)``,
+    ready for ``block_sparse_attention`` with ``max_kv = topk``."""
+    _check_bf16_cuda(q, k)
+    B, H, Sp, D = q.shape
+    if Sp % tile:
+        raise ValueError("sequence length is not a multiple of the tile")
+    NT = Sp // tile
+    dims = make_dims(B, H, NT, tile, D, topk)
+    need = vsa_coarse_select_workspace_size(dims)
+    if need == 0:
+        raise VsaError(VSA_ERR_ARG, "vsa_coarse_select_workspace_size")
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    idx = torch.empty((B, H, NT, topk), dtype=torch.int32, device=q.device)
+    num = torch.empty((B, H, NT), dtype=torch.int32, device=q.device)
+    vsa_coarse_select(q, k, block_sizes.contiguous(), topk, idx, num, dims, workspace, stream)
+    return idx, num
 
 
 def tile_layout(q_tok, k_tok, v_tok, row_to_token, num_tiles: int, tile: int, stream=None):

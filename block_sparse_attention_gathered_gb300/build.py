@@ -1,6 +1,6 @@
 """Builds the C-ABI library ``_build/libvsa.so`` for sm_103a with nvcc.
 
-Three translation units compile in parallel with one ``-gencode`` each, then
+The translation units compile in parallel with one ``-gencode`` each, then
 link into a shared library with the CUDA runtime linked statically.  Nothing
 is installed outside the package directory.
 """
@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libvsa.so")
-SOURCES = ["vsa_api.cu", "vsa_attn.cu", "vsa_layout.cu", "vsa_noalloc.cu"]
+SOURCES = ["vsa_api.cu", "vsa_attn.cu", "vsa_layout.cu", "vsa_noalloc.cu", "vsa_select.cu"]
 GENCODE = "arch=compute_103a,code=sm_103a"
 
 
@@ -69,8 +69,7 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
     if verbose or ptxas_info:
         print(logs)
     tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [cc, "-shared", "-gencode", GENCODE, "-o", tmp, *[o for o, _ in results], "-lcuda"
-           ] if False else [cc, "-shared", "-gencode", GENCODE, "-o", tmp, *[o for o, _ in results]]
+    cmd = [cc, "-shared", "-gencode", GENCODE, "-o", tmp, *[o for o, _ in results]]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

@@ -228,7 +228,7 @@ using namespace vsa;
 
 extern "C" {
 
-int32_t vsa_version(void) { return 1000; }
+int32_t vsa_version(void) { return 1001; }
 
 const char *vsa_status_string(vsa_status s) {
     switch (s) {
@@ -401,6 +401,67 @@ vsa_status vsa_validate_indices(const int32_t *q2k_idx, const int32_t *q2k_num, 
     if (cudaGetLastError() != cudaSuccess) return VSA_ERR_CUDA;
     t_route = vsa_route{};
     t_route.kernel = VSA_KERNEL_VALIDATE;
+    return VSA_OK;
+}
+
+size_t vsa_coarse_select_workspace_size(const vsa_dims *dims) {
+    if (check_dims(dims) != VSA_OK) return 0;
+    return 2 * (size_t)dims->B * dims->H * dims->num_tiles * dims->head_dim * sizeof(float);
+}
+
+vsa_status vsa_coarse_select(const void *q, const void *k, const int32_t *block_sizes, int32_t topk,
+                             int32_t *q2k_idx, int32_t *q2k_num, const vsa_dims *dims, void *workspace,
+                             size_t workspace_bytes, vsa_stream_t stream) {
+    vsa_status st = check_dims(dims);
+    if (st != VSA_OK) return st;
+    if (!q || !k || !block_sizes || !q2k_num || topk < 0 || (!q2k_idx && topk > 0)) return VSA_ERR_ARG;
+    if (topk > VSA_MAX_TILES) return VSA_ERR_LIMITS;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(block_sizes, 4) || !aligned(q2k_num, 4) ||
+        (q2k_idx && !aligned(q2k_idx, 4)))
+        return VSA_ERR_ALIGN;
+    const size_t need = vsa_coarse_select_workspace_size(dims);
+    if (!workspace || workspace_bytes < need) return VSA_ERR_WORKSPACE;
+    if (!aligned(workspace, 16)) return VSA_ERR_ALIGN;
+    int dev = 0;
+    if ((st = current_device(&dev)) != VSA_OK) return st;
+    DeviceCache &dc = g_dev[dev];
+    constexpr unsigned kSelectBit = 1u << 4;
+    if (!(dc.attn_prepared.load(std::memory_order_acquire) & kSelectBit)) {
+        if (select_prepare() != cudaSuccess) {
+            cudaGetLastError();
+            return VSA_ERR_CUDA;
+        }
+        dc.attn_prepared.fetch_or(kSelectBit, std::memory_order_acq_rel);
+    }
+    SelectParams p;
+    p.q = q;
+    p.k = k;
+    p.block_sizes = block_sizes;
+    const size_t means = (size_t)dims->B * dims->H * dims->num_tiles * dims->head_dim;
+    p.qm = reinterpret_cast<float *>(workspace);
+    p.km = p.qm + means;
+    p.q2k_idx = q2k_idx;
+    p.q2k_num = q2k_num;
+    p.status = dc.status_ptr.load(std::memory_order_acquire);
+    p.B = dims->B;
+    p.H = dims->H;
+    p.NT = dims->num_tiles;
+    p.T = dims->tile;
+    p.D = dims->head_dim;
+    p.topk = topk;
+    if (launch_select(p, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return VSA_ERR_CUDA;
+    }
+    const int w = select_warps(p.NT, p.D);
+    t_route = vsa_route{};
+    t_route.kernel = VSA_KERNEL_SELECT;
+    t_route.tile = p.T;
+    t_route.head_dim = p.D;
+    t_route.grid = (p.NT + w - 1) / w * p.B * p.H;
+    t_route.block = 32 * w;
+    t_route.work_items = (int64_t)p.B * p.H * p.NT;
+    t_route.smem_bytes = (int32_t)select_smem_bytes(p.NT, p.D, w);
     return VSA_OK;
 }
 

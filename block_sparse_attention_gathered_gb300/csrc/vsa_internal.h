@@ -65,4 +65,23 @@ struct LayoutParams {
 
 cudaError_t launch_layout(const LayoutParams &p, int num_sms, cudaStream_t stream);
 
+// Coarse key-tile selection (vsa_select.cu).
+constexpr uint32_t kSelectSmemLimit = 232448;  // 227 KB opt-in per CTA
+
+struct SelectParams {
+    const void *q, *k;           // bf16 tile-major [B*H*NT*T, D]
+    const int32_t *block_sizes;  // [NT]
+    float *qm, *km;              // workspace: fp32 tile means [B*H*NT, D]
+    int32_t *q2k_idx;            // [B*H*NT, topk]
+    int32_t *q2k_num;            // [B*H*NT]
+    int32_t *status;             // device status word
+    int32_t B, H, NT, T, D, topk;
+};
+
+// Query tiles (warps) per select CTA so that the per-warp score rows fit.
+int select_warps(int NT, int D);
+size_t select_smem_bytes(int NT, int D, int warps);
+cudaError_t select_prepare();
+cudaError_t launch_select(const SelectParams &p, cudaStream_t stream);
+
 }  // namespace vsa

@@ -90,6 +90,7 @@ typedef struct {
 #define VSA_KERNEL_ATTN_TCGEN05 1
 #define VSA_KERNEL_LAYOUT 2
 #define VSA_KERNEL_VALIDATE 3
+#define VSA_KERNEL_SELECT 4
 
 /* Bytes of workspace vsa_block_sparse_fwd needs for `dims` (the on-device work
  * order and its counter).  Returns 0 when `dims` is invalid. */
@@ -183,6 +184,42 @@ vsa_status vsa_tile_layout(const void *q_tok, const void *k_tok, const void *v_t
 vsa_status vsa_validate_indices(const int32_t *q2k_idx, const int32_t *q2k_num,
                                 const int32_t *block_sizes, const vsa_dims *dims,
                                 int32_t *dev_status, vsa_stream_t stream);
+
+/*
+ * Coarse key-tile selection: produces the q2k_idx / q2k_num that
+ * vsa_block_sparse_fwd consumes.  The FastVideo kernel page names video
+ * sparse attention and its block-sparse fine stage (commit adding the sm_121a
+ * tile-128 forward; "Wan VSA inference" in the fused tile_to_bhsd commit) but
+ * not the coarse stage's arithmetic; this is its plain reading:
+ *   1. every non-empty tile t is pooled to the mean of its valid rows
+ *      (rows r < block_sizes[t] of q and of k; padding rows are never read);
+ *   2. query tile t scores key tile j by the dot product of the two means;
+ *   3. query tile t keeps the topk key tiles with the largest scores (ties to
+ *      the smaller index), never an empty key tile or a NaN score; fewer if
+ *      fewer qualify; none for an empty query tile.
+ * The kept set is decided in fp32 with a fixed arithmetic -- each mean summed
+ * over rows in order then divided once, each score summed over d in order of
+ * fused multiply-adds -- so it is reproducible bit for bit.
+ *
+ *   q, k         bf16 [B, H, NT*tile, D] tile-major (the attention inputs)
+ *   block_sizes  int32 [NT], each in [0, tile]; a size outside that range
+ *                is never read past the tile, makes the tile unselectable and
+ *                flags VSA_ERR_INDEX in the device status word
+ *   topk         kept tiles per query tile, 0 <= topk <= VSA_MAX_TILES
+ *   q2k_idx      int32 [B, H, NT, topk] out: kept tiles in ascending order,
+ *                -1 after the last one (may be NULL when topk == 0)
+ *   q2k_num      int32 [B, H, NT] out: number kept
+ *   dims         B, H, num_tiles, tile, head_dim as for the forward pass
+ *                (max_kv and scale are not used)
+ *   workspace    vsa_coarse_select_workspace_size(dims) bytes of device
+ *                scratch (the fp32 tile means), 16-byte aligned
+ * The outputs feed vsa_block_sparse_fwd directly with max_kv = topk.
+ */
+size_t vsa_coarse_select_workspace_size(const vsa_dims *dims);
+
+vsa_status vsa_coarse_select(const void *q, const void *k, const int32_t *block_sizes, int32_t topk,
+                             int32_t *q2k_idx, int32_t *q2k_num, const vsa_dims *dims, void *workspace,
+                             size_t workspace_bytes, vsa_stream_t stream);
 
 /* Synchronises `stream`, then reads and clears the current device's status
  * word: VSA_OK, VSA_ERR_INDEX or VSA_ERR_TIMEOUT (the most severe seen since

@@ -38,7 +38,7 @@ def test_exports_every_declared_symbol(vsa):
     for name in declared:
         assert hasattr(lib, name), name
     assert set(declared) == set(vsa.EXPORTED)
-    assert vsa.vsa_version() == 1000
+    assert vsa.vsa_version() == 1001
 
 
 def test_status_strings(vsa):
@@ -113,6 +113,31 @@ def test_validate_argument_errors(vsa):
     V = vsa.library().vsa_validate_indices
     assert V(P(FAKE), P(FAKE), P(FAKE), ctypes.byref(d), None, None) == vsa.VSA_ERR_ARG
     assert V(P(FAKE), P(FAKE + 2), P(FAKE), ctypes.byref(d), P(FAKE), None) == vsa.VSA_ERR_ALIGN
+
+
+def test_coarse_select_argument_errors(vsa):
+    P = ctypes.c_void_p
+    d = vsa.make_dims(1, 2, 4, 64, 64, 0)
+    S = vsa.library().vsa_coarse_select
+    need = vsa.vsa_coarse_select_workspace_size(d)
+    assert need == 2 * 1 * 2 * 4 * 64 * 4  # fp32 tile means of q and k
+
+    def f(q=FAKE, k=FAKE, bs=FAKE, topk=2, idx=FAKE, num=FAKE, dims=d, ws=FAKE, ws_bytes=need):
+        return S(P(q) if q else None, P(k) if k else None, P(bs) if bs else None, topk,
+                 P(idx) if idx else None, P(num) if num else None, ctypes.byref(dims),
+                 P(ws) if ws else None, ws_bytes, None)
+
+    assert f(q=0) == vsa.VSA_ERR_ARG
+    assert f(num=0) == vsa.VSA_ERR_ARG
+    assert f(topk=-1) == vsa.VSA_ERR_ARG
+    assert f(idx=0) == vsa.VSA_ERR_ARG                    # topk > 0 needs q2k_idx
+    assert f(topk=8193) == vsa.VSA_ERR_LIMITS
+    assert f(dims=vsa.make_dims(1, 2, 4, 48, 64, 0)) == vsa.VSA_ERR_ARG
+    assert f(k=FAKE + 8) == vsa.VSA_ERR_ALIGN
+    assert f(idx=FAKE + 2) == vsa.VSA_ERR_ALIGN
+    assert f(ws=0) == vsa.VSA_ERR_WORKSPACE
+    assert f(ws_bytes=need - 1) == vsa.VSA_ERR_WORKSPACE
+    assert vsa.vsa_coarse_select_workspace_size(vsa.make_dims(256, 256, 4, 64, 64, 0)) == 0
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
