@@ -453,15 +453,15 @@ vsa_status vsa_coarse_select(const void *q, const void *k, const int32_t *block_
         cudaGetLastError();
         return VSA_ERR_CUDA;
     }
-    const int w = select_warps(p.NT, p.D);
+    const int rows = select_rows(p.NT, p.D);
     t_route = vsa_route{};
     t_route.kernel = VSA_KERNEL_SELECT;
     t_route.tile = p.T;
     t_route.head_dim = p.D;
-    t_route.grid = (p.NT + w - 1) / w * p.B * p.H;
-    t_route.block = 32 * w;
+    t_route.grid = (p.NT + rows - 1) / rows * p.B * p.H;
+    t_route.block = 32 * select_warps(p.NT, p.D);
     t_route.work_items = (int64_t)p.B * p.H * p.NT;
-    t_route.smem_bytes = (int32_t)select_smem_bytes(p.NT, p.D, w);
+    t_route.smem_bytes = (int32_t)select_smem_bytes(p.NT, p.D, rows);
     return VSA_OK;
 }
 

@@ -78,9 +78,10 @@ struct SelectParams {
     int32_t B, H, NT, T, D, topk;
 };
 
-// Query tiles (warps) per select CTA so that the per-warp score rows fit.
+// Warps and query tiles (score rows) per select CTA, chosen so the score rows fit.
 int select_warps(int NT, int D);
-size_t select_smem_bytes(int NT, int D, int warps);
+int select_rows(int NT, int D);
+size_t select_smem_bytes(int NT, int D, int rows);
 cudaError_t select_prepare();
 cudaError_t launch_select(const SelectParams &p, cudaStream_t stream);
 

@@ -19,11 +19,12 @@
 //   pool_kernel    one thread per 16-byte column vector of one tile of Q or K,
 //                  walking the tile's valid rows in order with 16 rows of loads
 //                  in flight.  HBM-bound (reads every valid row of Q and K once).
-//   select_kernel  one warp per query tile: scores against all key tiles into
-//                  shared memory (key means staged in 64-tile chunks, two key
-//                  tiles per lane, 16-byte shared loads), then a
-//                  4-pass 8-bit radix select of the topk-th largest score and
-//                  an ascending emit with ballots.
+//   select_kernel  four query tiles per warp, two key tiles per lane: scores
+//                  against all key tiles into shared memory (key means staged
+//                  in 64-tile chunks, each 16-byte load serving four scores),
+//                  then per query tile a bitwise search (per-lane counts, one
+//                  warp reduction per bit) for the topk-th largest score and an
+//                  ascending emit with ballots.
 #include "vsa_internal.h"
 
 namespace vsa {
@@ -99,154 +100,66 @@ __device__ __forceinline__ uint32_t score_key(float s, bool candidate) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Dynamic shared memory: query means [W][D], key-mean chunk [64][D+4],
-// keys [W][NT], histograms [W][256].
-template <int D>
-__global__ void select_kernel(const float *__restrict__ qm, const float *__restrict__ km,
-                              const int32_t *__restrict__ block_sizes, int32_t *__restrict__ q2k_idx,
-                              int32_t *__restrict__ q2k_num, int NT, int T, int topk) {
-    constexpr int KS = D + 4;  // padded key-mean row: 16-byte aligned, no bank conflicts on 16-byte loads
-    extern __shared__ __align__(16) float sm[];
-    const int nw = blockDim.x >> 5;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t bh = blockIdx.y;
-    const int t0 = blockIdx.x * nw;
-    float *sq = sm;                                   // [nw][D]
-    float *skc = sq + nw * D;                         // [64][KS]
-    uint32_t *keys = reinterpret_cast<uint32_t *>(skc + kSelectKeyChunk * KS);  // [nw][NT]
-    uint32_t *hist = keys + (size_t)nw * NT;          // [nw][256]
-    const int t = t0 + warp;
-    const bool live = t < NT;
+constexpr int kKeyRegs = 16;  // most keys per lane held in registers for the top-k search (NT <= 512)
 
-    for (int i = threadIdx.x; i < nw * D; i += blockDim.x) {
-        const int w = i / D, tt = t0 + w;
-        sq[i] = tt < NT ? qm[(bh * NT + tt) * D + (i - w * D)] : 0.f;
-    }
-    uint32_t *mykeys = keys + (size_t)warp * NT;
-    // ---- scores of query tile t against every key tile, as keys.  Each lane
-    // scores two key tiles of a 64-tile chunk; every score is a sum over d in
-    // order of fused multiply-adds.
-    for (int j0 = 0; j0 < NT; j0 += kSelectKeyChunk) {
-        __syncthreads();  // previous chunk consumed (and sq written, first time)
-        const int nj = NT - j0 < kSelectKeyChunk ? NT - j0 : kSelectKeyChunk;
-        for (int i = threadIdx.x; i < nj * (D / 4); i += blockDim.x) {
-            const int jj = i / (D / 4), d4 = i - jj * (D / 4);
-            reinterpret_cast<float4 *>(skc + jj * KS)[d4] =
-                reinterpret_cast<const float4 *>(km + (bh * NT + j0 + jj) * D)[d4];
-        }
-        __syncthreads();
-        if (live && lane < nj) {
-            const float4 *a = reinterpret_cast<const float4 *>(sq + warp * D);
-            const float4 *b0 = reinterpret_cast<const float4 *>(skc + lane * KS);
-            const float4 *b1 = reinterpret_cast<const float4 *>(skc + (lane + 32) * KS);
-            const bool two = lane + 32 < nj;
-            float s0 = 0.f, s1 = 0.f;
-#pragma unroll 8
-            for (int d4 = 0; d4 < D / 4; ++d4) {
-                const float4 x = a[d4], y = b0[d4];
-                s0 = __fmaf_rn(x.x, y.x, s0);
-                s0 = __fmaf_rn(x.y, y.y, s0);
-                s0 = __fmaf_rn(x.z, y.z, s0);
-                s0 = __fmaf_rn(x.w, y.w, s0);
-                if (two) {
-                    const float4 z = b1[d4];
-                    s1 = __fmaf_rn(x.x, z.x, s1);
-                    s1 = __fmaf_rn(x.y, z.y, s1);
-                    s1 = __fmaf_rn(x.z, z.z, s1);
-                    s1 = __fmaf_rn(x.w, z.w, s1);
-                }
-            }
-            const int j = j0 + lane;
-            const int n0 = __ldg(block_sizes + j);
-            mykeys[j] = score_key(s0, n0 > 0 && n0 <= T);
-            if (two) {
-                const int n1 = __ldg(block_sizes + j + 32);
-                mykeys[j + 32] = score_key(s1, n1 > 0 && n1 <= T);
-            }
-        }
-    }
-    __syncwarp();
-    if (!live) return;
-
-    // ---- number kept: every candidate up to topk; none for an empty query tile
-    int n_cand = 0;
-    for (int j = lane; j < NT; j += 32) n_cand += mykeys[j] != 0u;
+// Writes the topk best of one row of keys (ascending tile order, -1 after)
+// and returns how many were kept.  The kk-th largest key is found one bit at
+// a time from the top: among keys that share the bits decided so far, those
+// with bit b set are larger than those with it clear.  KR > 0 keeps the row's
+// keys in KR registers per lane (NT <= 32 * KR) and counts in four
+// independent partial sums; KR == 0 re-reads them from shared memory on every
+// pass.
+template <int KR>
+__device__ __forceinline__ int row_topk(const uint32_t *rk, int NT, int topk, int nt_tok, int T, int32_t *out,
+                                        int lane) {
+    uint32_t kr[KR > 0 ? KR : 1];
+    const int chunks = (NT + 31) / 32;
+    unsigned n_cand = 0;
+    if constexpr (KR > 0) {
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) n_cand += __shfl_xor_sync(0xffffffffu, n_cand, o);
-    const int nt_tok = __ldg(block_sizes + t);
-    const int kk = (nt_tok > 0 && nt_tok <= T) ? (topk < n_cand ? topk : n_cand) : 0;
-    int32_t *out = q2k_idx + (bh * NT + t) * (int64_t)topk;
-    if (lane == 0) q2k_num[bh * NT + t] = kk;
+        for (int c = 0; c < KR; ++c) {
+            const int j = c * 32 + lane;
+            kr[c] = j < NT ? rk[j] : 0u;
+            n_cand += kr[c] != 0u;
+        }
+    } else {
+        for (int c = 0; c < chunks; ++c) {
+            const int j = c * 32 + lane;
+            n_cand += j < NT && rk[j] != 0u;
+        }
+    }
+    n_cand = __reduce_add_sync(0xffffffffu, n_cand);
+    const int kk = (nt_tok > 0 && nt_tok <= T) ? (topk < (int)n_cand ? topk : (int)n_cand) : 0;
     if (kk == 0) {
         for (int i = lane; i < topk; i += 32) out[i] = -1;
-        return;
+        return 0;
     }
-
-    // ---- radix select of the kk-th largest key, 8 bits per pass from the top
-    uint32_t *h = hist + warp * 256;
-    uint32_t prefix = 0u;  // digits decided so far
-    int need = kk;         // keys still to take at or below the current prefix
+    uint32_t prefix = 0u;
+    int need = kk;  // keys still to take at or below the current prefix
 #pragma unroll 1
-    for (int shift = 24; shift >= 0; shift -= 8) {
-        __syncwarp();  // every lane has read the previous pass's bins
-        for (int i = lane; i < 256; i += 32) h[i] = 0u;
-        __syncwarp();
-        const uint32_t hi_mask = shift == 24 ? 0u : (0xffffffffu << (shift + 8));
-        // lanes with the same digit add their count once (scores of a row often
-        // share their leading digits, which would serialise plain atomics)
-        for (int j0 = 0; j0 < NT; j0 += 32) {
-            const int j = j0 + lane;
-            const uint32_t key = j < NT ? mykeys[j] : 0u;
-            const bool act = key != 0u && (key & hi_mask) == prefix;
-            const uint32_t dig = act ? ((key >> shift) & 255u) : 256u;
-            const uint32_t peers = __match_any_sync(0xffffffffu, dig);
-            if (act && lane == __ffs(peers) - 1) atomicAdd(&h[dig], (uint32_t)__popc(peers));
-        }
-        __syncwarp();
-        // lane l owns digits 255-8l .. 248-8l (descending); find the digit where
-        // the count of keys at or above it first reaches `need`
-        uint32_t c[8];
-        uint32_t own = 0;
+    for (int b = 31; b >= 0; --b) {
+        const uint32_t m = 0xffffffffu << b, cand = prefix | (1u << b);
+        // a key with the candidate prefix is non-zero, so no separate test for 0
+        unsigned c4[4] = {0u, 0u, 0u, 0u};
+        if constexpr (KR > 0) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            c[i] = h[255 - 8 * lane - i];
-            own += c[i];
-        }
-        uint32_t incl = own;  // inclusive scan over lanes (higher digits first)
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += v;
-        }
-        const uint32_t excl = incl - own;
-        const bool here = excl < (uint32_t)need && incl >= (uint32_t)need;
-        const uint32_t who = __ballot_sync(0xffffffffu, here);
-        const int src = __ffs(who) - 1;
-        uint32_t digit = 0, above = 0;
-        if (lane == src) {
-            uint32_t run = excl;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                if (run + c[i] >= (uint32_t)need) {
-                    digit = 255u - 8u * lane - i;
-                    above = run;
-                    break;
-                }
-                run += c[i];
+            for (int c = 0; c < KR; ++c) c4[c & 3] += (kr[c] & m) == cand;
+        } else {
+            for (int c = 0; c < chunks; ++c) {
+                const int j = c * 32 + lane;
+                c4[0] += j < NT && (rk[j] & m) == cand;
             }
         }
-        digit = __shfl_sync(0xffffffffu, digit, src);
-        above = __shfl_sync(0xffffffffu, above, src);
-        prefix |= digit << shift;
-        need -= (int)above;
+        const unsigned cnt = __reduce_add_sync(0xffffffffu, (c4[0] + c4[1]) + (c4[2] + c4[3]));
+        if ((int)cnt >= need) prefix = cand;
+        else need -= (int)cnt;
     }
-    // prefix is now the kk-th largest key; take every larger key and the first
-    // `need` keys equal to it, in ascending tile order
-    int base = 0, eq_seen = 0;
+    // every larger key and the first `need` keys equal to it, ascending
     const uint32_t lt = (1u << lane) - 1u;
-    for (int j0 = 0; j0 < NT; j0 += 32) {
-        const int j = j0 + lane;
-        const uint32_t key = j < NT ? mykeys[j] : 0u;
+    int base = 0, eq_seen = 0;
+    for (int c = 0; c < chunks; ++c) {
+        const int j = c * 32 + lane;
+        const uint32_t key = j < NT ? rk[j] : 0u;
         const bool gt = key > prefix, eq = key == prefix && key != 0u;
         const uint32_t beq = __ballot_sync(0xffffffffu, eq);
         const bool sel = gt || (eq && eq_seen + __popc(beq & lt) < need);
@@ -256,27 +169,148 @@ __global__ void select_kernel(const float *__restrict__ qm, const float *__restr
         eq_seen += __popc(beq);
     }
     for (int i = kk + lane; i < topk; i += 32) out[i] = -1;
+    return kk;
+}
+
+// Dynamic shared memory: query means [WARPS*QPW][D], key-mean chunk
+// [64][D+4], keys [WARPS*QPW][NT].
+template <int D, int QPW, int WARPS>
+__global__ void __launch_bounds__(WARPS * 32)
+    select_kernel(const float *__restrict__ qm, const float *__restrict__ km, const int32_t *__restrict__ block_sizes,
+                  int32_t *__restrict__ q2k_idx, int32_t *__restrict__ q2k_num, int NT, int T, int topk) {
+    constexpr int KS = D + 4;  // padded key-mean row: 16-byte aligned, no bank conflicts on 16-byte loads
+    constexpr int ROWS = WARPS * QPW;
+    constexpr int LOADS = kSelectKeyChunk * (D / 4) / (WARPS * 32);  // float4 copies per thread per chunk
+    extern __shared__ __align__(16) float sm[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t bh = blockIdx.y;
+    const int t0 = blockIdx.x * ROWS;
+    float *sq = sm;                                                              // [ROWS][D]
+    float *skc = sq + ROWS * D;                                                  // [64][KS]
+    uint32_t *keys = reinterpret_cast<uint32_t *>(skc + kSelectKeyChunk * KS);  // [ROWS][NT]
+
+    for (int i = threadIdx.x; i < ROWS * D; i += WARPS * 32) {
+        const int w = i / D, tt = t0 + w;
+        sq[i] = tt < NT ? qm[(bh * NT + tt) * D + (i - w * D)] : 0.f;
+    }
+    // ---- scores: each warp takes QPW query tiles, each lane two key tiles of
+    // a 64-tile chunk, so one 16-byte load of a key mean serves QPW scores.
+    // Every score is a sum over d in order of fused multiply-adds.
+    const int r0 = warp * QPW;  // first row (query tile) of this warp
+    // key means of the next chunk travel in registers while the current chunk
+    // is scored, so the global-load latency overlaps the arithmetic
+    float4 tmp[LOADS];
+    auto fetch = [&](int j0) {
+        const int nj = NT - j0 < kSelectKeyChunk ? NT - j0 : kSelectKeyChunk;
+#pragma unroll
+        for (int u = 0; u < LOADS; ++u) {
+            const int i = threadIdx.x + u * WARPS * 32;
+            const int jj = i / (D / 4);
+            tmp[u] = jj < nj ? reinterpret_cast<const float4 *>(km + (bh * NT + j0 + jj) * D)[i - jj * (D / 4)]
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    };
+    fetch(0);
+    for (int j0 = 0; j0 < NT; j0 += kSelectKeyChunk) {
+        __syncthreads();  // previous chunk consumed (and sq written, first time)
+#pragma unroll
+        for (int u = 0; u < LOADS; ++u) {
+            const int i = threadIdx.x + u * WARPS * 32;
+            const int jj = i / (D / 4);
+            reinterpret_cast<float4 *>(skc + jj * KS)[i - jj * (D / 4)] = tmp[u];
+        }
+        __syncthreads();
+        if (j0 + kSelectKeyChunk < NT) fetch(j0 + kSelectKeyChunk);
+        const int nj = NT - j0 < kSelectKeyChunk ? NT - j0 : kSelectKeyChunk;
+        float acc0[QPW], acc1[QPW];
+#pragma unroll
+        for (int q = 0; q < QPW; ++q) acc0[q] = acc1[q] = 0.f;
+        const float4 *b0 = reinterpret_cast<const float4 *>(skc + lane * KS);
+        const float4 *b1 = reinterpret_cast<const float4 *>(skc + (lane + 32) * KS);
+#pragma unroll 4
+        for (int d4 = 0; d4 < D / 4; ++d4) {
+            const float4 y = b0[d4], z = b1[d4];
+#pragma unroll
+            for (int q = 0; q < QPW; ++q) {
+                const float4 x = reinterpret_cast<const float4 *>(sq + (r0 + q) * D)[d4];
+                acc0[q] = __fmaf_rn(x.x, y.x, acc0[q]);
+                acc0[q] = __fmaf_rn(x.y, y.y, acc0[q]);
+                acc0[q] = __fmaf_rn(x.z, y.z, acc0[q]);
+                acc0[q] = __fmaf_rn(x.w, y.w, acc0[q]);
+                acc1[q] = __fmaf_rn(x.x, z.x, acc1[q]);
+                acc1[q] = __fmaf_rn(x.y, z.y, acc1[q]);
+                acc1[q] = __fmaf_rn(x.z, z.z, acc1[q]);
+                acc1[q] = __fmaf_rn(x.w, z.w, acc1[q]);
+            }
+        }
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+            const int jj = lane + 32 * h2;
+            if (jj < nj) {
+                const int j = j0 + jj;
+                const int n = __ldg(block_sizes + j);
+                const bool cand = n > 0 && n <= T;
+#pragma unroll
+                for (int q = 0; q < QPW; ++q)
+                    keys[(size_t)(r0 + q) * NT + j] = score_key(h2 ? acc1[q] : acc0[q], cand);
+            }
+        }
+    }
+    __syncwarp();
+
+    // ---- top-k of each of this warp's rows
+    for (int q = 0; q < QPW; ++q) {
+        const int t = t0 + r0 + q;
+        if (t >= NT) break;
+        const uint32_t *rk = keys + (size_t)(r0 + q) * NT;
+        int32_t *out = q2k_idx + (bh * NT + t) * (int64_t)topk;
+        const int nt_tok = __ldg(block_sizes + t);
+        int kk;
+        if (NT <= 32 * 4) kk = row_topk<4>(rk, NT, topk, nt_tok, T, out, lane);
+        else if (NT <= 32 * 8) kk = row_topk<8>(rk, NT, topk, nt_tok, T, out, lane);
+        else if (NT <= 32 * 12) kk = row_topk<12>(rk, NT, topk, nt_tok, T, out, lane);
+        else if (NT <= 32 * kKeyRegs) kk = row_topk<kKeyRegs>(rk, NT, topk, nt_tok, T, out, lane);
+        else kk = row_topk<0>(rk, NT, topk, nt_tok, T, out, lane);
+        if (lane == 0) q2k_num[bh * NT + t] = kk;
+    }
 }
 
 }  // namespace
 
-size_t select_smem_bytes(int NT, int D, int warps) {
-    return sizeof(float) * ((size_t)warps * D + (size_t)kSelectKeyChunk * (D + 4)) +
-           sizeof(uint32_t) * ((size_t)warps * NT + (size_t)warps * 256);
+// Layouts of the select kernel: 4 warps x 4 query tiles per warp while their
+// score rows fit in shared memory, else 4 warps x 1 query tile.
+struct SelectShape {
+    int warps, qpw;
+};
+
+SelectShape select_shape(int NT, int D) {
+    if (select_smem_bytes(NT, D, 4 * 4) <= kSelectSmemLimit) return {4, 4};
+    return {4, 1};
 }
 
-int select_warps(int NT, int D) {
-    int w = 8;
-    while (w > 1 && select_smem_bytes(NT, D, w) > kSelectSmemLimit) --w;
-    return w;
+size_t select_smem_bytes(int NT, int D, int rows) {
+    return sizeof(float) * ((size_t)rows * D + (size_t)kSelectKeyChunk * (D + 4)) + sizeof(uint32_t) * (size_t)rows * NT;
+}
+
+int select_warps(int NT, int D) { return select_shape(NT, D).warps; }
+
+int select_rows(int NT, int D) {
+    const SelectShape sh = select_shape(NT, D);
+    return sh.warps * sh.qpw;
+}
+
+template <int D, int QPW, int WARPS>
+cudaError_t select_attr() {
+    return cudaFuncSetAttribute(select_kernel<D, QPW, WARPS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)kSelectSmemLimit);
 }
 
 cudaError_t select_prepare() {
-    cudaError_t e = cudaFuncSetAttribute(select_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kSelectSmemLimit);
-    if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(select_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)kSelectSmemLimit);
+    cudaError_t e;
+    if ((e = select_attr<64, 4, 4>()) != cudaSuccess) return e;
+    if ((e = select_attr<128, 4, 4>()) != cudaSuccess) return e;
+    if ((e = select_attr<64, 1, 4>()) != cudaSuccess) return e;
+    return select_attr<128, 1, 4>();
 }
 
 cudaError_t launch_select(const SelectParams &p, cudaStream_t stream) {
@@ -288,15 +322,25 @@ cudaError_t launch_select(const SelectParams &p, cudaStream_t stream) {
         p.status, n_tiles, p.NT, p.T, Dv);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const int w = select_warps(p.NT, p.D);
-    dim3 grid((unsigned)((p.NT + w - 1) / w), (unsigned)(p.B * p.H));
-    const size_t smem = select_smem_bytes(p.NT, p.D, w);
-    if (p.D == 128)
-        select_kernel<128><<<grid, 32 * w, smem, stream>>>(p.qm, p.km, p.block_sizes, p.q2k_idx, p.q2k_num, p.NT,
-                                                             p.T, p.topk);
-    else
-        select_kernel<64><<<grid, 32 * w, smem, stream>>>(p.qm, p.km, p.block_sizes, p.q2k_idx, p.q2k_num, p.NT,
-                                                            p.T, p.topk);
+    const SelectShape sh = select_shape(p.NT, p.D);
+    const int rows = sh.warps * sh.qpw;
+    dim3 grid((unsigned)((p.NT + rows - 1) / rows), (unsigned)(p.B * p.H));
+    const size_t smem = select_smem_bytes(p.NT, p.D, rows);
+    if (sh.qpw == 4) {
+        if (p.D == 128)
+            select_kernel<128, 4, 4><<<grid, 128, smem, stream>>>(p.qm, p.km, p.block_sizes, p.q2k_idx, p.q2k_num,
+                                                                 p.NT, p.T, p.topk);
+        else
+            select_kernel<64, 4, 4><<<grid, 128, smem, stream>>>(p.qm, p.km, p.block_sizes, p.q2k_idx, p.q2k_num,
+                                                                p.NT, p.T, p.topk);
+    } else {
+        if (p.D == 128)
+            select_kernel<128, 1, 4><<<grid, 128, smem, stream>>>(p.qm, p.km, p.block_sizes, p.q2k_idx, p.q2k_num,
+                                                                 p.NT, p.T, p.topk);
+        else
+            select_kernel<64, 1, 4><<<grid, 128, smem, stream>>>(p.qm, p.km, p.block_sizes, p.q2k_idx, p.q2k_num,
+                                                                p.NT, p.T, p.topk);
+    }
     return cudaGetLastError();
 }
 
