@@ -219,6 +219,20 @@ def layout_bytes(w) -> int:
     return 3 * 2 * w.B * w.H * w.D * (w.S + w.Sp) + 4 * w.Sp
 
 
+def selected_flops(q2k_idx, q2k_num, block_sizes, D: int) -> int:
+    """4*D*sum over selected (b,h,t,j) of n_t*n_j for a selection given as tensors."""
+    bs = block_sizes.to(torch.int64)
+    B, H, NT, K = q2k_idx.shape
+    live = torch.arange(K)[None, None, None, :] < q2k_num[..., None].to(torch.int64)
+    nj = torch.where(live, bs[q2k_idx.clamp(min=0).to(torch.int64)], torch.zeros((), dtype=torch.int64))
+    return int(4 * D * (nj.sum(-1) * bs[None, None, :]).sum())
+
+
+def pooled_bytes(w) -> int:
+    """Bytes the tile pooling reads: every valid row of q and k once."""
+    return 2 * w.B * w.H * int(w.block_sizes.sum()) * w.D * 2
+
+
 def max_over_ranks(x: float, device) -> float:
     """The largest value of ``x`` over all ranks (``x`` itself on one rank)."""
     import torch.distributed as dist
@@ -256,7 +270,16 @@ def run_ours(args, cfg):
     tiles = [torch.empty((B, H, Sp, D), dtype=torch.bfloat16, device=dev) for _ in range(3)]
     out = torch.empty((B, H, Sp, D), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((B, H, Sp), dtype=torch.float32, device=dev) if w.want_lse else None
-    dims = vsa.make_dims(B, H, NT, T, D, w.max_kv, w.scale)
+    select = bool(args.select)
+    if select:
+        # the step also selects the key tiles on the GPU (coarse stage), and
+        # the attention runs on that selection
+        topk = int(w.notes["topk"])
+        sel_dims = vsa.make_dims(B, H, NT, T, D, topk)
+        sel_ws = torch.empty(vsa.vsa_coarse_select_workspace_size(sel_dims), dtype=torch.uint8, device=dev)
+        idx = torch.empty((B, H, NT, topk), dtype=torch.int32, device=dev)
+        num = torch.empty((B, H, NT), dtype=torch.int32, device=dev)
+    dims = vsa.make_dims(B, H, NT, T, D, idx.shape[-1], w.scale)
     ws = torch.empty(vsa.vsa_block_sparse_workspace_size(dims), dtype=torch.uint8, device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)  # > 129 MB L2
     stream = torch.cuda.current_stream()
@@ -265,15 +288,21 @@ def run_ours(args, cfg):
         return torch.cuda.Event(enable_timing=True)
 
     def step(qt, kt, vt):
-        """One pass of the hot path; returns events around the layout and the
-        attention call (recorded on the launching stream)."""
+        """One pass of the hot path; returns events after the layout, after the
+        selection (the same event when there is none) and after the attention
+        call (recorded on the launching stream)."""
         l0, l1, a1 = ev(), ev(), ev()
         l0.record(stream)
         vsa.vsa_tile_layout(qt, kt, vt, tiles[0], tiles[1], tiles[2], r2t, B, S, H, D, NT, T, stream)
         l1.record(stream)
+        s1 = l1
+        if select:
+            vsa.vsa_coarse_select(tiles[0], tiles[1], bs, topk, idx, num, sel_dims, sel_ws, stream)
+            s1 = ev()
+            s1.record(stream)
         vsa.vsa_block_sparse_fwd(tiles[0], tiles[1], tiles[2], idx, num, bs, out, lse, dims, ws, stream)
         a1.record(stream)
-        return l0, l1, a1
+        return l0, l1, s1, a1
 
     def barrier():
         if world > 1:
@@ -286,6 +315,8 @@ def run_ours(args, cfg):
     barrier()
     if vsa.vsa_check_device_status() != 0:
         raise RuntimeError("device status error during warm-up")
+    if select:  # effective FLOPs of the selection the GPU made
+        eff = selected_flops(idx.cpu(), num.cpu(), w.block_sizes, D)
 
     # ---------------------------------------------------------------- device-timed steps
     marks = []
@@ -295,9 +326,10 @@ def run_ours(args, cfg):
             flush.zero_()  # L2 flush, outside the timed events
             marks.append(step(q_tok, k_tok, v_tok))
         barrier()
-    step_ms = [a.elapsed_time(c) for a, b, c in marks]
-    layout_ms = [a.elapsed_time(b) for a, b, c in marks]
-    attn_ms = [b.elapsed_time(c) for a, b, c in marks]
+    step_ms = [m[0].elapsed_time(m[3]) for m in marks]
+    layout_ms = [m[0].elapsed_time(m[1]) for m in marks]
+    select_ms = [m[1].elapsed_time(m[2]) for m in marks] if select else None
+    attn_ms = [m[2].elapsed_time(m[3]) for m in marks]
     ms = max_over_ranks(sum(step_ms) / len(step_ms), dev)
     if vsa.vsa_check_device_status() != 0:
         raise RuntimeError("device status error in the timed region")
@@ -305,13 +337,16 @@ def run_ours(args, cfg):
     # ---------------------------------------------------------------- end to end from host buffers
     hq, hk, hv = (x.pin_memory() for x in (w.q_tok, w.k_tok, w.v_tok))
     hidx, hnum, hbs, hr2t = (x.pin_memory() for x in (w.q2k_idx, w.q2k_num, w.block_sizes, w.row_to_token))
+    # with the GPU selection the selection arrays are outputs, not inputs
+    h_in = ((q_tok, hq), (k_tok, hk), (v_tok, hv), (bs, hbs), (r2t, hr2t)) + \
+        (() if select else ((idx, hidx), (num, hnum)))
     hout = torch.empty((B, H, Sp, D), dtype=torch.bfloat16).pin_memory()
     hlse = torch.empty((B, H, Sp), dtype=torch.float32).pin_memory() if lse is not None else None
-    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hidx, hnum, hbs, hr2t))
+    h2d = sum(h_.numel() * h_.element_size() for _, h_ in h_in)
     d2h = hout.numel() * 2 + (hlse.numel() * 4 if hlse is not None else 0)
 
     def e2e_step():
-        for d_, h_ in ((q_tok, hq), (k_tok, hk), (v_tok, hv), (idx, hidx), (num, hnum), (bs, hbs), (r2t, hr2t)):
+        for d_, h_ in h_in:
             d_.copy_(h_, non_blocking=True)
         step(q_tok, k_tok, v_tok)
         hout.copy_(out, non_blocking=True)
@@ -357,11 +392,21 @@ def run_ours(args, cfg):
                                 "peak_source": f"{src} HBM copy", "kernel": "layout_kernel"},
             "e2e": {"value": aggregate(eff, world, e2e_ms), "unit": UNIT, "ms_per_step": e2e_ms,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            # per step: tile layout, work-ordering sort, attention
-            "gpu_launches": 3 * args.steps,
+            # per step: tile layout, [tile pooling, selection,] work-ordering sort, attention
+            "gpu_launches": (5 if select else 3) * args.steps,
             "clocks": clk.summary(),
             "route": route,
         }
+        if select:
+            sel_avg = sum(select_ms) / len(select_ms)
+            pool_bytes = pooled_bytes(w)
+            line["select_ms"] = sel_avg
+            line["select_roofline"] = {
+                "bound": "hbm", "achieved": pool_bytes / (sel_avg / 1e3) / 1e9, "peak": hbm, "unit": "GB/s",
+                "frac": pool_bytes / (sel_avg / 1e3) / 1e9 / hbm, "bytes": pool_bytes,
+                "kernel": "pool_kernel + select_kernel (bytes: valid rows of q and k read once)"}
+            line["config"]["step"] = "tile layout + coarse top-k selection + work ordering + tcgen05 attention"
+            line["config"]["topk"] = topk
         if not args.no_cpu_baseline and world == 1:
             line["cpu_baseline"] = cpu_oracle_run(w, args.cpu_seconds)
         print(json.dumps(line), flush=True)
@@ -378,8 +423,12 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", type=int, default=5, choices=[2, 4, 5])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--select", action="store_true",
+                    help="video-grid workload only: select the key tiles on the GPU inside the step")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     args = ap.parse_args()
+    if args.select and args.config != 4:
+        ap.error("--select needs the video-grid workload (--config 4)")
     if args.impl == "reference":
         run_reference(args, args.config)
     else:

@@ -50,3 +50,13 @@ def test_single_process_needs_no_group():
     import bench
     assert bench.max_over_ranks(1.25, torch.device("cpu")) == 1.25
     assert bench.aggregate(1e12, 1, 1.0) == pytest.approx(1000.0)
+
+
+def test_selected_flops_matches_workload_count():
+    # the bench recounts effective FLOPs from a selection held in tensors (the
+    # GPU's own selection); on the seeded workloads it must equal their count
+    import bench
+    import workloads as W
+    for cfg in (3, 4):
+        w = W.make_workload(cfg)
+        assert bench.selected_flops(w.q2k_idx, w.q2k_num, w.block_sizes, w.D) == W.effective_flops(w)
