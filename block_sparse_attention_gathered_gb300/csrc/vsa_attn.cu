@@ -16,25 +16,27 @@
 //     in ascending order, through a ring of K/V stages with TMA, so a key
 //     tile that both units select is fetched once ("gathered" fetch).  The
 //     ring is as deep as shared memory allows.
-//   * One MMA-issuing warp per unit issues S_u = Q_u K_j^T (tcgen05, smem x
+//   * One MMA-issuing thread per unit issues S_u = Q_u K_j^T (tcgen05, smem x
 //     smem -> TMEM) for the key tiles the unit selects, and O_u += P_u V_j
 //     with P read from TMEM.  tcgen05.mma issue runs only ~2 instructions
-//     ahead of execution and every barrier wait costs the issuing thread
-//     ~100 cycles, so two issuers let one warp's waits overlap the other's
-//     issue; descriptors are precomputed and advanced by constant offsets.
-//   * Two softmax warpgroups, one per unit, run the online softmax with exp2
-//     on their TMEM rows (one thread per query row), write P (bf16) into the
-//     TMEM columns of S, rescale O only when the running maximum grows by more
-//     than 2^8 (lazy rescale), and finish with O / l.  The two units
-//     ping-pong: the tensor core works on one unit while the other's softmax
-//     runs.  The row maximum uses 3-input max, the exponent argument a packed
-//     f32x2 FMA, and l accumulates the bf16-rounded P that P V uses.
+//     ahead of execution and every barrier wait costs the issuing thread ~100
+//     cycles, so two issuers let one unit's waits overlap the other's issue.
+//   * TMEM holds O of both units, ONE S buffer the units take turns on (a
+//     shared-memory counter tells an issuer when every earlier S has been
+//     copied out), and P of each unit as bf16 pairs.
+//   * Eight softmax warps per unit, two threads per query row in the same
+//     warp (the .16x32bx2 TMEM shape: thread t holds row t%16 of the warp's
+//     16 lanes and one half of its columns).  The row maximum and the final
+//     row sum combine the halves with one shuffle.  Online softmax with exp2;
+//     O is rescaled only when the running maximum grows by more than 2^8
+//     (lazy rescale); l accumulates the bf16-rounded P that P V uses; the
+//     epilogue writes O / l and the natural-log LSE.
 //   * Masks are applied only on tail key tiles (valid count < tile).  For a
 //     tail tile P V runs only over the 16-key blocks that hold valid keys, and
 //     a fix-up warp zeroes the few padding rows inside the last block in
 //     shared memory first, so NaN/Inf padding in V never meets a zero weight
 //     (0 * NaN = NaN).
-//   * 12 warps: two softmax warpgroups, then a control warpgroup (two MMA
+//   * 20 warps: four softmax warpgroups, then a control warpgroup (two MMA
 //     issuers, the TMA producer, the V fix-up warp) that hands registers to
 //     the softmax warpgroups with setmaxnreg.
 //   * Every wait is bounded (about 2 s); on expiry the CTA sets the timeout
@@ -49,17 +51,18 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kSoftmaxWarps = 8;
-constexpr int kMmaWarp0 = 8;      // MMA issuer of unit 0; kMmaWarp0 + 1 issues for unit 1
-constexpr int kProducerWarp = 10;
-constexpr int kFixupWarp = 11;    // zeroes V padding rows of tail key tiles
+constexpr int kSoftmaxWarps = 16;
+constexpr int kUnitWarps = 8;      // softmax warps per unit; each adds 1 to the S counter per S
+constexpr int kMmaWarp0 = 16;      // MMA issuer of unit 0; kMmaWarp0 + 1 issues for unit 1
+constexpr int kProducerWarp = 18;
+constexpr int kFixupWarp = 19;     // zeroes V padding rows of tail key tiles
 constexpr int kMaxStages = 8;
-// Register split per tile size (control warpgroup, softmax warpgroups); both
-// sum to the 384 x 168 registers the CTA is launched with.
+// Register split (control warpgroup, four softmax warpgroups); the sum stays
+// within the 640 x 96 registers the CTA is launched with.
 template <int T> struct RegSplit {
-    static constexpr uint32_t kControl = T == 128 ? 80 : 104;
-    static constexpr uint32_t kSoftmax = T == 128 ? 208 : 200;
-    static_assert(128 * kControl + 256 * kSoftmax <= kAttnThreads * 168, "register split");
+    static constexpr uint32_t kControl = 64;
+    static constexpr uint32_t kSoftmax = 104;
+    static_assert(128 * kControl + 512 * kSoftmax <= kAttnThreads * 96, "register split");
 };
 constexpr uint32_t kSmemLimit = 232448;  // 227 KB opt-in per CTA
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
@@ -196,7 +199,9 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
     }
 }
 
-// Bounded wait until a monotonic shared-memory counter reaches `target`.
+// Bounded wait until a monotonic shared-memory counter reaches `target`.  A
+// counter, not an mbarrier: the waiter may be any number of S tiles ahead of
+// the last release, which an mbarrier's phase parity cannot tell apart.
 __device__ __forceinline__ bool wait_count(uint32_t addr, uint32_t target, volatile int *abort_flag,
                                            int32_t *status) {
     uint64_t t0 = 0;
@@ -239,7 +244,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const SmemPlan L = smem_plan<T, D>(W, NS);
     const uint32_t sQ = base + L.q;
     // Count of S tiles the softmax warps have copied out of the shared S buffer
-    // (each of the four warps of a unit adds 1 per S).
+    // (each of the eight warps of a unit adds 1 per S).
     const uint32_t sFree = base + L.sfree;
     const uint32_t sRing = base + L.ring;
     uint32_t *bm = reinterpret_cast<uint32_t *>(gbase + L.bm);           // [2][4][W]
@@ -263,7 +268,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             mbar_init(BAR(BI.q_full(u)), 1);
             mbar_init(BAR(BI.q_empty(u)), 1);
             mbar_init(BAR(BI.s_full(u)), 1);
-            mbar_init(BAR(BI.p_full(u)), 128);
+            mbar_init(BAR(BI.p_full(u)), 32 * kUnitWarps);
             mbar_init(BAR(BI.o_done(u)), 1);
             mbar_init(BAR(BI.bm_full(u)), 32);
             mbar_init(BAR(BI.bm_empty(u)), 2 + 32 + 32 * kSoftmaxWarps);  // issuers' lane 0, fix-up, softmax
@@ -527,7 +532,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                             // the previous S; then the pending P V.
                             if (!(ok = wait_bar(BAR(BI.kv_full(kst)), kph, abort_flag, P.status))) break;
                             // every earlier S tile has left the shared S buffer
-                            if (!(ok = wait_count(sFree, 4u * g, abort_flag, P.status))) break;
+                            if (!(ok = wait_count(sFree, (uint32_t)kUnitWarps * g, abort_flag, P.status))) break;
                             tc_fence_after();
 #pragma unroll
                             for (int kk = 0; kk < D / 16; ++kk)
@@ -568,11 +573,21 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     } else {
         regs_inc<RegSplit<T>::kSoftmax>();
         // ------------------------------------------------------------ softmax
-        const int u = warp >> 2;
+        // Eight warps per unit, two threads per query row in the same warp.
+        // Warp 8u + 4sb + q4 takes TMEM lanes (rows) 32q4 + 16sb .. +15 with
+        // the .16x32bx2 shape: thread t holds row t%16 and the columns of half
+        // t/16 (S: T/2 columns, O: D/2 columns, P: T/4 packed columns).  The
+        // row maximum and the final row sum combine the halves with one shuffle.
+        constexpr int TH = T / 2;   // S columns per thread
+        constexpr int DH = D / 2;   // O columns per thread
+        const int u = warp >> 3;
+        const int sb = (warp >> 2) & 1;
         const int q4 = warp & 3;
-        const int row = q4 * 32 + lane;  // query row within the unit
-        const int half = (T == 64) ? (row >> 6) : 0;
-        const uint32_t tl = (uint32_t)(q4 * 32) << 16;
+        const int hf = lane >> 4;                        // column half
+        const int rb0 = q4 * 32 + sb * 16;               // first row of this warp's block
+        const int row = rb0 + (lane & 15);               // query row within the unit
+        const int tsub = (T == 64) ? (q4 >> 1) : 0;      // which 64-row tile of the unit (T == 64)
+        const uint32_t tl = (uint32_t)rb0 << 16;
         const uint32_t tS = tmem + tl + C::kTmemS;
         const uint32_t tP = tmem + tl + (u ? C::kTmemP1 : C::kTmemP0);
         const uint32_t tO = tmem + tl + (u ? C::kTmemO1 : C::kTmemO0);
@@ -585,14 +600,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             if (item < 0) break;
             const uint32_t *bmp = bm + p * 4 * W;
             const int bh = item / P.G, g = item - (item / P.G) * P.G;
-            const int t = (T == 128) ? 2 * g + u : 4 * g + 2 * u + half;
+            const int t = (T == 128) ? 2 * g + u : 4 * g + 2 * u + tsub;
             const int r = (T == 128) ? row : (row & 63);
             const int n_t = (t < NT) ? __ldg(P.block_sizes + t) : 0;
-            float m = -INFINITY, l0 = 0.f, l1 = 0.f;
+            float m = -INFINITY, l0 = 0.f, l1 = 0.f;  // l: this thread's columns
             uint32_t n_mine = 0;
             bool ok = true;
             const uint32_t *pa = bmp + (2 * u) * W, *pb = bmp + (2 * u + 1) * W;
-            const uint32_t *pm = half ? pb : pa;
+            const uint32_t *pm = tsub ? pb : pa;
             for (int w = 0; w < W && ok; ++w) {
                 uint32_t bits = pa[w] | pb[w];
                 const uint32_t mine = pm[w];
@@ -600,13 +615,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     const int b = __ffs(bits) - 1;
                     bits &= bits - 1;
                     const int j = w * 32 + b;
+                    const int nj = __ldg(P.block_sizes + j);  // loaded before the wait for S
                     if (!(ok = wait_warp(BAR(BI.s_full(u)), cnt & 1u, abort_flag, P.status))) break;
                     tc_fence_after();
                     const bool member_row = ((mine >> b) & 1u) != 0u;  // warp-uniform
-                    float s[T];
+                    float s[TH];
                     if (member_row) {
-                        if constexpr (T == 128) tmem_ld128(tS, s);
-                        else tmem_ld64(tS, s);
+                        if constexpr (T == 128) tmem_ld2x_64<TH>(tS, s);
+                        else tmem_ld2x_32<TH>(tS, s);
                     }
                     // S is in registers: the shared S buffer may take the next S.
                     tc_fence_before();
@@ -615,22 +631,22 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     float m_new = m;
                     bool fresh = false, resc = false;
                     if (member_row) {
-                        const int nj = __ldg(P.block_sizes + j);
                         if (nj < T) {
 #pragma unroll
-                            for (int i = 0; i < T; ++i)
-                                if (i >= nj) s[i] = -INFINITY;
+                            for (int i = 0; i < TH; ++i)
+                                if (hf * TH + i >= nj) s[i] = -INFINITY;
                         }
                         float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
 #pragma unroll
-                        for (int i = 0; i < T; i += 8) {
+                        for (int i = 0; i < TH; i += 8) {
                             a0 = max3(a0, s[i], s[i + 1]);
                             a1 = max3(a1, s[i + 2], s[i + 3]);
                             a2 = max3(a2, s[i + 4], s[i + 5]);
                             a3 = max3(a3, s[i + 6], s[i + 7]);
                         }
-                        const float mx = max3(a0, a1, fmaxf(a2, a3)) * c;
-                        m_new = fmaxf(m, mx);
+                        float mx = max3(a0, a1, fmaxf(a2, a3));
+                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                        m_new = fmaxf(m, mx * c);
                         fresh = (m == -INFINITY);
                         resc = !fresh && (m_new > m + kRescaleThreshold);
                     }
@@ -642,47 +658,44 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     }
                     if (__any_sync(0xffffffffu, resc)) {
                         const float alpha = resc ? ex2(m - m_new) : 1.f;
+                        // 8 columns at a time: S is still held in registers here
 #pragma unroll
-                        for (int ch = 0; ch < D / 32; ++ch) {
-                            float o[32];
-                            tmem_ld32(tO + ch * 32, o);
+                        for (int ch = 0; ch < DH / 8; ++ch) {
+                            float o[8];
+                            tmem_ld2x_8<DH>(tO + ch * 8, o);
 #pragma unroll
-                            for (int i = 0; i < 32; ++i) o[i] *= alpha;
-                            tmem_st32(tO + ch * 32, o);
+                            for (int i = 0; i < 8; ++i) o[i] *= alpha;
+                            tmem_st2x_8f<DH>(tO + ch * 8, o);
                         }
-                        tmem_wait_st();
                         l0 *= alpha;
                         l1 *= alpha;
                     }
                     if (fresh || resc) m = m_new;
                     const float neg_m = -m;
-                    // This tile's part of l in 8 independent sums: one running sum
-                    // would chain 128 dependent adds through the row.
-                    float la[8];
+                    // this tile's part of l in 4 independent sums
+                    float lq[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) la[q] = 0.f;
-#pragma unroll
-                    for (int ch = 0; ch < T / 32; ++ch) {
-                        uint32_t pk[16];
+                    for (int cc = 0; cc < TH / 16; ++cc) {
+                        uint32_t pk[8];
                         if (member_row) {
 #pragma unroll
-                            for (int i = 0; i < 16; ++i) {
+                            for (int i = 0; i < 8; ++i) {
                                 float x0, x1;
-                                fma2_scalar(x0, x1, s[ch * 32 + 2 * i], s[ch * 32 + 2 * i + 1], c, neg_m);
+                                fma2_scalar(x0, x1, s[cc * 16 + 2 * i], s[cc * 16 + 2 * i + 1], c, neg_m);
                                 pk[i] = pack_bf16x2(ex2(x0), ex2(x1));
                                 // l sums the bf16 values P V actually uses, so the
                                 // weights P / l stay exactly normalised.
-                                add_bf16x2_f32(la[2 * (i & 3)], la[2 * (i & 3) + 1], pk[i]);
+                                add_bf16x2_f32(lq[2 * (i & 1)], lq[2 * (i & 1) + 1], pk[i]);
                             }
                         } else {
-                            // this half of the unit does not select tile j: zero P rows
+                            // this tile of the unit does not select tile j: zero P rows
 #pragma unroll
-                            for (int i = 0; i < 16; ++i) pk[i] = 0u;
+                            for (int i = 0; i < 8; ++i) pk[i] = 0u;
                         }
-                        tmem_st16(tP + ch * 16, pk);
+                        tmem_st2x_8<TH / 2>(tP + cc * 8, pk);
                     }
-                    l0 += (la[0] + la[2]) + (la[4] + la[6]);
-                    l1 += (la[1] + la[3]) + (la[5] + la[7]);
+                    l0 += lq[0] + lq[2];
+                    l1 += lq[1] + lq[3];
                     tmem_wait_st();
                     tc_fence_before();
                     mbar_arrive(BAR(BI.p_full(u)));
@@ -696,33 +709,32 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 if (!wait_warp(BAR(BI.o_done(u)), (cnt - 1u) & 1u, abort_flag, P.status)) break;
                 tc_fence_after();
             }
-            const float l = l0 + l1;
+            float l = l0 + l1;
+            l += __shfl_xor_sync(0xffffffffu, l, 16);
             const bool write_row = t < NT;
             const bool valid = r < n_t;
             const bool use_o = (n_mine > 0) && valid && (l != 0.f);  // NaN l keeps use_o: NaN row
             const float inv = use_o ? 1.f / l : 0.f;
             const int64_t orow = (int64_t)bh * Sp + (int64_t)t * T + r;
-            uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(P.out) + orow * D);
+            uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(P.out) + orow * D + hf * DH);
 #pragma unroll
-            for (int ch = 0; ch < D / 32; ++ch) {
-                float o[32];
+            for (int ch = 0; ch < DH / 16; ++ch) {
+                float o[16];
                 if (n_mine > 0) {
-                    tmem_ld32(tO + ch * 32, o);
+                    tmem_ld2x_16<DH>(tO + ch * 16, o);
                 } else {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) o[i] = 0.f;
+                    for (int i = 0; i < 16; ++i) o[i] = 0.f;
                 }
                 if (write_row) {
-                    uint32_t wv[16];
+                    uint32_t wv[8];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        wv[i] = use_o ? pack_bf16x2(o[2 * i] * inv, o[2 * i + 1] * inv) : 0u;
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        dst[ch * 4 + i] = make_uint4(wv[4 * i], wv[4 * i + 1], wv[4 * i + 2], wv[4 * i + 3]);
+                    for (int i = 0; i < 8; ++i) wv[i] = use_o ? pack_bf16x2(o[2 * i] * inv, o[2 * i + 1] * inv) : 0u;
+                    dst[2 * ch] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+                    dst[2 * ch + 1] = make_uint4(wv[4], wv[5], wv[6], wv[7]);
                 }
             }
-            if (P.lse && write_row) {
+            if (P.lse && write_row && hf == 0) {
                 float v = -INFINITY;
                 if (use_o) v = (m + lg2(l)) * 0.69314718055994531f;
                 P.lse[orow] = v;

@@ -14,7 +14,7 @@ enum : int32_t { kFlagIndex = 1, kFlagTimeout = 2 };
 // Query rows of one work item: two 128-row units, each one MMA M=128.
 constexpr int kUnitRows = 128;
 constexpr int kItemRows = 256;
-constexpr int kAttnThreads = 384;  // 8 softmax warps, 2 MMA issuers, 1 producer, 1 fix-up warp
+constexpr int kAttnThreads = 640;  // 16 softmax warps, 2 MMA issuers, 1 producer, 1 fix-up warp
 constexpr int kMaxTiles = 8192;     // VSA_MAX_TILES
 
 struct AttnParams {
