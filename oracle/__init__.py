@@ -54,6 +54,8 @@ def _load():
         lib.oracle_tile_layout.restype = i32
         lib.oracle_coarse_select.argtypes = [P, P, P, i32, i32, i32, i32, i32, i32, P, P, P]
         lib.oracle_coarse_select.restype = i32
+        lib.oracle_untile.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, i32]
+        lib.oracle_untile.restype = i32
         _lib = lib
     return _lib
 
@@ -149,6 +151,25 @@ def coarse_select(q, k, block_sizes, T: int, topk: int, want_scores: bool = True
     if rc != 0:
         raise ValueError(f"oracle_coarse_select: {ERRORS.get(rc, rc)}")
     return idx, num, sc
+
+
+def untile(o_tile, gate_tok, row_to_token, S: int, T: int, out=None) -> np.ndarray:
+    """Tile-major bf16 ``o_tile [B, H, NT*T, D]`` -> token-major bf16 bits
+    ``[B, S, H, D]``, times ``gate_tok`` (bf16 ``[B, S, H, D]``) when given, one
+    round-to-nearest-even per element (see ``oracle_untile``).  Tokens no row
+    maps to keep the values of ``out`` (zeros by default)."""
+    ob = _bf16_bits(o_tile)
+    B, H, Sp, D = ob.shape
+    NT = Sp // T
+    gb = _bf16_bits(gate_tok) if gate_tok is not None else None
+    r2t = _i32(row_to_token)
+    assert r2t.shape == (Sp,)
+    dst = np.zeros((B, S, H, D), dtype=np.uint16) if out is None else np.ascontiguousarray(out, dtype=np.uint16)
+    rc = _load().oracle_untile(_ptr(ob), _ptr(gb) if gb is not None else None, _ptr(r2t), _ptr(dst), B, S, H, D,
+                               NT, T)
+    if rc != 0:
+        raise ValueError(f"oracle_untile: {ERRORS.get(rc, rc)}")
+    return dst
 
 
 def bits_to_float(bits: np.ndarray) -> np.ndarray:

@@ -1,6 +1,7 @@
 /*
- * CPU oracle for the block-sparse attention forward pass, the tile layout and
- * the coarse key-tile selection that produces the block-sparse selection.
+ * CPU oracle for the block-sparse attention forward pass, the tile layout, the
+ * coarse key-tile selection that produces the block-sparse selection, and the
+ * output un-tiling with the gate.
  *
  * TEST INFRASTRUCTURE ONLY.  This file is the plain, slow, obviously correct
  * FP64 statement of what the GPU library computes.  Only the tests, the smoke
@@ -337,5 +338,48 @@ int oracle_coarse_select(const uint16_t *q, const uint16_t *k, const int32_t *bl
     free(km);
     free(row);
     free(taken);
+    return ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------------
+ * Output un-tiling with the gate: the step after the block-sparse forward.
+ * The fused tile_to_bhsd commit on the page describes the layer's tiled path
+ * (Q, K, V and the gate scattered into a tile buffer); reading of the step
+ * back: every tile-major output row r that holds a token (s = row_to_token[r]
+ * >= 0) goes back to token-major order, multiplied element-wise by that
+ * token's gate when a gate is given:
+ *   out_tok[b, s, h, :] = bf16( float(O[b, h, r, :]) * float(gate[b, s, h, :]) )
+ * The product of two bf16 values is exact in fp32, so the only rounding is
+ * the final round-to-nearest-even to bf16 (NaN stays NaN).  Padding rows are
+ * not read; tokens that no row maps to are left as they are.
+ *   o_tile bf16 bits [B, H, NT*T, D]; gate NULL or bf16 bits [B, S, H, D];
+ *   out bf16 bits [B, S, H, D].
+ * ------------------------------------------------------------------------ */
+static uint16_t f32_to_bf16_rne(float f) {
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    if ((u & 0x7f800000u) == 0x7f800000u && (u & 0x007fffffu)) return (uint16_t)((u >> 16) | 0x0040u);
+    u += 0x7fffu + ((u >> 16) & 1u);  /* ties to the even upper half */
+    return (uint16_t)(u >> 16);
+}
+
+int oracle_untile(const uint16_t *o_tile, const uint16_t *gate, const int32_t *row_to_token, uint16_t *out,
+                  int B, int S, int H, int D, int NT, int T) {
+    if (!o_tile || !row_to_token || !out || B <= 0 || S < 0 || H <= 0 || D <= 0 || NT <= 0 || T <= 0)
+        return ORACLE_ERR_ARG;
+    const int64_t Sp = (int64_t)NT * T;
+    for (int64_t row = 0; row < Sp; ++row)
+        if (row_to_token[row] < -1 || row_to_token[row] >= S) return ORACLE_ERR_INDEX;
+    for (int b = 0; b < B; ++b)
+        for (int h = 0; h < H; ++h)
+            for (int64_t row = 0; row < Sp; ++row) {
+                const int32_t s = row_to_token[row];
+                if (s < 0) continue;
+                const uint16_t *o = o_tile + (((int64_t)b * H + h) * Sp + row) * D;
+                uint16_t *dst = out + (((int64_t)b * S + s) * H + h) * D;
+                const uint16_t *gt = gate ? gate + (((int64_t)b * S + s) * H + h) * D : NULL;
+                for (int d = 0; d < D; ++d)
+                    dst[d] = gt ? f32_to_bf16_rne((float)(bf16_to_double(o[d]) * bf16_to_double(gt[d]))) : o[d];
+            }
     return ORACLE_OK;
 }
