@@ -25,7 +25,7 @@ LIB_PATH = os.path.join(_HERE, "_build", "libvsa.so")
 VSA_OK, VSA_ERR_ARG, VSA_ERR_ALIGN, VSA_ERR_LIMITS, VSA_ERR_ARCH = 0, -1, -2, -3, -4
 VSA_ERR_CUDA, VSA_ERR_TIMEOUT, VSA_ERR_INDEX, VSA_ERR_WORKSPACE = -5, -6, -7, -8
 VSA_KERNEL_NONE, VSA_KERNEL_ATTN_TCGEN05, VSA_KERNEL_LAYOUT, VSA_KERNEL_VALIDATE = 0, 1, 2, 3
-VSA_KERNEL_SELECT = 4
+VSA_KERNEL_SELECT, VSA_KERNEL_UNTILE = 4, 5
 VSA_MAX_BATCH_HEADS, VSA_MAX_TILES = 65535, 8192
 
 
@@ -64,6 +64,7 @@ def _load() -> ctypes.CDLL:
         "vsa_block_sparse_fwd_noalloc": ([P, P, P, P, P, P, P, P, dims_p, P], i32),
         "vsa_tile_layout": ([P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, P], i32),
         "vsa_validate_indices": ([P, P, P, dims_p, P, P], i32),
+        "vsa_untile": ([P, P, P, P, i32, i32, i32, i32, i32, i32, P], i32),
         "vsa_coarse_select_workspace_size": ([dims_p], sz),
         "vsa_coarse_select": ([P, P, P, i32, P, P, dims_p, P, sz, P], i32),
         "vsa_check_device_status": ([P], i32),
@@ -79,7 +80,7 @@ def _load() -> ctypes.CDLL:
 
 _lib = _load()
 EXPORTED = ("vsa_block_sparse_workspace_size", "vsa_block_sparse_fwd", "vsa_block_sparse_fwd_noalloc",
-            "vsa_tile_layout", "vsa_coarse_select_workspace_size", "vsa_coarse_select",
+            "vsa_tile_layout", "vsa_untile", "vsa_coarse_select_workspace_size", "vsa_coarse_select",
             "vsa_validate_indices", "vsa_check_device_status", "vsa_last_route",
             "vsa_status_string", "vsa_version")
 
@@ -148,6 +149,13 @@ def vsa_tile_layout(q_tok, k_tok, v_tok, q_tile, k_tile, v_tile, row_to_token, B
                               int(num_tiles), int(tile), _stream(stream))
     if st != VSA_OK:
         raise VsaError(st, "vsa_tile_layout")
+
+
+def vsa_untile(o_tile, gate_tok, out_tok, row_to_token, B, S, H, D, num_tiles, tile, stream=None) -> None:
+    st = _lib.vsa_untile(_ptr(o_tile), _ptr(gate_tok), _ptr(out_tok), _ptr(row_to_token), int(B), int(S), int(H),
+                         int(D), int(num_tiles), int(tile), _stream(stream))
+    if st != VSA_OK:
+        raise VsaError(st, "vsa_untile")
 
 
 def vsa_coarse_select_workspace_size(dims: VsaDims) -> int:
@@ -242,6 +250,17 @@ def coarse_select(q, k, block_sizes, tile: int, topk: int, workspace: Optional[t
     num = torch.empty((B, H, NT), dtype=torch.int32, device=q.device)
     vsa_coarse_select(q, k, block_sizes.contiguous(), topk, idx, num, dims, workspace, stream)
     return idx, num
+
+
+def untile(o_tile, row_to_token, num_tokens: int, tile: int, gate_tok=None, out=None, stream=None):
+    """Tile-major bf16 ``o_tile [B, H, NT*tile, D]`` -> token-major ``[B, S, H, D]``
+    (times ``gate_tok`` when given)."""
+    _check_bf16_cuda(o_tile, gate_tok)
+    B, H, Sp, D = o_tile.shape
+    if out is None:
+        out = torch.zeros((B, num_tokens, H, D), dtype=torch.bfloat16, device=o_tile.device)
+    vsa_untile(o_tile, gate_tok, out, row_to_token.contiguous(), B, num_tokens, H, D, Sp // tile, tile, stream)
+    return out
 
 
 def tile_layout(q_tok, k_tok, v_tok, row_to_token, num_tiles: int, tile: int, stream=None):

@@ -381,6 +381,44 @@ vsa_status vsa_tile_layout(const void *q_tok, const void *k_tok, const void *v_t
     return VSA_OK;
 }
 
+vsa_status vsa_untile(const void *o_tile, const void *gate_tok, void *out_tok, const int32_t *row_to_token,
+                      int32_t B, int32_t S, int32_t H, int32_t D, int32_t num_tiles, int32_t tile,
+                      vsa_stream_t stream) {
+    if (!o_tile || !out_tok || !row_to_token || B <= 0 || S < 0 || H <= 0 || D <= 0 || (D % 8) != 0 ||
+        num_tiles <= 0 || tile <= 0)
+        return VSA_ERR_ARG;
+    if (!aligned(o_tile, 16) || !aligned(out_tok, 16) || (gate_tok && !aligned(gate_tok, 16)) ||
+        !aligned(row_to_token, 4))
+        return VSA_ERR_ALIGN;
+    if ((int64_t)B * H > VSA_MAX_BATCH_HEADS) return VSA_ERR_LIMITS;
+    const int64_t Sp = (int64_t)num_tiles * tile;
+    if ((int64_t)B * H * Sp >= (int64_t(1) << VSA_MAX_ROWS_LOG2) || (int64_t)B * S * H >= (int64_t(1) << 31))
+        return VSA_ERR_LIMITS;
+    int dev = 0;
+    vsa_status st = current_device(&dev);
+    if (st != VSA_OK) return st;
+    DeviceCache &dc = g_dev[dev];
+    UntileParams p;
+    p.o_tile = o_tile;
+    p.gate = gate_tok;
+    p.out = out_tok;
+    p.row_to_token = row_to_token;
+    p.status = dc.status_ptr.load(std::memory_order_acquire);
+    p.B = B;
+    p.S = S;
+    p.H = H;
+    p.Dv = D / 8;
+    p.Sp = Sp;
+    if (launch_untile(p, dc.sm_count.load(std::memory_order_acquire), reinterpret_cast<cudaStream_t>(stream)) !=
+        cudaSuccess)
+        return VSA_ERR_CUDA;
+    t_route = vsa_route{};
+    t_route.kernel = VSA_KERNEL_UNTILE;
+    t_route.tile = tile;
+    t_route.head_dim = D;
+    return VSA_OK;
+}
+
 vsa_status vsa_validate_indices(const int32_t *q2k_idx, const int32_t *q2k_num, const int32_t *block_sizes,
                                 const vsa_dims *dims, int32_t *dev_status, vsa_stream_t stream) {
     vsa_status st = check_dims(dims);

@@ -65,6 +65,18 @@ struct LayoutParams {
 
 cudaError_t launch_layout(const LayoutParams &p, int num_sms, cudaStream_t stream);
 
+struct UntileParams {
+    const void *o_tile;         // bf16 [B, H, Sp, D] tile-major output
+    const void *gate;           // bf16 [B, S, H, D] or nullptr
+    void *out;                  // bf16 [B, S, H, D] token-major
+    const int32_t *row_to_token;
+    int32_t *status;
+    int32_t B, S, H, Dv;        // Dv = head_dim / 8
+    int64_t Sp;
+};
+
+cudaError_t launch_untile(const UntileParams &p, int num_sms, cudaStream_t stream);
+
 // Coarse key-tile selection (vsa_select.cu).
 constexpr uint32_t kSelectSmemLimit = 232448;  // 227 KB opt-in per CTA
 

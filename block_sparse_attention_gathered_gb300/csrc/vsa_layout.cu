@@ -1,4 +1,4 @@
-// Fused tile layout for sm_103a (fused tile_to_bhsd commit on the FastVideo
+// Fused tile layout and its inverse for sm_103a (fused tile_to_bhsd commit on the FastVideo
 // kernel page, hao-ai-lab/FastVideo commit 8503617: one pass that moves
 // token-major Q/K/V into tile-major BHSD instead of a scatter plus transposed
 // copies).
@@ -66,18 +66,90 @@ __global__ void __launch_bounds__(kLayoutThreads)
     if (bad) atomicOr(P.status, kFlagIndex);
 }
 
+// Output un-tiling, the inverse of layout_kernel: every tile-major row that
+// holds a token goes back to token-major order, times the token's gate when
+// one is given.  bf16 x bf16 is exact in fp32, so the product is rounded once
+// (to nearest even) to bf16.  Padding rows are not read.
+__global__ void __launch_bounds__(kLayoutThreads)
+    untile_kernel(const UntileParams P, int rows_per_block, int hv_per_block) {
+    const int HV = P.H * P.Dv;
+    const int rl = threadIdx.x / hv_per_block;
+    const int hv = blockIdx.y * hv_per_block + (threadIdx.x - rl * hv_per_block);
+    if (rl >= rows_per_block || hv >= HV) return;
+    const int h = hv / P.Dv;
+    const int vec = hv - h * P.Dv;
+    const int b = blockIdx.z;
+    const int64_t Sp = P.Sp;
+    const uint4 *src = reinterpret_cast<const uint4 *>(P.o_tile) + (((int64_t)b * P.H + h) * Sp) * P.Dv + vec;
+    const int64_t tok_b = (int64_t)b * P.S * HV + hv;  // + s*HV
+    const int64_t step = (int64_t)gridDim.x * rows_per_block;
+    bool bad = false;
+    for (int64_t row0 = (int64_t)blockIdx.x * rows_per_block + rl; row0 < Sp; row0 += step * kRowsInFlight) {
+        int64_t rows[kRowsInFlight];
+        int32_t tok[kRowsInFlight];
+        uint4 o[kRowsInFlight], gt[kRowsInFlight];
+#pragma unroll
+        for (int i = 0; i < kRowsInFlight; ++i) {
+            rows[i] = row0 + i * step;
+            tok[i] = rows[i] < Sp ? __ldg(P.row_to_token + rows[i]) : -1;
+            if (tok[i] >= P.S || tok[i] < -1) {
+                bad = true;
+                tok[i] = -1;
+            }
+            if (tok[i] >= 0) {
+                o[i] = __ldcs(src + rows[i] * P.Dv);
+                if (P.gate) gt[i] = __ldcs(reinterpret_cast<const uint4 *>(P.gate) + tok_b + (int64_t)tok[i] * HV);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < kRowsInFlight; ++i) {
+            if (tok[i] < 0) continue;
+            uint4 v = o[i];
+            if (P.gate) {
+                uint32_t a[4] = {o[i].x, o[i].y, o[i].z, o[i].w}, g[4] = {gt[i].x, gt[i].y, gt[i].z, gt[i].w};
+                uint32_t r[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float lo = __uint_as_float(a[k] << 16) * __uint_as_float(g[k] << 16);
+                    const float hi = __uint_as_float(a[k] & 0xffff0000u) * __uint_as_float(g[k] & 0xffff0000u);
+                    uint32_t w;
+                    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(w) : "f"(hi), "f"(lo));
+                    r[k] = w;
+                }
+                v = make_uint4(r[0], r[1], r[2], r[3]);
+            }
+            __stcs(reinterpret_cast<uint4 *>(P.out) + tok_b + (int64_t)tok[i] * HV, v);
+        }
+    }
+    if (bad) atomicOr(P.status, kFlagIndex);
+}
+
 }  // namespace
 
-cudaError_t launch_layout(const LayoutParams &p, int num_sms, cudaStream_t stream) {
-    const int HV = p.H * p.Dv;
+static dim3 row_grid(int H, int Dv, int B, int64_t Sp, int num_sms, int *R_out, int *hvb_out) {
+    const int HV = H * Dv;
     const int hvb = HV < kLayoutThreads ? HV : kLayoutThreads;
     const int R = kLayoutThreads / hvb;  // rows per block iteration
     const int gy = (HV + hvb - 1) / hvb;
-    const int64_t row_blocks = (p.Sp + R - 1) / R;
-    int64_t gx = ((int64_t)num_sms * (2048 / kLayoutThreads) + (int64_t)gy * p.B - 1) / ((int64_t)gy * p.B);
+    const int64_t row_blocks = (Sp + R - 1) / R;
+    int64_t gx = ((int64_t)num_sms * (2048 / kLayoutThreads) + (int64_t)gy * B - 1) / ((int64_t)gy * B);
     gx = gx < 1 ? 1 : gx;
     gx = gx > row_blocks ? row_blocks : gx;
-    dim3 grid((unsigned)gx, (unsigned)gy, (unsigned)p.B);
+    *R_out = R;
+    *hvb_out = hvb;
+    return dim3((unsigned)gx, (unsigned)gy, (unsigned)B);
+}
+
+cudaError_t launch_untile(const UntileParams &p, int num_sms, cudaStream_t stream) {
+    int R, hvb;
+    const dim3 grid = row_grid(p.H, p.Dv, p.B, p.Sp, num_sms, &R, &hvb);
+    untile_kernel<<<grid, R * hvb, 0, stream>>>(p, R, hvb);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_layout(const LayoutParams &p, int num_sms, cudaStream_t stream) {
+    int R, hvb;
+    const dim3 grid = row_grid(p.H, p.Dv, p.B, p.Sp, num_sms, &R, &hvb);
     layout_kernel<<<grid, R * hvb, 0, stream>>>(p, R, hvb);
     return cudaGetLastError();
 }

@@ -91,6 +91,7 @@ typedef struct {
 #define VSA_KERNEL_LAYOUT 2
 #define VSA_KERNEL_VALIDATE 3
 #define VSA_KERNEL_SELECT 4
+#define VSA_KERNEL_UNTILE 5
 
 /* Bytes of workspace vsa_block_sparse_fwd needs for `dims` (the on-device work
  * order and its counter).  Returns 0 when `dims` is invalid. */
@@ -173,6 +174,27 @@ vsa_status vsa_tile_layout(const void *q_tok, const void *k_tok, const void *v_t
                            void *k_tile, void *v_tile, const int32_t *row_to_token, int32_t B,
                            int32_t S, int32_t H, int32_t D, int32_t num_tiles, int32_t tile,
                            vsa_stream_t stream);
+
+/*
+ * Output un-tiling with the gate, the inverse of vsa_tile_layout (the fused
+ * tile_to_bhsd commit describes the layer's tiled path: Q, K, V and the gate
+ * go into a tile buffer; this is the step back).  For every tile-major row r
+ * with a token s = row_to_token[r] >= 0:
+ *   out_tok[b, s, h, :] = bf16( float(o_tile[b, h, r, :]) * float(gate[b, s, h, :]) )
+ * or a plain copy of the row when gate_tok is NULL.  The product of two bf16
+ * values is exact in fp32, so the result is rounded once, to nearest even.
+ * Padding rows are not read; tokens that no row maps to are not written.
+ *
+ *   o_tile       bf16 [B, H, NT*tile, D] tile-major (the forward's output)
+ *   gate_tok     NULL, or bf16 [B, S, H, D] token-major gate
+ *   out_tok      bf16 [B, S, H, D] token-major output
+ *   row_to_token int32 [NT*tile], the map vsa_tile_layout used; a value
+ *                outside [-1, S) skips the row and flags VSA_ERR_INDEX
+ *   D            head_dim, a multiple of 8 (16-byte rows)
+ */
+vsa_status vsa_untile(const void *o_tile, const void *gate_tok, void *out_tok, const int32_t *row_to_token,
+                      int32_t B, int32_t S, int32_t H, int32_t D, int32_t num_tiles, int32_t tile,
+                      vsa_stream_t stream);
 
 /*
  * Opt-in selection check (sm_121a hardening commit, launch-limit and

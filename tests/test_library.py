@@ -115,6 +115,19 @@ def test_validate_argument_errors(vsa):
     assert V(P(FAKE), P(FAKE + 2), P(FAKE), ctypes.byref(d), P(FAKE), None) == vsa.VSA_ERR_ALIGN
 
 
+def test_untile_argument_errors(vsa):
+    P = ctypes.c_void_p
+    U = vsa.library().vsa_untile
+    f = lambda o, g, out, m, *a: U(P(o) if o else None, P(g) if g else None, P(out) if out else None,
+                                   P(m) if m else None, *a, None)
+    assert f(0, 0, FAKE, FAKE, 1, 8, 2, 64, 1, 8) == vsa.VSA_ERR_ARG            # no input
+    assert f(FAKE, 0, FAKE, 0, 1, 8, 2, 64, 1, 8) == vsa.VSA_ERR_ARG            # no map
+    assert f(FAKE, 0, FAKE, FAKE, 1, 8, 2, 60, 1, 8) == vsa.VSA_ERR_ARG         # D % 8
+    assert f(FAKE, FAKE + 8, FAKE, FAKE, 1, 8, 2, 64, 1, 8) == vsa.VSA_ERR_ALIGN  # gate
+    assert f(FAKE, 0, FAKE + 4, FAKE, 1, 8, 2, 64, 1, 8) == vsa.VSA_ERR_ALIGN   # output
+    assert f(FAKE, 0, FAKE, FAKE, 256, 8, 256, 64, 1, 8) == vsa.VSA_ERR_LIMITS  # batch * heads
+
+
 def test_coarse_select_argument_errors(vsa):
     P = ctypes.c_void_p
     d = vsa.make_dims(1, 2, 4, 64, 64, 0)
