@@ -279,6 +279,12 @@ def run_ours(args, cfg):
         sel_ws = torch.empty(vsa.vsa_coarse_select_workspace_size(sel_dims), dtype=torch.uint8, device=dev)
         idx = torch.empty((B, H, NT, topk), dtype=torch.int32, device=dev)
         num = torch.empty((B, H, NT), dtype=torch.int32, device=dev)
+    untile = bool(args.untile)
+    if untile:
+        # the step ends with the un-tiling of the output, times a gate
+        gate = (torch.rand((B, S, H, D), generator=torch.Generator().manual_seed(W.SEED_BASE + 100)) * 2
+                ).to(torch.bfloat16).to(dev)
+        out_tok = torch.empty((B, S, H, D), dtype=torch.bfloat16, device=dev)
     dims = vsa.make_dims(B, H, NT, T, D, idx.shape[-1], w.scale)
     ws = torch.empty(vsa.vsa_block_sparse_workspace_size(dims), dtype=torch.uint8, device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)  # > 129 MB L2
@@ -302,7 +308,12 @@ def run_ours(args, cfg):
             s1.record(stream)
         vsa.vsa_block_sparse_fwd(tiles[0], tiles[1], tiles[2], idx, num, bs, out, lse, dims, ws, stream)
         a1.record(stream)
-        return l0, l1, s1, a1
+        u1 = a1
+        if untile:
+            vsa.vsa_untile(out, gate, out_tok, r2t, B, S, H, D, NT, T, stream)
+            u1 = ev()
+            u1.record(stream)
+        return l0, l1, s1, a1, u1
 
     def barrier():
         if world > 1:
@@ -326,7 +337,8 @@ def run_ours(args, cfg):
             flush.zero_()  # L2 flush, outside the timed events
             marks.append(step(q_tok, k_tok, v_tok))
         barrier()
-    step_ms = [m[0].elapsed_time(m[3]) for m in marks]
+    step_ms = [m[0].elapsed_time(m[4]) for m in marks]
+    untile_ms = [m[3].elapsed_time(m[4]) for m in marks] if untile else None
     layout_ms = [m[0].elapsed_time(m[1]) for m in marks]
     select_ms = [m[1].elapsed_time(m[2]) for m in marks] if select else None
     attn_ms = [m[2].elapsed_time(m[3]) for m in marks]
@@ -341,6 +353,10 @@ def run_ours(args, cfg):
     h_in = ((q_tok, hq), (k_tok, hk), (v_tok, hv), (bs, hbs), (r2t, hr2t)) + \
         (() if select else ((idx, hidx), (num, hnum)))
     hout = torch.empty((B, H, Sp, D), dtype=torch.bfloat16).pin_memory()
+    if untile:  # the gate is an input too, and the token-major output is read back
+        hgate = gate.cpu().pin_memory()
+        h_in = h_in + ((gate, hgate),)
+        hout = torch.empty((B, S, H, D), dtype=torch.bfloat16).pin_memory()
     hlse = torch.empty((B, H, Sp), dtype=torch.float32).pin_memory() if lse is not None else None
     h2d = sum(h_.numel() * h_.element_size() for _, h_ in h_in)
     d2h = hout.numel() * 2 + (hlse.numel() * 4 if hlse is not None else 0)
@@ -349,7 +365,7 @@ def run_ours(args, cfg):
         for d_, h_ in h_in:
             d_.copy_(h_, non_blocking=True)
         step(q_tok, k_tok, v_tok)
-        hout.copy_(out, non_blocking=True)
+        hout.copy_(out_tok if untile else out, non_blocking=True)
         if hlse is not None:
             hlse.copy_(lse, non_blocking=True)
 
@@ -392,8 +408,8 @@ def run_ours(args, cfg):
                                 "peak_source": f"{src} HBM copy", "kernel": "layout_kernel"},
             "e2e": {"value": aggregate(eff, world, e2e_ms), "unit": UNIT, "ms_per_step": e2e_ms,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            # per step: tile layout, [tile pooling, selection,] work-ordering sort, attention
-            "gpu_launches": (5 if select else 3) * args.steps,
+            # per step: tile layout, [tile pooling, selection,] work-ordering sort, attention, [un-tiling]
+            "gpu_launches": (3 + (2 if select else 0) + (1 if untile else 0)) * args.steps,
             "clocks": clk.summary(),
             "route": route,
         }
@@ -407,6 +423,14 @@ def run_ours(args, cfg):
                 "kernel": "pool_kernel + select_kernel (bytes: valid rows of q and k read once)"}
             line["config"]["step"] = "tile layout + coarse top-k selection + work ordering + tcgen05 attention"
             line["config"]["topk"] = topk
+        if untile:
+            ut_avg = sum(untile_ms) / len(untile_ms)
+            ut_bytes = 3 * B * S * H * D * 2 + 4 * NT * T  # output rows and gate read, token output written, map
+            line["untile_ms"] = ut_avg
+            line["untile_roofline"] = {
+                "bound": "hbm", "achieved": ut_bytes / (ut_avg / 1e3) / 1e9, "peak": hbm, "unit": "GB/s",
+                "frac": ut_bytes / (ut_avg / 1e3) / 1e9 / hbm, "bytes": ut_bytes, "kernel": "untile_kernel (gated)"}
+            line["config"]["step"] += " + un-tiling with gate"
         if not args.no_cpu_baseline and world == 1:
             line["cpu_baseline"] = cpu_oracle_run(w, args.cpu_seconds)
         print(json.dumps(line), flush=True)
@@ -423,6 +447,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", type=int, default=5, choices=[2, 4, 5])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--untile", action="store_true",
+                    help="end the step with the un-tiling of the output times a gate")
     ap.add_argument("--select", action="store_true",
                     help="video-grid workload only: select the key tiles on the GPU inside the step")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
