@@ -43,8 +43,8 @@ FALLBACK_HBM_GBS = 6800.0
 # the SHA-256 of the attention kernel source the capture was taken with; a
 # changed kernel reports null until it is captured again.
 ATTN_TRAFFIC = {
-    # profiles/attn_fwd_t128d128_dense_b1h6_s31200.md: 313.0 MB read + 36.8 MB written
-    ("dense_b1h6d128_s31200_t128x244_lse", "3461624eb2703e31"): 349.78e6,
+    # profiles/attn_fwd_t128d128_dense_b1h6_s31200.md: 241.4 MB read + 37.2 MB written
+    ("dense_b1h6d128_s31200_t128x244_lse", "6669ba4b948f17aa"): 278.62e6,
 }
 
 
