@@ -93,11 +93,12 @@ vsa_status current_device(int *dev_out) {
 vsa_status check_dims(const vsa_dims *d) {
     if (!d) return VSA_ERR_ARG;
     if (d->B <= 0 || d->H <= 0 || d->num_tiles <= 0 || d->max_kv < 0) return VSA_ERR_ARG;
-    if (d->tile != 64 && d->tile != 128) return VSA_ERR_ARG;
+    if (d->tile != 64 && d->tile != 128 && d->tile != 256) return VSA_ERR_ARG;
     if (d->head_dim != 64 && d->head_dim != 128) return VSA_ERR_ARG;
     if (!std::isfinite(d->scale)) return VSA_ERR_ARG;
     if ((int64_t)d->B * d->H > VSA_MAX_BATCH_HEADS) return VSA_ERR_LIMITS;
-    if (d->num_tiles > VSA_MAX_TILES) return VSA_ERR_LIMITS;
+    // 256-token tiles run as two 128-token halves each
+    if ((int64_t)d->num_tiles * (d->tile == 256 ? 2 : 1) > VSA_MAX_TILES) return VSA_ERR_LIMITS;
     const int64_t rows = (int64_t)d->B * d->H * d->num_tiles * d->tile;
     if (rows + kItemRows >= (int64_t(1) << VSA_MAX_ROWS_LOG2)) return VSA_ERR_LIMITS;
     if ((int64_t)d->B * d->H * d->num_tiles * (int64_t)d->max_kv >= (int64_t(1) << 31)) return VSA_ERR_LIMITS;
@@ -141,7 +142,7 @@ __global__ void __launch_bounds__(kSchedThreads)
     int32_t *cursor = sh + bins;  // [bins]
     __shared__ int32_t warp_tot[kSchedThreads / 32];
     const int tid = threadIdx.x;
-    const int per_item = (T == 128) ? 2 : 4;
+    const int per_item = kItemRows / T;  // caller tiles per work item: 4, 2 or 1
     const int64_t wmax = (int64_t)per_item * (max_kv > 0 ? max_kv : 1);
     for (int i = tid; i < bins; i += kSchedThreads) hist[i] = 0;
     __syncthreads();
@@ -269,9 +270,11 @@ vsa_status vsa_block_sparse_fwd(const void *q, const void *k, const void *v, con
     DeviceCache &dc = g_dev[dev];
 
     const int T = dims->tile, D = dims->head_dim, NT = dims->num_tiles;
-    const unsigned variant_bit = 1u << ((T == 128 ? 2 : 0) + (D == 128 ? 1 : 0));
+    // 256-token tiles: the 128-token kernel on the two halves of every tile
+    const int Tk = T == 256 ? 128 : T, sub = T / Tk;
+    const unsigned variant_bit = 1u << ((Tk == 128 ? 2 : 0) + (D == 128 ? 1 : 0));
     if (!(dc.attn_prepared.load(std::memory_order_acquire) & variant_bit)) {
-        if (attn_prepare(T, D, dev) != cudaSuccess) {
+        if (attn_prepare(Tk, D, dev) != cudaSuccess) {
             cudaGetLastError();
             return VSA_ERR_CUDA;
         }
@@ -282,12 +285,12 @@ vsa_status vsa_block_sparse_fwd(const void *q, const void *k, const void *v, con
     const int64_t rows = (int64_t)dims->B * dims->H * Sp;
     CUtensorMap tm_q, tm_k, tm_v;
     if ((st = encode_rows_map(&tm_q, q, rows, D, kUnitRows)) != VSA_OK) return st;
-    if ((st = encode_rows_map(&tm_k, k, rows, D, T)) != VSA_OK) return st;
-    if ((st = encode_rows_map(&tm_v, v, rows, D, T)) != VSA_OK) return st;
+    if ((st = encode_rows_map(&tm_k, k, rows, D, Tk)) != VSA_OK) return st;
+    if ((st = encode_rows_map(&tm_v, v, rows, D, Tk)) != VSA_OK) return st;
 
     const int G = (int)items_per_seq(dims);
     const int n_items = (int)((int64_t)dims->B * dims->H * G);
-    const int per_item = (T == 128) ? 2 : 4;
+    const int per_item = kItemRows / T;
     const int64_t wmax = (int64_t)per_item * (dims->max_kv > 0 ? dims->max_kv : 1);
     const int bins = (int)(wmax + 1 < 2048 ? wmax + 1 : 2048);
     int32_t *counter = reinterpret_cast<int32_t *>(workspace);
@@ -307,19 +310,20 @@ vsa_status vsa_block_sparse_fwd(const void *q, const void *k, const void *v, con
     p.order = order;
     p.work_counter = counter;
     p.status = dc.status_ptr.load(std::memory_order_acquire);
-    p.NT = NT;
+    p.NT = NT * sub;
+    p.sub = sub;
     p.max_kv = dims->max_kv;
     p.G = G;
-    p.bm_words = (NT + 31) / 32;
+    p.bm_words = (NT * sub + 31) / 32;
     p.n_items = n_items;
     p.Sp = Sp;
     const float scale = dims->scale > 0.f ? dims->scale : 1.0f / std::sqrt((float)D);
     p.scale_log2 = scale * 1.4426950408889634f;
     const int sms = dc.sm_count.load(std::memory_order_acquire);
     const int grid = n_items < sms ? n_items : sms;
-    if (launch_attn(T, D, tm_q, tm_k, tm_v, p, grid, s) != cudaSuccess) return VSA_ERR_CUDA;
+    if (launch_attn(Tk, D, tm_q, tm_k, tm_v, p, grid, s) != cudaSuccess) return VSA_ERR_CUDA;
 
-    const AttnLaunchInfo info = attn_launch_info(T, D, p.bm_words);
+    const AttnLaunchInfo info = attn_launch_info(Tk, D, p.bm_words);
     t_route.kernel = VSA_KERNEL_ATTN_TCGEN05;
     t_route.tile = T;
     t_route.head_dim = D;

@@ -229,6 +229,15 @@ __device__ __forceinline__ int tile_of_slot(int g, int s) {
     return 4 * g + s;
 }
 
+// Valid tokens of kernel tile jj.  With 256-token tiles (sub == 2) the kernel
+// works on 128-token halves: half jj of caller tile jj/2 holds the tile's
+// tokens from 128*(jj%2) on.
+__device__ __forceinline__ int tile_size(const int32_t *block_sizes, int jj, int sub) {
+    if (sub == 1) return __ldg(block_sizes + jj);
+    const int n = __ldg(block_sizes + (jj >> 1)) - 128 * (jj & 1);
+    return n < 0 ? 0 : (n > 128 ? 128 : n);
+}
+
 template <int T, int D>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -322,10 +331,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 for (int i = lane; i < 4 * W; i += 32) bmp[i] = 0u;
                 __syncwarp();
                 const int bh = item / P.G, g = item - (item / P.G) * P.G;
+                // selections are per caller tile: with 256-token tiles both units
+                // (the two halves of tile g) share row g, and a selected tile j
+                // stands for its two halves 2j and 2j+1
+                const int sub = P.sub, NTc = NT / sub;
                 for (int s = 0; s < 4; ++s) {
                     const int t = tile_of_slot<T>(g, s);
                     if (t < 0 || t >= NT) continue;
-                    const int64_t row = (int64_t)bh * NT + t;
+                    const int64_t row = (int64_t)bh * NTc + t / sub;
                     int K = __ldg(P.q2k_num + row);
                     if (K < 0 || K > P.max_kv) {
                         bad = 1;
@@ -334,14 +347,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     const int32_t *sel = P.q2k_idx + row * P.max_kv;
                     for (int i = lane; i < K; i += 32) {
                         const int j = __ldg(sel + i);
-                        if (j < 0 || j >= NT) {
+                        if (j < 0 || j >= NTc) {
                             bad = 1;
                             continue;
                         }
-                        if (__ldg(P.block_sizes + j) <= 0) continue;
-                        const uint32_t bit = 1u << (j & 31);
-                        const uint32_t old = atomicOr(&bmp[s * W + (j >> 5)], bit);
-                        if (old & bit) bad = 1;  // repeated index
+                        for (int h2 = 0; h2 < sub; ++h2) {
+                            const int jj = j * sub + h2;
+                            if (tile_size(P.block_sizes, jj, sub) <= 0) continue;
+                            const uint32_t bit = 1u << (jj & 31);
+                            const uint32_t old = atomicOr(&bmp[s * W + (jj >> 5)], bit);
+                            if (old & bit) bad = 1;  // repeated index
+                        }
                     }
                 }
                 if (lane == 0) hdr[p * 4] = item;
@@ -432,7 +448,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     // cycle ahead of the fills it waits for.
                     if (!(ok = wait_warp(BAR(BI.kv_full(kst)), kph, abort_flag, P.status))) break;
                     if (!(ok = wait_warp(BAR(BI.kv_full(vst)), vph, abort_flag, P.status))) break;
-                    const int nj = __ldg(P.block_sizes + j);
+                    const int nj = tile_size(P.block_sizes, j, P.sub);
                     if ((nj & 15) == 0) continue;
                     uint4 *vs = reinterpret_cast<uint4 *>(gbase + L.ring + vst * C::kStageBytes);
                     const int n16 = (16 - (nj & 15)) * 8;
@@ -519,7 +535,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         ring.next(NS);
                         const uint32_t vst = ring.st, vph = ring.ph;
                         ring.next(NS);
-                        const int nj = __ldg(P.block_sizes + j);
+                        const int nj = tile_size(P.block_sizes, j, P.sub);
                         const bool tail = (nj & 15) != 0;
                         const uint32_t vzp = (vz_par >> vst) & 1u;
                         if (tail) vz_par ^= 1u << vst;
@@ -602,7 +618,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             const int bh = item / P.G, g = item - (item / P.G) * P.G;
             const int t = (T == 128) ? 2 * g + u : 4 * g + 2 * u + tsub;
             const int r = (T == 128) ? row : (row & 63);
-            const int n_t = (t < NT) ? __ldg(P.block_sizes + t) : 0;
+            const int n_t = (t < NT) ? tile_size(P.block_sizes, t, P.sub) : 0;
             float m = -INFINITY, l0 = 0.f, l1 = 0.f;  // l: this thread's columns
             uint32_t n_mine = 0;
             bool ok = true;
@@ -615,7 +631,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     const int b = __ffs(bits) - 1;
                     bits &= bits - 1;
                     const int j = w * 32 + b;
-                    const int nj = __ldg(P.block_sizes + j);  // loaded before the wait for S
+                    const int nj = tile_size(P.block_sizes, j, P.sub);  // loaded before the wait for S
                     if (!(ok = wait_warp(BAR(BI.s_full(u)), cnt & 1u, abort_flag, P.status))) break;
                     tc_fence_after();
                     const bool member_row = ((mine >> b) & 1u) != 0u;  // warp-uniform

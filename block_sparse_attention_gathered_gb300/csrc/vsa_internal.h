@@ -26,7 +26,8 @@ struct AttnParams {
     const int32_t *order;        // [n_items] work order (longest first)
     int32_t *work_counter;       // next slot of `order` to hand out
     int32_t *status;             // device status word
-    int32_t NT;
+    int32_t NT;                  // kernel tiles (128-token halves when sub == 2)
+    int32_t sub;                 // kernel tiles per caller tile: 1, or 2 for 256-token tiles
     int32_t max_kv;
     int32_t G;                   // work items per (b, h)
     int32_t bm_words;            // 32-bit words of one selection bitmap

@@ -61,13 +61,14 @@ typedef enum {
  * shared memory), tighter than the page's 2^22. */
 #define VSA_MAX_BATCH_HEADS 65535
 #define VSA_MAX_ROWS_LOG2 31        /* B*H*num_tiles*tile < 2^31 */
-#define VSA_MAX_TILES 8192          /* num_tiles <= 8192 */
+#define VSA_MAX_TILES 8192          /* num_tiles <= 8192 (4096 with 256-token tiles) */
 
 typedef struct {
     int32_t B;          /* batch */
     int32_t H;          /* heads */
     int32_t num_tiles;  /* tiles per sequence (NT) */
-    int32_t tile;       /* tokens per tile: 64 or 128 */
+    int32_t tile;       /* tokens per tile: 64, 128 or 256 (256: the fused-layout
+                           commit's training tiles; run as two 128-token halves) */
     int32_t head_dim;   /* 64 or 128 */
     int32_t max_kv;     /* row length of q2k_idx (>= 0) */
     float scale;        /* softmax scale; <= 0 selects 1/sqrt(head_dim) */

@@ -145,7 +145,7 @@ def _random_case(seed, B, H, NT, T, D, pad="naninf", empty_frac=0.15, full=False
 
 
 @pytest.mark.parametrize("T,D,NT", [(64, 64, 9), (64, 128, 7), (128, 64, 5), (128, 128, 5), (64, 64, 1),
-                                    (128, 128, 3)])
+                                    (128, 128, 3), (256, 64, 5), (256, 128, 3), (256, 128, 1)])
 def test_variants_ragged(vsa, oracle_mod, T, D, NT):
     w = _random_case(100 + T + D + NT, 2, 3, NT, T, D)
     (q, k, v), refs = _to_tile_major(w, vsa, oracle_mod)

@@ -61,6 +61,7 @@ def _compare(vsa, oracle_mod, q, k, bs, T, topk, label):
     (1, 4, 70, 128, 128, 12),    # more than two 32-tile chunks of key means
     (1, 2, 9, 128, 64, 20),      # topk above the tile count
     (2, 2, 33, 64, 128, 0),      # topk = 0
+    (1, 2, 9, 256, 128, 4),      # 256-token tiles
 ])
 def test_select_matches_oracle(vsa, oracle_mod, B, H, NT, T, D, topk):
     g = torch.Generator().manual_seed(100 + NT + topk)

@@ -88,6 +88,16 @@ def test_launch_limits(vsa):
     assert _fwd(vsa, vsa.make_dims(65535, 1, 257, 128, 128, 1)) == vsa.VSA_ERR_LIMITS
 
 
+def test_tile_256_limits(vsa):
+    # 256-token tiles run as two 128-token halves: at most 4096 of them
+    assert vsa.vsa_block_sparse_workspace_size(vsa.make_dims(1, 2, 4096, 256, 128, 2)) > 0
+    assert vsa.vsa_block_sparse_workspace_size(vsa.make_dims(1, 2, 4097, 256, 128, 2)) == 0
+    assert _fwd(vsa, vsa.make_dims(1, 2, 4097, 256, 128, 2)) == vsa.VSA_ERR_LIMITS
+    assert _fwd(vsa, vsa.make_dims(1, 2, 4, 512, 128, 2)) == vsa.VSA_ERR_ARG
+    # one 256-row work item per 256-token tile
+    assert vsa.vsa_block_sparse_workspace_size(vsa.make_dims(2, 3, 10, 256, 64, 4)) == 256 + 4 * 6 * 10
+
+
 def test_workspace_size(vsa):
     # header (256 bytes) + one int32 per 256-query-row work item
     d = vsa.make_dims(1, 6, 244, 128, 128, 244)
