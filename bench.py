@@ -178,7 +178,7 @@ def run_reference(args, cfg):
     rank, world, _ = _rank_env()
     if rank != 0:
         return
-    w = W.make_workload(cfg)
+    w = W.make_workload(cfg, tile=args.tile)
     import oracle
     oracle.build()
     nthreads = oracle.default_threads()
@@ -258,7 +258,7 @@ def run_ours(args, cfg):
         torch.cuda.set_device(local)
         dist.init_process_group("nccl")
     dev = torch.device("cuda", torch.cuda.current_device())
-    w = W.make_workload(cfg)
+    w = W.make_workload(cfg, tile=args.tile)
     assert w.token_major
     eff = W.effective_flops(w)
     B, H, D, T, NT, S = w.B, w.H, w.D, w.T, w.NT, w.S
@@ -402,7 +402,7 @@ def run_ours(args, cfg):
             "attn_ms": attn_avg, "layout_ms": lay_avg,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                          "frac": achieved / peak, "traffic": traffic,
-                         "peak_source": f"{src} bf16 burst (cuBLAS)", "kernel": f"attn_fwd_kernel<{T},{D}>"},
+                         "peak_source": f"{src} bf16 burst (cuBLAS)", "kernel": f"attn_fwd_kernel<{min(T, 128)},{D}>"},
             "layout_roofline": {"bound": "hbm", "achieved": lay_gbs, "peak": hbm, "unit": "GB/s",
                                 "frac": lay_gbs / hbm, "bytes": layout_bytes(w),
                                 "peak_source": f"{src} HBM copy", "kernel": "layout_kernel"},
@@ -447,12 +447,16 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", type=int, default=5, choices=[2, 4, 5])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tile", type=int, default=None, choices=[128, 256],
+                    help="dense-limit workload only: tile size (default 128)")
     ap.add_argument("--untile", action="store_true",
                     help="end the step with the un-tiling of the output times a gate")
     ap.add_argument("--select", action="store_true",
                     help="video-grid workload only: select the key tiles on the GPU inside the step")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     args = ap.parse_args()
+    if args.tile not in (None, 128) and args.config != 5:
+        ap.error("--tile 256 needs the dense-limit workload (--config 5)")
     if args.select and args.config != 4:
         ap.error("--select needs the video-grid workload (--config 4)")
     if args.impl == "reference":
