@@ -56,6 +56,8 @@ def _load():
         lib.oracle_coarse_select.restype = i32
         lib.oracle_untile.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, i32]
         lib.oracle_untile.restype = i32
+        lib.oracle_block_sparse_bwd.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, f64, P, P, P, i32]
+        lib.oracle_block_sparse_bwd.restype = i32
         _lib = lib
     return _lib
 
@@ -112,6 +114,25 @@ def block_sparse_attention(q, k, v, q2k_idx, q2k_num, block_sizes, T: int, scale
     if rc != 0:
         raise ValueError(f"oracle_block_sparse_fwd: {ERRORS.get(rc, rc)}")
     return out, lse
+
+
+def block_sparse_attention_bwd(q, k, v, dout, q2k_idx, q2k_num, block_sizes, T: int, scale: float,
+                               nthreads: Optional[int] = None):
+    """FP64 gradients (dq, dk, dv) of the block-sparse forward for tile-major
+    bf16 ``q, k, v`` and upstream gradient ``dout`` ``[B, H, NT*T, D]``; each is a
+    float64 array of the same shape (see ``oracle_block_sparse_bwd``)."""
+    qb, kb, vb, db = _bf16_bits(q), _bf16_bits(k), _bf16_bits(v), _bf16_bits(dout)
+    B, H, Sp, D = qb.shape
+    NT = Sp // T
+    idx, num, bs = _i32(q2k_idx), _i32(q2k_num), _i32(block_sizes)
+    max_kv = int(idx.shape[3])
+    dq, dk, dv = (np.empty((B, H, Sp, D), dtype=np.float64) for _ in range(3))
+    rc = _load().oracle_block_sparse_bwd(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(db), _ptr(idx), _ptr(num), _ptr(bs),
+                                         B, H, NT, T, D, max_kv, float(scale), _ptr(dq), _ptr(dk), _ptr(dv),
+                                         int(nthreads or default_threads()))
+    if rc != 0:
+        raise ValueError(f"oracle_block_sparse_bwd: {ERRORS.get(rc, rc)}")
+    return dq, dk, dv
 
 
 def tile_layout(x_tok, row_to_token, NT: int, T: int) -> np.ndarray:

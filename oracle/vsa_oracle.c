@@ -1,7 +1,7 @@
 /*
- * CPU oracle for the block-sparse attention forward pass, the tile layout, the
- * coarse key-tile selection that produces the block-sparse selection, and the
- * output un-tiling with the gate.
+ * CPU oracle for the block-sparse attention forward and backward passes, the
+ * tile layout, the coarse key-tile selection that produces the block-sparse
+ * selection, and the output un-tiling with the gate.
  *
  * TEST INFRASTRUCTURE ONLY.  This file is the plain, slow, obviously correct
  * FP64 statement of what the GPU library computes.  Only the tests, the smoke
@@ -382,4 +382,159 @@ int oracle_untile(const uint16_t *o_tile, const uint16_t *gate, const int32_t *r
                     dst[d] = gt ? f32_to_bf16_rne((float)(bf16_to_double(o[d]) * bf16_to_double(gt[d]))) : o[d];
             }
     return ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------------
+ * Block-sparse attention backward (the Attn-QAT SM100 commit on the page
+ * names the backward pass and its 64x128 dQ / dK-dV tiles; the gradients are
+ * those of the forward defined above).  For every valid query row with key
+ * list L (the valid rows of its selected key tiles), in FP64:
+ *   s_e = scale * q.k_e,  p = softmax(s) over L,
+ *   dp_e = do.v_e,  delta = sum_e p_e dp_e,  ds_e = p_e (dp_e - delta),
+ *   dq = scale * sum_e ds_e k_e,  dk_e += scale * ds_e q,  dv_e += p_e do.
+ * A row with no keys contributes nothing and gets dq = 0; keys no row selects
+ * get dk = dv = 0; padding rows of dq, dk, dv are 0.  Computed per
+ * (batch, head) in index order, one thread per (batch, head).
+ *   q, k, v, dout: bf16 bits [B,H,NT*T,D]; dq, dk, dv: double [B,H,NT*T,D].
+ * ------------------------------------------------------------------------ */
+typedef struct {
+    const uint16_t *q, *k, *v, *dout;
+    const int32_t *q2k_idx, *q2k_num, *block_sizes;
+    int B, H, NT, T, D, max_kv;
+    double scale;
+    double *dq, *dk, *dv;
+    int64_t next;
+    pthread_mutex_t lock;
+    int status;
+} bwd_job_t;
+
+static void bwd_one_head(bwd_job_t *J, int64_t bh, double *s, double *p, double *dp, double *qrow,
+                         double *drow) {
+    const int T = J->T, D = J->D, NT = J->NT;
+    const int64_t Sp = (int64_t)NT * T;
+    const uint16_t *Qp = J->q + bh * Sp * D, *Kp = J->k + bh * Sp * D, *Vp = J->v + bh * Sp * D;
+    const uint16_t *dOp = J->dout + bh * Sp * D;
+    double *dQ = J->dq + bh * Sp * D, *dK = J->dk + bh * Sp * D, *dV = J->dv + bh * Sp * D;
+    for (int64_t i = 0; i < Sp * D; ++i) dQ[i] = dK[i] = dV[i] = 0.0;
+    for (int t = 0; t < NT; ++t) {
+        const int64_t unit = bh * NT + t;
+        const int K = J->q2k_num[unit];
+        const int32_t *sel = J->q2k_idx + unit * J->max_kv;
+        for (int r = 0; r < J->block_sizes[t]; ++r) {
+            const int64_t qi = (int64_t)t * T + r;
+            for (int d = 0; d < D; ++d) {
+                qrow[d] = bf16_to_double(Qp[qi * D + d]);
+                drow[d] = bf16_to_double(dOp[qi * D + d]);
+            }
+            int64_t n = 0;
+            for (int i = 0; i < K; ++i) {
+                const int j = sel[i];
+                for (int c = 0; c < J->block_sizes[j]; ++c) {
+                    const int64_t kr = (int64_t)j * T + c;
+                    double dot = 0.0, dv = 0.0;
+                    for (int d = 0; d < D; ++d) {
+                        dot += qrow[d] * bf16_to_double(Kp[kr * D + d]);
+                        dv += drow[d] * bf16_to_double(Vp[kr * D + d]);
+                    }
+                    s[n] = J->scale * dot;
+                    dp[n] = dv;
+                    ++n;
+                }
+            }
+            if (n == 0) continue;
+            double m = -INFINITY;
+            for (int64_t e = 0; e < n; ++e) {
+                if (isnan(s[e]) || isnan(m)) m = NAN;
+                else if (s[e] > m) m = s[e];
+            }
+            double l = 0.0;
+            for (int64_t e = 0; e < n; ++e) l += (p[e] = exp(s[e] - m));
+            double delta = 0.0;
+            for (int64_t e = 0; e < n; ++e) {
+                p[e] /= l;
+                delta += p[e] * dp[e];
+            }
+            int64_t e = 0;
+            for (int i = 0; i < K; ++i) {
+                const int j = sel[i];
+                for (int c = 0; c < J->block_sizes[j]; ++c, ++e) {
+                    const int64_t kr = (int64_t)j * T + c;
+                    const double ds = p[e] * (dp[e] - delta);
+                    for (int d = 0; d < D; ++d) {
+                        dQ[qi * D + d] += J->scale * ds * bf16_to_double(Kp[kr * D + d]);
+                        dK[kr * D + d] += J->scale * ds * qrow[d];
+                        dV[kr * D + d] += p[e] * drow[d];
+                    }
+                }
+            }
+        }
+    }
+}
+
+static void *bwd_worker(void *arg) {
+    bwd_job_t *J = (bwd_job_t *)arg;
+    const int64_t max_keys = (int64_t)(J->max_kv > 0 ? J->max_kv : 1) * J->T;
+    double *s = (double *)malloc(sizeof(double) * (size_t)max_keys);
+    double *p = (double *)malloc(sizeof(double) * (size_t)max_keys);
+    double *dp = (double *)malloc(sizeof(double) * (size_t)max_keys);
+    double *qrow = (double *)malloc(sizeof(double) * (size_t)J->D);
+    double *drow = (double *)malloc(sizeof(double) * (size_t)J->D);
+    if (!s || !p || !dp || !qrow || !drow) {
+        pthread_mutex_lock(&J->lock);
+        J->status = ORACLE_ERR_NOMEM;
+        pthread_mutex_unlock(&J->lock);
+    } else {
+        for (;;) {
+            pthread_mutex_lock(&J->lock);
+            const int64_t bh = J->next++;
+            pthread_mutex_unlock(&J->lock);
+            if (bh >= (int64_t)J->B * J->H) break;
+            bwd_one_head(J, bh, s, p, dp, qrow, drow);
+        }
+    }
+    free(s);
+    free(p);
+    free(dp);
+    free(qrow);
+    free(drow);
+    return NULL;
+}
+
+int oracle_block_sparse_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, const uint16_t *dout,
+                            const int32_t *q2k_idx, const int32_t *q2k_num, const int32_t *block_sizes, int B,
+                            int H, int NT, int T, int D, int max_kv, double scale, double *dq, double *dk,
+                            double *dv, int nthreads) {
+    if (!q || !k || !v || !dout || !q2k_num || !block_sizes || !dq || !dk || !dv || B <= 0 || H <= 0 ||
+        NT <= 0 || T <= 0 || D <= 0 || max_kv < 0 || (!q2k_idx && max_kv > 0))
+        return ORACLE_ERR_ARG;
+    bwd_job_t J;
+    memset(&J, 0, sizeof J);
+    J.q = q; J.k = k; J.v = v; J.dout = dout;
+    J.q2k_idx = q2k_idx; J.q2k_num = q2k_num; J.block_sizes = block_sizes;
+    J.B = B; J.H = H; J.NT = NT; J.T = T; J.D = D; J.max_kv = max_kv; J.scale = scale;
+    J.dq = dq; J.dk = dk; J.dv = dv;
+    /* the same selection checks as the forward */
+    job_t C;
+    memset(&C, 0, sizeof C);
+    C.q2k_idx = q2k_idx; C.q2k_num = q2k_num; C.block_sizes = block_sizes;
+    C.B = B; C.H = H; C.NT = NT; C.T = T; C.max_kv = max_kv;
+    C.n_units = (int64_t)B * H * NT;
+    int64_t *all = (int64_t *)malloc(sizeof(int64_t) * (size_t)C.n_units);
+    if (!all) return ORACLE_ERR_NOMEM;
+    for (int64_t u = 0; u < C.n_units; ++u) all[u] = u;
+    C.units = all;
+    const int rc = check_units(&C);
+    free(all);
+    if (rc != ORACLE_OK) return rc;
+    pthread_mutex_init(&J.lock, NULL);
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 256) nthreads = 256;
+    pthread_t th[256];
+    int started = 0;
+    for (int i = 0; i < nthreads; ++i)
+        if (pthread_create(&th[i], NULL, bwd_worker, &J) == 0) ++started;
+    if (started == 0) bwd_worker(&J);
+    for (int i = 0; i < started; ++i) pthread_join(th[i], NULL);
+    pthread_mutex_destroy(&J.lock);
+    return J.status;
 }
