@@ -25,7 +25,7 @@ LIB_PATH = os.path.join(_HERE, "_build", "libvsa.so")
 VSA_OK, VSA_ERR_ARG, VSA_ERR_ALIGN, VSA_ERR_LIMITS, VSA_ERR_ARCH = 0, -1, -2, -3, -4
 VSA_ERR_CUDA, VSA_ERR_TIMEOUT, VSA_ERR_INDEX, VSA_ERR_WORKSPACE = -5, -6, -7, -8
 VSA_KERNEL_NONE, VSA_KERNEL_ATTN_TCGEN05, VSA_KERNEL_LAYOUT, VSA_KERNEL_VALIDATE = 0, 1, 2, 3
-VSA_KERNEL_SELECT, VSA_KERNEL_UNTILE = 4, 5
+VSA_KERNEL_SELECT, VSA_KERNEL_UNTILE, VSA_KERNEL_BWD = 4, 5, 6
 VSA_MAX_BATCH_HEADS, VSA_MAX_TILES = 65535, 8192
 
 
@@ -65,6 +65,8 @@ def _load() -> ctypes.CDLL:
         "vsa_tile_layout": ([P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, P], i32),
         "vsa_validate_indices": ([P, P, P, dims_p, P, P], i32),
         "vsa_untile": ([P, P, P, P, i32, i32, i32, i32, i32, i32, P], i32),
+        "vsa_block_sparse_bwd_workspace_size": ([dims_p], sz),
+        "vsa_block_sparse_bwd": ([P] * 12 + [dims_p, P, sz, P], i32),
         "vsa_coarse_select_workspace_size": ([dims_p], sz),
         "vsa_coarse_select": ([P, P, P, i32, P, P, dims_p, P, sz, P], i32),
         "vsa_check_device_status": ([P], i32),
@@ -80,7 +82,7 @@ def _load() -> ctypes.CDLL:
 
 _lib = _load()
 EXPORTED = ("vsa_block_sparse_workspace_size", "vsa_block_sparse_fwd", "vsa_block_sparse_fwd_noalloc",
-            "vsa_tile_layout", "vsa_untile", "vsa_coarse_select_workspace_size", "vsa_coarse_select",
+            "vsa_block_sparse_bwd_workspace_size", "vsa_block_sparse_bwd", "vsa_tile_layout", "vsa_untile", "vsa_coarse_select_workspace_size", "vsa_coarse_select",
             "vsa_validate_indices", "vsa_check_device_status", "vsa_last_route",
             "vsa_status_string", "vsa_version")
 
@@ -149,6 +151,21 @@ def vsa_tile_layout(q_tok, k_tok, v_tok, q_tile, k_tile, v_tile, row_to_token, B
                               int(num_tiles), int(tile), _stream(stream))
     if st != VSA_OK:
         raise VsaError(st, "vsa_tile_layout")
+
+
+def vsa_block_sparse_bwd_workspace_size(dims: VsaDims) -> int:
+    return int(_lib.vsa_block_sparse_bwd_workspace_size(ctypes.byref(dims)))
+
+
+def vsa_block_sparse_bwd(q, k, v, out, dout, lse, q2k_idx, q2k_num, block_sizes, dq, dk, dv, dims: VsaDims,
+                         workspace: torch.Tensor, stream=None) -> None:
+    st = _lib.vsa_block_sparse_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), _ptr(q2k_idx),
+                                   _ptr(q2k_num), _ptr(block_sizes), _ptr(dq), _ptr(dk), _ptr(dv),
+                                   ctypes.byref(dims), _ptr(workspace),
+                                   workspace.numel() * workspace.element_size() if workspace is not None else 0,
+                                   _stream(stream))
+    if st != VSA_OK:
+        raise VsaError(st, "vsa_block_sparse_bwd")
 
 
 def vsa_untile(o_tile, gate_tok, out_tok, row_to_token, B, S, H, D, num_tiles, tile, stream=None) -> None:
@@ -228,6 +245,27 @@ def block_sparse_attention(q, k, v, q2k_idx, q2k_num, block_sizes, tile: int,
     vsa_block_sparse_fwd(q, k, v, q2k_idx, q2k_num.contiguous(), block_sizes.contiguous(), out, lse,
                          dims, workspace, stream)
     return (out, lse) if want_lse else out
+
+
+def block_sparse_attention_bwd(q, k, v, out, dout, lse, q2k_idx, q2k_num, block_sizes, tile: int,
+                               scale: Optional[float] = None, workspace: Optional[torch.Tensor] = None,
+                               stream=None):
+    """Gradients ``(dq, dk, dv)`` (bf16, tile-major like ``q``) of the forward
+    that produced ``out`` and ``lse``."""
+    _check_bf16_cuda(q, k, v, out, dout)
+    B, H, Sp, D = q.shape
+    NT = Sp // tile
+    q2k_idx = q2k_idx.contiguous()
+    dims = make_dims(B, H, NT, tile, D, q2k_idx.shape[-1], scale)
+    need = vsa_block_sparse_bwd_workspace_size(dims)
+    if need == 0:
+        raise VsaError(VSA_ERR_ARG, "vsa_block_sparse_bwd_workspace_size")
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+    vsa_block_sparse_bwd(q, k, v, out, dout, lse.contiguous(), q2k_idx, q2k_num.contiguous(),
+                         block_sizes.contiguous(), dq, dk, dv, dims, workspace, stream)
+    return dq, dk, dv
 
 
 def coarse_select(q, k, block_sizes, tile: int, topk: int, workspace: Optional[torch.Tensor] = None,

@@ -385,6 +385,104 @@ vsa_status vsa_tile_layout(const void *q_tok, const void *k_tok, const void *v_t
     return VSA_OK;
 }
 
+static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// Workspace of the backward: [header | delta | k2q offsets | k2q lists].
+struct BwdWs {
+    size_t delta, offs, list, total;
+};
+
+static BwdWs bwd_ws(const vsa_dims *d) {
+    const size_t BH = (size_t)d->B * d->H, NT = (size_t)d->num_tiles, Sp = NT * d->tile;
+    BwdWs w;
+    w.delta = kWsHeader;
+    w.offs = w.delta + align256(4 * BH * Sp);
+    w.list = w.offs + align256(4 * BH * (NT + 1));
+    w.total = w.list + align256(4 * BH * NT * (size_t)(d->max_kv > 0 ? d->max_kv : 1));
+    return w;
+}
+
+size_t vsa_block_sparse_bwd_workspace_size(const vsa_dims *dims) {
+    if (check_dims(dims) != VSA_OK || dims->tile != 128) return 0;
+    return bwd_ws(dims).total;
+}
+
+vsa_status vsa_block_sparse_bwd(const void *q, const void *k, const void *v, const void *out, const void *dout,
+                                const float *lse, const int32_t *q2k_idx, const int32_t *q2k_num,
+                                const int32_t *block_sizes, void *dq, void *dk, void *dv, const vsa_dims *dims,
+                                void *workspace, size_t workspace_bytes, vsa_stream_t stream) {
+    vsa_status st = check_dims(dims);
+    if (st != VSA_OK) return st;
+    if (dims->tile != 128) return VSA_ERR_ARG;
+    if (!q || !k || !v || !out || !dout || !lse || !q2k_num || !block_sizes || !dq || !dk || !dv ||
+        (!q2k_idx && dims->max_kv > 0))
+        return VSA_ERR_ARG;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) || !aligned(dout, 16) ||
+        !aligned(lse, 16) || !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(q2k_num, 4) ||
+        !aligned(block_sizes, 4) || (q2k_idx && !aligned(q2k_idx, 4)))
+        return VSA_ERR_ALIGN;
+    const BwdWs w = bwd_ws(dims);
+    if (!workspace || workspace_bytes < w.total) return VSA_ERR_WORKSPACE;
+    if (!aligned(workspace, 16)) return VSA_ERR_ALIGN;
+    int dev = 0;
+    if ((st = current_device(&dev)) != VSA_OK) return st;
+    DeviceCache &dc = g_dev[dev];
+    constexpr unsigned kBwdBit = 1u << 5;
+    if (!(dc.attn_prepared.load(std::memory_order_acquire) & kBwdBit)) {
+        if (bwd_prepare() != cudaSuccess) {
+            cudaGetLastError();
+            return VSA_ERR_CUDA;
+        }
+        dc.attn_prepared.fetch_or(kBwdBit, std::memory_order_acq_rel);
+    }
+    const int D = dims->head_dim, NT = dims->num_tiles;
+    const int64_t Sp = (int64_t)NT * 128;
+    const int64_t rows = (int64_t)dims->B * dims->H * Sp;
+    CUtensorMap tm_q, tm_k, tm_v, tm_do;
+    if ((st = encode_rows_map(&tm_q, q, rows, D, 128)) != VSA_OK) return st;
+    if ((st = encode_rows_map(&tm_k, k, rows, D, 128)) != VSA_OK) return st;
+    if ((st = encode_rows_map(&tm_v, v, rows, D, 128)) != VSA_OK) return st;
+    if ((st = encode_rows_map(&tm_do, dout, rows, D, 128)) != VSA_OK) return st;
+    char *ws = reinterpret_cast<char *>(workspace);
+    BwdLaunch L;
+    L.tm_q = &tm_q;
+    L.tm_k = &tm_k;
+    L.tm_v = &tm_v;
+    L.tm_do = &tm_do;
+    L.out = out;
+    L.dout = dout;
+    L.lse = lse;
+    L.delta = reinterpret_cast<float *>(ws + w.delta);
+    L.q2k_idx = q2k_idx;
+    L.q2k_num = q2k_num;
+    L.block_sizes = block_sizes;
+    L.k2q_offs = reinterpret_cast<int32_t *>(ws + w.offs);
+    L.k2q_list = reinterpret_cast<int32_t *>(ws + w.list);
+    L.dq = dq;
+    L.dk = dk;
+    L.dv = dv;
+    L.status = dc.status_ptr.load(std::memory_order_acquire);
+    L.BH = dims->B * dims->H;
+    L.NT = NT;
+    L.D = D;
+    L.max_kv = dims->max_kv;
+    L.Sp = Sp;
+    L.scale = dims->scale > 0.f ? dims->scale : 1.0f / std::sqrt((float)D);
+    if (launch_bwd(L, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return VSA_ERR_CUDA;
+    }
+    t_route = vsa_route{};
+    t_route.kernel = VSA_KERNEL_BWD;
+    t_route.tile = 128;
+    t_route.head_dim = D;
+    t_route.grid = (int32_t)((int64_t)L.BH * NT);
+    t_route.block = 160;
+    t_route.work_items = (int64_t)L.BH * NT;
+    t_route.smem_bytes = (int32_t)bwd_smem_bytes(D);
+    return VSA_OK;
+}
+
 vsa_status vsa_untile(const void *o_tile, const void *gate_tok, void *out_tok, const int32_t *row_to_token,
                       int32_t B, int32_t S, int32_t H, int32_t D, int32_t num_tiles, int32_t tile,
                       vsa_stream_t stream) {

@@ -78,6 +78,25 @@ struct UntileParams {
 
 cudaError_t launch_untile(const UntileParams &p, int num_sms, cudaStream_t stream);
 
+// Backward pass (vsa_bwd.cu), 128-token tiles.
+struct BwdLaunch {
+    const CUtensorMap *tm_q, *tm_k, *tm_v, *tm_do;  // rows of D bf16, box {64, 128}
+    const void *out, *dout;                           // bf16 [B*H*Sp, D]
+    const float *lse;                                 // [B*H*Sp]
+    float *delta;                                     // workspace [B*H*Sp]
+    const int32_t *q2k_idx, *q2k_num, *block_sizes;
+    int32_t *k2q_offs, *k2q_list;                     // workspace [B*H, NT+1], [B*H, NT*max_kv]
+    void *dq, *dk, *dv;                               // bf16 [B*H*Sp, D]
+    int32_t *status;
+    int32_t BH, NT, D, max_kv;
+    int64_t Sp;
+    float scale;
+};
+
+size_t bwd_smem_bytes(int D);
+cudaError_t bwd_prepare();
+cudaError_t launch_bwd(const BwdLaunch &L, cudaStream_t stream);
+
 // Coarse key-tile selection (vsa_select.cu).
 constexpr uint32_t kSelectSmemLimit = 232448;  // 227 KB opt-in per CTA
 

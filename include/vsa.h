@@ -93,6 +93,7 @@ typedef struct {
 #define VSA_KERNEL_VALIDATE 3
 #define VSA_KERNEL_SELECT 4
 #define VSA_KERNEL_UNTILE 5
+#define VSA_KERNEL_BWD 6
 
 /* Bytes of workspace vsa_block_sparse_fwd needs for `dims` (the on-device work
  * order and its counter).  Returns 0 when `dims` is invalid. */
@@ -175,6 +176,34 @@ vsa_status vsa_tile_layout(const void *q_tok, const void *k_tok, const void *v_t
                            void *k_tile, void *v_tile, const int32_t *row_to_token, int32_t B,
                            int32_t S, int32_t H, int32_t D, int32_t num_tiles, int32_t tile,
                            vsa_stream_t stream);
+
+/*
+ * Block-sparse attention backward (the Attn-QAT SM100 commit names the
+ * backward pass and its dQ / dK-dV tiles; the gradients are those of
+ * vsa_block_sparse_fwd).  With p = exp(scale * q.k - lse) over the valid rows
+ * of the selected key tiles and delta = rowsum(dout * out):
+ *   dv_k = sum_i p_ik dout_i,   ds_ik = p_ik (dout_i.v_k - delta_i),
+ *   dq_i = scale * sum_k ds_ik k_k,   dk_k = scale * sum_i ds_ik q_i.
+ * Rows with no keys get dq = 0, keys no row selects get dk = dv = 0, padding
+ * rows are +0; a NaN row of the forward gives NaN gradients on its keys.
+ *
+ *   q, k, v, out, dout  bf16 [B, H, NT*128, D] tile-major (out and lse as
+ *                       vsa_block_sparse_fwd wrote them; lse is required)
+ *   q2k_idx, q2k_num, block_sizes  the forward's selection (distinct,
+ *                       in-range tiles; out-of-range entries are skipped and
+ *                       flagged, repeated ones count twice)
+ *   dq, dk, dv          bf16 [B, H, NT*128, D] outputs, written completely
+ *   dims                tile must be 128; head_dim 64 or 128
+ *   workspace           vsa_block_sparse_bwd_workspace_size(dims) bytes
+ * Deterministic: dQ is recomputed per query tile instead of accumulated with
+ * atomics, and dK/dV sum their query tiles in ascending order.
+ */
+size_t vsa_block_sparse_bwd_workspace_size(const vsa_dims *dims);
+
+vsa_status vsa_block_sparse_bwd(const void *q, const void *k, const void *v, const void *out, const void *dout,
+                                const float *lse, const int32_t *q2k_idx, const int32_t *q2k_num,
+                                const int32_t *block_sizes, void *dq, void *dk, void *dv, const vsa_dims *dims,
+                                void *workspace, size_t workspace_bytes, vsa_stream_t stream);
 
 /*
  * Output un-tiling with the gate, the inverse of vsa_tile_layout (the fused
