@@ -14,16 +14,18 @@
 //   k2q_kernel     per (batch, head) the transposed selection: for every key
 //                  tile, the query tiles that select it, in ascending order
 //                  (one CTA per (batch, head), deterministic).
-//   dkdv_kernel    one CTA per (batch, head, key tile j): K_j and V_j stay in
-//                  shared memory; for every query tile t that selects j,
-//                  S^T = K_j Q_t^T and dP^T = V_j dO_t^T go to TMEM, four
-//                  elementwise warps (one thread per key row) form P^T and
-//                  dS^T in bf16 in shared memory, and dV += P^T dO_t,
-//                  dK += dS^T Q_t accumulate in TMEM.
-//   dq_kernel      one CTA per (batch, head, query tile t): Q_t and dO_t stay;
-//                  for every selected key tile, S and dP again, dS in shared
-//                  memory, dQ += dS K_j in TMEM.  Recomputing S and dP keeps
-//                  dQ free of atomics and the result deterministic.
+//   bwd_kernel<D, true>   one CTA per (batch, head, key tile j): K_j and V_j
+//                  stay in shared memory; the query tiles t that select j
+//                  stream through two buffers (the next pair's copies overlap
+//                  this pair's work).  S^T = K_j Q_t^T and dP^T = V_j dO_t^T
+//                  go to TMEM; four elementwise warps (one thread per key row)
+//                  write P^T and dS^T as bf16 back into TMEM over the columns
+//                  they read; dV += P^T dO_t and dK += dS^T Q_t accumulate in
+//                  TMEM with the A operand taken from TMEM.
+//   bwd_kernel<D, false>  one CTA per (batch, head, query tile t): Q_t and dO_t
+//                  stay; for every selected key tile, S and dP again, dS back
+//                  into TMEM, dQ += dS K_j.  Recomputing S and dP keeps dQ
+//                  free of atomics and the result deterministic.
 // Padding rows are kept out of every product: P and dS are set (not
 // multiplied) to 0 outside the valid rows and columns, and padding rows of an
 // operand that is summed over (Q and dO in dk/dv, K in dq) are zeroed in shared
@@ -48,17 +50,9 @@ constexpr uint32_t kChunkBytes = kBT * 128;  // one 64-column (128-byte) chunk o
 template <int D>
 struct BwdCfg {
     static constexpr uint32_t kTile = kBT * D * 2;   // one Q/K/V/dO tile in shared memory
-    static constexpr uint32_t kPanel = kBT * kBT * 2;  // P^T, dS^T or dS: 128 x 128 bf16
     static constexpr uint32_t kIdescSq = idesc_bf16(128, kBT, false);  // S-like products, N = 128
     static constexpr uint32_t kIdescAcc = idesc_bf16(128, D, true);    // accumulations, B MN-major
 };
-
-// Byte offset of element (row, col) of a 128-row bf16 panel stored as 64-column
-// chunks with the 128-byte swizzle (16-byte granule g of row r sits at g ^ (r & 7)).
-__device__ __forceinline__ uint32_t sw128(int row, int col) {
-    const int chunk = col >> 6, g = (col >> 3) & 7;
-    return (uint32_t)(chunk * kChunkBytes + row * 128 + ((g ^ (row & 7)) << 4) + (col & 7) * 2);
-}
 
 // Zeroes rows [from, 128) of a tile of D columns (whole rows, so the swizzle
 // does not matter); thread `row` clears its own row.
@@ -81,17 +75,6 @@ __device__ __forceinline__ void mma_sq(uint32_t tdst, uint32_t a_saddr, uint32_t
     for (int kk = 0; kk < D / 16; ++kk)
         mma_ss(tdst, a + (kk >> 2) * (kChunkBytes >> 4) + (kk & 3) * 2, b + (kk >> 2) * (kChunkBytes >> 4) + (kk & 3) * 2,
                BwdCfg<D>::kIdescSq, kk > 0 ? 1u : 0u);
-}
-
-// Issues the 8 MMAs of acc(128 x D) += panel(128 x 128, K-major) x tile(128 x D,
-// MN-major: the tile's rows are the summed dimension).
-template <int D>
-__device__ __forceinline__ void mma_acc(uint32_t tacc, uint32_t panel_saddr, uint32_t tile_saddr, bool accumulate) {
-    const uint64_t a = sdesc_sw128(panel_saddr, 16, 1024), b = sdesc_sw128(tile_saddr, kChunkBytes, 1024);
-#pragma unroll
-    for (int kk = 0; kk < kBT / 16; ++kk)
-        mma_ss(tacc, a + (kk >> 2) * (kChunkBytes >> 4) + (kk & 3) * 2, b + kk * (2048 >> 4), BwdCfg<D>::kIdescAcc,
-               (accumulate || kk > 0) ? 1u : 0u);
 }
 
 // ---------------------------------------------------------------- delta
@@ -167,19 +150,22 @@ __global__ void __launch_bounds__(1024)
 }
 
 // ---------------------------------------------------------------- shared memory
+// Resident pair of tiles (K_j, V_j for dK/dV; Q_t, dO_t for dQ), two buffers of
+// the per-pair tiles (so the next pair's copies overlap this pair's work), and
+// per buffer the lse and delta rows of the query tile (dK/dV only).
 template <int D>
 struct BwdSmem {
-    static constexpr uint32_t kA = 0;                                   // K_j (dkdv) / Q_t (dq)
-    static constexpr uint32_t kB = kA + BwdCfg<D>::kTile;               // V_j / dO_t
-    static constexpr uint32_t kC = kB + BwdCfg<D>::kTile;               // Q_t / K_j
-    static constexpr uint32_t kE = kC + BwdCfg<D>::kTile;               // dO_t / V_j
-    static constexpr uint32_t kP = kE + BwdCfg<D>::kTile;               // P^T panel (dkdv)
-    static constexpr uint32_t kS = kP + BwdCfg<D>::kPanel;              // dS^T / dS panel
-    static constexpr uint32_t kVec = kS + BwdCfg<D>::kPanel;            // lse [128], delta [128] floats
-    static constexpr uint32_t kBars = kVec + 2 * kBT * 4;               // 8 mbarriers
-    static constexpr uint32_t kSlot = kBars + 8 * 8;                    // TMEM address
-    static constexpr uint32_t kFlag = kSlot + 4;                        // abort flag
-    static constexpr uint32_t kTotal = kFlag + 4 + 1024;                // + alignment slack
+    static constexpr uint32_t kRes0 = 0;
+    static constexpr uint32_t kRes1 = kRes0 + BwdCfg<D>::kTile;
+    static constexpr uint32_t kBuf = kRes1 + BwdCfg<D>::kTile;                  // [2][2 tiles]
+    static constexpr uint32_t kVec = kBuf + 4 * BwdCfg<D>::kTile;               // [2][lse 128 | delta 128]
+    static constexpr uint32_t kBars = kVec + 2 * 2 * kBT * 4;                   // mbarriers
+    static constexpr uint32_t kSlot = kBars + 8 * 8;                            // TMEM address
+    static constexpr uint32_t kFlag = kSlot + 4;                                // abort flag
+    static constexpr uint32_t kTotal = kFlag + 4 + 1024;                        // + alignment slack
+    static __device__ __forceinline__ uint32_t buf(int b, int which) {
+        return kBuf + (uint32_t)(2 * b + which) * BwdCfg<D>::kTile;
+    }
 };
 
 struct BwdArgs {
@@ -194,16 +180,30 @@ struct BwdArgs {
     float scale;
 };
 
-// mbarriers: resident tiles loaded, per-pair tiles loaded, S and dP in TMEM,
-// P/dS panels written, pair's accumulations done, and the issuer's final drain
-enum { kBarLd0 = 0, kBarLd1 = 1, kBarS = 2, kBarEw = 3, kBarPair = 4, kBarDrain = 5 };
+// mbarriers: resident tiles loaded, per-buffer tiles loaded (two), S and dP in
+// TMEM, P/dS written back to TMEM, the pair's accumulations done, the
+// issuer's final drain
+enum { kBarRes = 0, kBarBuf0 = 1, kBarBuf1 = 2, kBarS = 3, kBarEw = 4, kBarPair = 5, kBarDrain = 6 };
 
-// ---------------------------------------------------------------- dK, dV
+// Issues the 8 MMAs of acc(128 x D) += A(128 x 128, bf16 pairs in TMEM) x
+// tile(128 x D, MN-major in shared memory: the tile's rows are summed).
 template <int D>
+__device__ __forceinline__ void mma_acc_ts(uint32_t tacc, uint32_t ta, uint32_t tile_saddr, bool accumulate) {
+    const uint64_t b = sdesc_sw128(tile_saddr, kChunkBytes, 1024);
+#pragma unroll
+    for (int kk = 0; kk < kBT / 16; ++kk)
+        mma_ts(tacc, ta + kk * 8, b + kk * (2048 >> 4), BwdCfg<D>::kIdescAcc, (accumulate || kk > 0) ? 1u : 0u);
+}
+
+// Common shape of both kernels: one resident tile pair, a list of partner
+// tiles streamed through two buffers, per pair two 128 x 128 products into
+// TMEM (S-like and dP-like), an elementwise step by 128 threads that writes
+// bf16 operands back into TMEM, and one or two accumulations from TMEM.
+template <int D, bool KV>
 __global__ void __launch_bounds__(160, 1)
-    dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                const BwdArgs A) {
+    bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+               const BwdArgs A) {
     using C = BwdCfg<D>;
     using L = BwdSmem<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -213,26 +213,33 @@ __global__ void __launch_bounds__(160, 1)
     const uint32_t bars = base + L::kBars;
     auto BAR = [&](int i) -> uint32_t { return bars + 8u * (uint32_t)i; };
     volatile int *abort_flag = reinterpret_cast<int *>(g + L::kFlag);
-    const float *s_lse = reinterpret_cast<const float *>(g + L::kVec);
-    const float *s_dl = s_lse + kBT;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    const int64_t bhj = blockIdx.x;
+    // the resident tile x and its list of partners: key tile j and the query
+    // tiles selecting it (KV), or query tile t and its selected key tiles
+    const int64_t bhx = blockIdx.x;
     const int NT = A.NT;
-    const int j = (int)(bhj % NT);
-    const int64_t bh = bhj / NT;
-    const int n_j = __ldg(A.block_sizes + j);
-    const int32_t off0 = __ldg(A.k2q_offs + bh * (NT + 1) + j), off1 = __ldg(A.k2q_offs + bh * (NT + 1) + j + 1);
-    const int32_t *lst = A.k2q_list + bh * (int64_t)NT * A.max_kv + off0;
-    const int n = off1 - off0;
+    const int x = (int)(bhx % NT);
+    const int64_t bh = bhx / NT;
+    const int n_x = __ldg(A.block_sizes + x);
+    const int32_t *lst;
+    int n;
+    if (KV) {
+        const int32_t off0 = __ldg(A.k2q_offs + bh * (NT + 1) + x), off1 = __ldg(A.k2q_offs + bh * (NT + 1) + x + 1);
+        lst = A.k2q_list + bh * (int64_t)NT * A.max_kv + off0;
+        n = off1 - off0;
+    } else {
+        lst = A.q2k_idx + bhx * A.max_kv;
+        n = __ldg(A.q2k_num + bhx);
+        n = n < 0 ? 0 : (n > A.max_kv ? A.max_kv : n);
+    }
+    auto partner = [&](int i) -> int {
+        const int y = __ldg(lst + i);
+        return (y < 0 || y >= NT) ? -1 : y;  // bad entries were flagged by k2q_kernel
+    };
 
     if (threadIdx.x == 0) {
-        mbar_init(BAR(kBarLd0), 1);
-        mbar_init(BAR(kBarLd1), 1);
-        mbar_init(BAR(kBarS), 1);
-        mbar_init(BAR(kBarEw), kEwThreads);
-        mbar_init(BAR(kBarPair), 1);
-        mbar_init(BAR(kBarDrain), 1);
+        for (int b = 0; b < 7; ++b) mbar_init(BAR(b), b == kBarEw ? kEwThreads : 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -244,50 +251,71 @@ __global__ void __launch_bounds__(160, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(g + L::kSlot);
-    const uint32_t tS = tmem, tdP = tmem + kBT, tdV = tmem + 2 * kBT, tdK = tmem + 2 * kBT + D;
+    // TMEM: accumulators first (dV, dK) or (dQ), then S-like and dP-like; the
+    // bf16 P / dS operands are written back over the first half of those
+    const uint32_t tAcc0 = tmem, tAcc1 = tmem + D;
+    const uint32_t tS = tmem + (KV ? 2 * D : D), tdP = tS + kBT;
 
     if (warp == kCtlWarp) {
         if (lane == 0) {
-            const int32_t krow = (int32_t)(bh * A.Sp + (int64_t)j * kBT);
             bool ok = true;
-            int ld1 = 0, ld1_seen = 0;  // per-pair loads issued / waited for
-            if (n > 0) {
-                mbar_arrive_expect_tx(BAR(kBarLd0), 2 * C::kTile);
+            int issued[2] = {0, 0}, seen[2] = {0, 0};  // per-buffer loads issued / waited for
+            const int32_t xrow = (int32_t)(bh * A.Sp + (int64_t)x * kBT);
+            auto load_pair = [&](int i) {
+                const int b = i & 1, y = partner(i);
+                const int64_t yrow = bh * A.Sp + (int64_t)(y < 0 ? 0 : y) * kBT;
+                const uint32_t bar = BAR(kBarBuf0 + b);
+                mbar_arrive_expect_tx(bar, 2 * C::kTile + (KV ? 2 * kBT * 4 : 0));
                 for (int c = 0; c < D / 64; ++c) {
-                    tma_load_2d(base + L::kA + c * kChunkBytes, &tm_k, c * 64, krow, BAR(kBarLd0), l2_policy_evict_first());
-                    tma_load_2d(base + L::kB + c * kChunkBytes, &tm_v, c * 64, krow, BAR(kBarLd0), l2_policy_evict_first());
+                    tma_load_2d(base + L::buf(b, 0) + c * kChunkBytes, KV ? (const void *)&tm_q : (const void *)&tm_k,
+                                c * 64, (int32_t)yrow, bar, l2_policy_evict_last());
+                    tma_load_2d(base + L::buf(b, 1) + c * kChunkBytes, KV ? (const void *)&tm_do : (const void *)&tm_v,
+                                c * 64, (int32_t)yrow, bar, l2_policy_evict_last());
                 }
+                if (KV) {
+                    bulk_load(base + L::kVec + b * 2 * kBT * 4, A.lse + yrow, kBT * 4, bar);
+                    bulk_load(base + L::kVec + b * 2 * kBT * 4 + kBT * 4, A.delta + yrow, kBT * 4, bar);
+                }
+                ++issued[b];
+            };
+            if (n > 0) {
+                mbar_arrive_expect_tx(BAR(kBarRes), 2 * C::kTile);
+                for (int c = 0; c < D / 64; ++c) {
+                    tma_load_2d(base + L::kRes0 + c * kChunkBytes, KV ? (const void *)&tm_k : (const void *)&tm_q,
+                                c * 64, xrow, BAR(kBarRes), l2_policy_evict_first());
+                    tma_load_2d(base + L::kRes1 + c * kChunkBytes, KV ? (const void *)&tm_v : (const void *)&tm_do,
+                                c * 64, xrow, BAR(kBarRes), l2_policy_evict_first());
+                }
+                load_pair(0);
             }
             for (int i = 0; i < n && ok; ++i) {
-                const int t = __ldg(lst + i);
-                // the previous pair's products are done: Q, dO and both panels are free
+                const int b = i & 1;
+                // the previous pair is done: its TMEM operands and its buffer are free
                 if (i > 0 && !(ok = wait_bar(BAR(kBarPair), (i - 1) & 1u, abort_flag, A.status))) break;
-                const int64_t qrow = bh * A.Sp + (int64_t)t * kBT;
-                mbar_arrive_expect_tx(BAR(kBarLd1), 2 * C::kTile + 2 * kBT * 4);
-                for (int c = 0; c < D / 64; ++c) {
-                    tma_load_2d(base + L::kC + c * kChunkBytes, &tm_q, c * 64, (int32_t)qrow, BAR(kBarLd1), l2_policy_evict_last());
-                    tma_load_2d(base + L::kE + c * kChunkBytes, &tm_do, c * 64, (int32_t)qrow, BAR(kBarLd1), l2_policy_evict_last());
-                }
-                bulk_load(base + L::kVec, A.lse + qrow, kBT * 4, BAR(kBarLd1));
-                bulk_load(base + L::kVec + kBT * 4, A.delta + qrow, kBT * 4, BAR(kBarLd1));
-                ++ld1;
-                if (i == 0 && !(ok = wait_bar(BAR(kBarLd0), 0u, abort_flag, A.status))) break;
-                if (!(ok = wait_bar(BAR(kBarLd1), i & 1u, abort_flag, A.status))) break;
-                ++ld1_seen;
+                if (i + 1 < n) load_pair(i + 1);
+                if (i == 0 && !(ok = wait_bar(BAR(kBarRes), 0u, abort_flag, A.status))) break;
+                if (!(ok = wait_bar(BAR(kBarBuf0 + b), (i >> 1) & 1u, abort_flag, A.status))) break;
+                ++seen[b];
                 tc_fence_after();
-                mma_sq<D>(tS, base + L::kA, base + L::kC);   // S^T = K_j Q_t^T
-                mma_sq<D>(tdP, base + L::kB, base + L::kE);  // dP^T = V_j dO_t^T
+                // KV: S^T = K_j Q_t^T, dP^T = V_j dO_t^T; else S = Q_t K_j^T, dP = dO_t V_j^T
+                mma_sq<D>(tS, base + L::kRes0, base + L::buf(b, 0));
+                mma_sq<D>(tdP, base + L::kRes1, base + L::buf(b, 1));
                 mma_commit(BAR(kBarS));
                 if (!(ok = wait_bar(BAR(kBarEw), i & 1u, abort_flag, A.status))) break;
                 tc_fence_after();
-                mma_acc<D>(tdV, base + L::kP, base + L::kE, i > 0);  // dV += P^T dO_t
-                mma_acc<D>(tdK, base + L::kS, base + L::kC, i > 0);  // dK += dS^T Q_t
+                if (KV) {
+                    mma_acc_ts<D>(tAcc0, tS, base + L::buf(b, 1), i > 0);   // dV += P^T dO_t
+                    mma_acc_ts<D>(tAcc1, tdP, base + L::buf(b, 0), i > 0);  // dK += dS^T Q_t
+                } else {
+                    mma_acc_ts<D>(tAcc0, tS, base + L::buf(b, 0), i > 0);   // dQ += dS K_j
+                }
                 mma_commit(BAR(kBarPair));
             }
             if (!ok) {
                 // copies in flight must land before the CTA leaves
-                if (n > 0) drain_wait(BAR(kBarLd0), 0u);
-                if (ld1 > ld1_seen) drain_wait(BAR(kBarLd1), (ld1 - 1) & 1u);
+                if (n > 0) drain_wait(BAR(kBarRes), 0u);
+                for (int b = 0; b < 2; ++b)
+                    if (issued[b] > seen[b]) drain_wait(BAR(kBarBuf0 + b), (issued[b] - 1) & 1u);
             }
             // every MMA this thread issued completes before TMEM is released
             mma_commit(BAR(kBarDrain));
@@ -296,24 +324,31 @@ __global__ void __launch_bounds__(160, 1)
         __syncwarp();
     } else {
         // ------------------------------------------------------------ elementwise
-        const int r = threadIdx.x;  // key row (TMEM lane)
+        // thread r owns TMEM lane r: a key row (KV) or a query row
+        const int r = threadIdx.x;
         const uint32_t tl = (uint32_t)(warp * 32) << 16;
         const float c1 = A.scale * 1.4426950408889634f;
+        const int64_t xrow_r = bh * A.Sp + (int64_t)x * kBT + r;
+        const float lse2_r = KV ? 0.f : __ldg(A.lse + xrow_r) * 1.4426950408889634f;
+        const float dl_r = KV ? 0.f : __ldg(A.delta + xrow_r);
         bool ok = true;
         for (int i = 0; i < n; ++i) {
-            const int t = __ldg(lst + i);
-            const int n_t = __ldg(A.block_sizes + t);
+            const int b = i & 1, y = partner(i);
+            const int n_y = y < 0 ? 0 : __ldg(A.block_sizes + y);
             if (!(ok = wait_warp(BAR(kBarS), i & 1u, abort_flag, A.status))) break;
-            // the pair's copies (Q_t, dO_t, lse, delta) are complete and visible here
-            if (!(ok = wait_warp(BAR(kBarLd1), i & 1u, abort_flag, A.status))) break;
+            // the pair's copies are complete and visible here
+            if (!(ok = wait_warp(BAR(kBarBuf0 + b), (i >> 1) & 1u, abort_flag, A.status))) break;
             tc_fence_after();
-            // Q_t and dO_t are summed over their rows next: clear the padding rows
-            zero_row_if<D>(g + L::kC, r, n_t);
-            zero_row_if<D>(g + L::kE, r, n_t);
+            // operands summed over their rows next get their padding rows cleared:
+            // Q_t and dO_t (KV), K_j (dQ)
+            zero_row_if<D>(g + L::buf(b, 0), r, n_y);
+            if (KV) zero_row_if<D>(g + L::buf(b, 1), r, n_y);
+            const float *s_lse = reinterpret_cast<const float *>(g + L::kVec + b * 2 * kBT * 4);
+            const float *s_dl = s_lse + kBT;
 #pragma unroll 1
             for (int cb = 0; cb < kBT / 32; ++cb) {
-                float s[32], dp[32];
-                tmem_ld32(tS + tl + cb * 32, s);
+                float sv[32], dp[32];
+                tmem_ld32(tS + tl + cb * 32, sv);
                 tmem_ld32(tdP + tl + cb * 32, dp);
                 uint32_t pw[16], dw[16];
 #pragma unroll
@@ -321,23 +356,23 @@ __global__ void __launch_bounds__(160, 1)
                     float pv[2], dv[2];
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
-                        const int c = cb * 32 + e + h;  // query column
-                        const bool live = r < n_j && c < n_t;
-                        const float p = live ? ex2(fmaf(c1, s[e + h], -s_lse[c] * 1.4426950408889634f)) : 0.f;
+                        const int c = cb * 32 + e + h;  // column: query (KV) or key
+                        const bool live = r < n_x && c < n_y;
+                        const float lse2 = KV ? s_lse[c] * 1.4426950408889634f : lse2_r;
+                        const float dl = KV ? s_dl[c] : dl_r;
+                        const float p = live ? ex2(fmaf(c1, sv[e + h], -lse2)) : 0.f;
                         pv[h] = p;
-                        dv[h] = live ? p * (dp[e + h] - s_dl[c]) : 0.f;
+                        dv[h] = live ? p * (dp[e + h] - dl) : 0.f;
                     }
                     pw[e >> 1] = pack_bf16x2(pv[0], pv[1]);
                     dw[e >> 1] = pack_bf16x2(dv[0], dv[1]);
                 }
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {  // four 16-byte granules of 8 columns
-                    const uint32_t o = sw128(r, cb * 32 + q * 8);
-                    *reinterpret_cast<uint4 *>(g + L::kP + o) = make_uint4(pw[4 * q], pw[4 * q + 1], pw[4 * q + 2], pw[4 * q + 3]);
-                    *reinterpret_cast<uint4 *>(g + L::kS + o) = make_uint4(dw[4 * q], dw[4 * q + 1], dw[4 * q + 2], dw[4 * q + 3]);
-                }
+                // bf16 pairs back over columns that were already read
+                if (KV) tmem_st16(tS + tl + cb * 16, pw);
+                tmem_st16((KV ? tdP : tS) + tl + cb * 16, dw);
             }
             fence_proxy_async_smem();
+            tmem_wait_st();
             tc_fence_before();
             mbar_arrive(BAR(kBarEw));
         }
@@ -345,185 +380,24 @@ __global__ void __launch_bounds__(160, 1)
         if (ok && n > 0 && !wait_warp(BAR(kBarPair), (n - 1) & 1u, abort_flag, A.status)) ok = false;
         if (ok) {
             tc_fence_after();
-            const int64_t orow = bh * A.Sp + (int64_t)j * kBT + r;
-            uint4 *dk = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(A.dk) + orow * D);
-            uint4 *dv = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(A.dv) + orow * D);
-            const bool live = n > 0 && r < n_j;
+            const bool live = n > 0 && r < n_x;
 #pragma unroll 1
-            for (int cb = 0; cb < D / 32; ++cb) {
-                float a[32] = {}, b[32] = {};
-                if (n > 0) {
-                    tmem_ld32(tdK + tl + cb * 32, a);
-                    tmem_ld32(tdV + tl + cb * 32, b);
-                }
-                uint32_t wk[16], wv[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    wk[e] = live ? pack_bf16x2(a[2 * e] * A.scale, a[2 * e + 1] * A.scale) : 0u;
-                    wv[e] = live ? pack_bf16x2(b[2 * e], b[2 * e + 1]) : 0u;
-                }
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    dk[cb * 4 + q] = make_uint4(wk[4 * q], wk[4 * q + 1], wk[4 * q + 2], wk[4 * q + 3]);
-                    dv[cb * 4 + q] = make_uint4(wv[4 * q], wv[4 * q + 1], wv[4 * q + 2], wv[4 * q + 3]);
-                }
-            }
-        }
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (warp == kCtlWarp) tmem_dealloc(tmem, 512);
-}
-
-// ---------------------------------------------------------------- dQ
-template <int D>
-__global__ void __launch_bounds__(160, 1)
-    dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-              const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do, const BwdArgs A) {
-    using C = BwdCfg<D>;
-    using L = BwdSmem<D>;
-    extern __shared__ __align__(1024) uint8_t smem_raw[];
-    const uint32_t raw = smem_u32(smem_raw);
-    const uint32_t base = (raw + 1023u) & ~1023u;
-    uint8_t *g = smem_raw + (base - raw);
-    const uint32_t bars = base + L::kBars;
-    auto BAR = [&](int i) -> uint32_t { return bars + 8u * (uint32_t)i; };
-    volatile int *abort_flag = reinterpret_cast<int *>(g + L::kFlag);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-    const int64_t bht = blockIdx.x;
-    const int NT = A.NT;
-    const int t = (int)(bht % NT);
-    const int64_t bh = bht / NT;
-    const int n_t = __ldg(A.block_sizes + t);
-    int n = __ldg(A.q2k_num + bht);
-    n = n < 0 ? 0 : (n > A.max_kv ? A.max_kv : n);
-    const int32_t *sel = A.q2k_idx + bht * A.max_kv;
-
-    if (threadIdx.x == 0) {
-        mbar_init(BAR(kBarLd0), 1);
-        mbar_init(BAR(kBarLd1), 1);
-        mbar_init(BAR(kBarS), 1);
-        mbar_init(BAR(kBarEw), kEwThreads);
-        mbar_init(BAR(kBarPair), 1);
-        mbar_init(BAR(kBarDrain), 1);
-        *abort_flag = 0;
-        fence_mbar_init();
-    }
-    if (warp == kCtlWarp) {
-        tmem_alloc(base + L::kSlot, 512);
-        tmem_relinquish();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(g + L::kSlot);
-    const uint32_t tS = tmem, tdP = tmem + kBT, tdQ = tmem + 2 * kBT;
-
-    if (warp == kCtlWarp) {
-        if (lane == 0) {
-            const int32_t qrow = (int32_t)(bh * A.Sp + (int64_t)t * kBT);
-            bool ok = true;
-            int ld1 = 0, ld1_seen = 0;
-            if (n > 0) {
-                mbar_arrive_expect_tx(BAR(kBarLd0), 2 * C::kTile);
-                for (int c = 0; c < D / 64; ++c) {
-                    tma_load_2d(base + L::kA + c * kChunkBytes, &tm_q, c * 64, qrow, BAR(kBarLd0), l2_policy_evict_first());
-                    tma_load_2d(base + L::kB + c * kChunkBytes, &tm_do, c * 64, qrow, BAR(kBarLd0), l2_policy_evict_first());
-                }
-            }
-            for (int i = 0; i < n && ok; ++i) {
-                int jj = __ldg(sel + i);
-                jj = (jj < 0 || jj >= NT) ? 0 : jj;  // bad entries were flagged by k2q_kernel; read a valid tile
-                if (i > 0 && !(ok = wait_bar(BAR(kBarPair), (i - 1) & 1u, abort_flag, A.status))) break;
-                const int32_t krow = (int32_t)(bh * A.Sp + (int64_t)jj * kBT);
-                mbar_arrive_expect_tx(BAR(kBarLd1), 2 * C::kTile);
-                for (int c = 0; c < D / 64; ++c) {
-                    tma_load_2d(base + L::kC + c * kChunkBytes, &tm_k, c * 64, krow, BAR(kBarLd1), l2_policy_evict_last());
-                    tma_load_2d(base + L::kE + c * kChunkBytes, &tm_v, c * 64, krow, BAR(kBarLd1), l2_policy_evict_last());
-                }
-                ++ld1;
-                if (i == 0 && !(ok = wait_bar(BAR(kBarLd0), 0u, abort_flag, A.status))) break;
-                if (!(ok = wait_bar(BAR(kBarLd1), i & 1u, abort_flag, A.status))) break;
-                ++ld1_seen;
-                tc_fence_after();
-                mma_sq<D>(tS, base + L::kA, base + L::kC);   // S = Q_t K_j^T
-                mma_sq<D>(tdP, base + L::kB, base + L::kE);  // dP = dO_t V_j^T
-                mma_commit(BAR(kBarS));
-                if (!(ok = wait_bar(BAR(kBarEw), i & 1u, abort_flag, A.status))) break;
-                tc_fence_after();
-                mma_acc<D>(tdQ, base + L::kS, base + L::kC, i > 0);  // dQ += dS K_j
-                mma_commit(BAR(kBarPair));
-            }
-            if (!ok) {
-                if (n > 0) drain_wait(BAR(kBarLd0), 0u);
-                if (ld1 > ld1_seen) drain_wait(BAR(kBarLd1), (ld1 - 1) & 1u);
-            }
-            mma_commit(BAR(kBarDrain));
-            drain_wait(BAR(kBarDrain), 0u);
-        }
-        __syncwarp();
-    } else {
-        // ------------------------------------------------------------ elementwise
-        const int r = threadIdx.x;  // query row (TMEM lane)
-        const uint32_t tl = (uint32_t)(warp * 32) << 16;
-        const float c1 = A.scale * 1.4426950408889634f;
-        const int64_t orow = bh * A.Sp + (int64_t)t * kBT + r;
-        const float lse2 = __ldg(A.lse + orow) * 1.4426950408889634f;
-        const float dl = __ldg(A.delta + orow);
-        bool ok = true;
-        for (int i = 0; i < n; ++i) {
-            int jj = __ldg(sel + i);
-            const int n_j = (jj < 0 || jj >= NT) ? 0 : __ldg(A.block_sizes + jj);
-            if (!(ok = wait_warp(BAR(kBarS), i & 1u, abort_flag, A.status))) break;
-            // the pair's copies (K_j, V_j) are complete and visible here
-            if (!(ok = wait_warp(BAR(kBarLd1), i & 1u, abort_flag, A.status))) break;
-            tc_fence_after();
-            // K_j is summed over its rows next: clear the padding rows
-            zero_row_if<D>(g + L::kC, r, n_j);
+            for (int which = 0; which < (KV ? 2 : 1); ++which) {
+                // KV: which 0 = dV, 1 = dK; else dQ
+                void *dst_base = KV ? (which ? A.dk : A.dv) : A.dq;
+                const float mul = (KV && which == 0) ? 1.f : A.scale;
+                uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(dst_base) + xrow_r * D);
+                const uint32_t tacc = which ? tAcc1 : tAcc0;
 #pragma unroll 1
-            for (int cb = 0; cb < kBT / 32; ++cb) {
-                float s[32], dp[32];
-                tmem_ld32(tS + tl + cb * 32, s);
-                tmem_ld32(tdP + tl + cb * 32, dp);
-                uint32_t dw[16];
+                for (int cb = 0; cb < D / 32; ++cb) {
+                    float a[32] = {};
+                    if (n > 0) tmem_ld32(tacc + tl + cb * 32, a);
+                    uint32_t w[16];
 #pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    float dv[2];
+                    for (int e = 0; e < 16; ++e) w[e] = live ? pack_bf16x2(a[2 * e] * mul, a[2 * e + 1] * mul) : 0u;
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int c = cb * 32 + e + h;  // key column
-                        const bool live = r < n_t && c < n_j;
-                        const float p = live ? ex2(fmaf(c1, s[e + h], -lse2)) : 0.f;
-                        dv[h] = live ? p * (dp[e + h] - dl) : 0.f;
-                    }
-                    dw[e >> 1] = pack_bf16x2(dv[0], dv[1]);
+                    for (int q = 0; q < 4; ++q) dst[cb * 4 + q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
                 }
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const uint32_t o = sw128(r, cb * 32 + q * 8);
-                    *reinterpret_cast<uint4 *>(g + L::kS + o) = make_uint4(dw[4 * q], dw[4 * q + 1], dw[4 * q + 2], dw[4 * q + 3]);
-                }
-            }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            mbar_arrive(BAR(kBarEw));
-        }
-        if (ok && n > 0 && !wait_warp(BAR(kBarPair), (n - 1) & 1u, abort_flag, A.status)) ok = false;
-        if (ok) {
-            tc_fence_after();
-            uint4 *dq = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(A.dq) + orow * D);
-            const bool live = n > 0 && r < n_t;
-#pragma unroll 1
-            for (int cb = 0; cb < D / 32; ++cb) {
-                float a[32] = {};
-                if (n > 0) tmem_ld32(tdQ + tl + cb * 32, a);
-                uint32_t w[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) w[e] = live ? pack_bf16x2(a[2 * e] * A.scale, a[2 * e + 1] * A.scale) : 0u;
-#pragma unroll
-                for (int q = 0; q < 4; ++q) dq[cb * 4 + q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
             }
         }
     }
@@ -537,15 +411,18 @@ __global__ void __launch_bounds__(160, 1)
 
 size_t bwd_smem_bytes(int D) { return D == 128 ? BwdSmem<128>::kTotal : BwdSmem<64>::kTotal; }
 
+template <int D, bool KV>
+static cudaError_t bwd_attr() {
+    return cudaFuncSetAttribute(bwd_kernel<D, KV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)BwdSmem<D>::kTotal);
+}
+
 cudaError_t bwd_prepare() {
     cudaError_t e;
-    if ((e = cudaFuncSetAttribute(dkdv_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)BwdSmem<64>::kTotal)))
-        return e;
-    if ((e = cudaFuncSetAttribute(dkdv_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)BwdSmem<128>::kTotal)))
-        return e;
-    if ((e = cudaFuncSetAttribute(dq_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)BwdSmem<64>::kTotal)))
-        return e;
-    return cudaFuncSetAttribute(dq_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)BwdSmem<128>::kTotal);
+    if ((e = bwd_attr<64, true>()) != cudaSuccess) return e;
+    if ((e = bwd_attr<64, false>()) != cudaSuccess) return e;
+    if ((e = bwd_attr<128, true>()) != cudaSuccess) return e;
+    return bwd_attr<128, false>();
 }
 
 cudaError_t launch_bwd(const BwdLaunch &L, cudaStream_t stream) {
@@ -576,13 +453,13 @@ cudaError_t launch_bwd(const BwdLaunch &L, cudaStream_t stream) {
     A.scale = L.scale;
     const unsigned grid = (unsigned)((int64_t)L.BH * L.NT);
     if (L.D == 128) {
-        dkdv_kernel<128><<<grid, 160, BwdSmem<128>::kTotal, stream>>>(*L.tm_q, *L.tm_k, *L.tm_v, *L.tm_do, A);
+        bwd_kernel<128, true><<<grid, 160, BwdSmem<128>::kTotal, stream>>>(*L.tm_q, *L.tm_k, *L.tm_v, *L.tm_do, A);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        dq_kernel<128><<<grid, 160, BwdSmem<128>::kTotal, stream>>>(*L.tm_q, *L.tm_k, *L.tm_v, *L.tm_do, A);
+        bwd_kernel<128, false><<<grid, 160, BwdSmem<128>::kTotal, stream>>>(*L.tm_q, *L.tm_k, *L.tm_v, *L.tm_do, A);
     } else {
-        dkdv_kernel<64><<<grid, 160, BwdSmem<64>::kTotal, stream>>>(*L.tm_q, *L.tm_k, *L.tm_v, *L.tm_do, A);
+        bwd_kernel<64, true><<<grid, 160, BwdSmem<64>::kTotal, stream>>>(*L.tm_q, *L.tm_k, *L.tm_v, *L.tm_do, A);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        dq_kernel<64><<<grid, 160, BwdSmem<64>::kTotal, stream>>>(*L.tm_q, *L.tm_k, *L.tm_v, *L.tm_do, A);
+        bwd_kernel<64, false><<<grid, 160, BwdSmem<64>::kTotal, stream>>>(*L.tm_q, *L.tm_k, *L.tm_v, *L.tm_do, A);
     }
     return cudaGetLastError();
 }
