@@ -346,6 +346,40 @@ def run_ours(args, cfg):
     if vsa.vsa_check_device_status() != 0:
         raise RuntimeError("device status error in the timed region")
 
+    # ---------------------------------------------------------------- backward (optional)
+    bwd_line = None
+    if args.bwd:
+        dout = torch.randn((B, H, Sp, D), generator=torch.Generator().manual_seed(W.SEED_BASE + 200)).to(
+            torch.bfloat16).to(dev)
+        grads = [torch.empty_like(out) for _ in range(3)]
+        bdims = vsa.make_dims(B, H, NT, T, D, idx.shape[-1], w.scale)
+        bws = torch.empty(vsa.vsa_block_sparse_bwd_workspace_size(bdims), dtype=torch.uint8, device=dev)
+
+        def bwd_step():
+            vsa.vsa_block_sparse_bwd(tiles[0], tiles[1], tiles[2], out, dout, lse, idx, num, bs, grads[0],
+                                     grads[1], grads[2], bdims, bws, stream)
+
+        step(q_tok, k_tok, v_tok)
+        for _ in range(max(args.warmup, 3)):
+            bwd_step()
+        barrier()
+        b_marks = []
+        for _ in range(max(3, args.steps // 5)):
+            flush.zero_()
+            b0, b1 = ev(), ev()
+            b0.record(stream)
+            bwd_step()
+            b1.record(stream)
+            b_marks.append((b0, b1))
+        barrier()
+        if vsa.vsa_check_device_status() != 0:
+            raise RuntimeError("device status error in the backward")
+        b_ms = sum(a.elapsed_time(b) for a, b in b_marks) / len(b_marks)
+        b_flops = 2.5 * eff  # dV, dP, dS-weighted dQ and dK, plus S: 5 products of the forward's 2
+        bwd_line = {"ms": b_ms, "effective_flops": b_flops, "achieved": b_flops / (b_ms / 1e3) / 1e12,
+                    "unit": "TFLOP/s", "frac": b_flops / (b_ms / 1e3) / 1e12 / _peaks()[0],
+                    "launches": len(b_marks), "kernels": "delta, k2q transpose, dK/dV, dQ (tcgen05)"}
+
     # ---------------------------------------------------------------- end to end from host buffers
     hq, hk, hv = (x.pin_memory() for x in (w.q_tok, w.k_tok, w.v_tok))
     hidx, hnum, hbs, hr2t = (x.pin_memory() for x in (w.q2k_idx, w.q2k_num, w.block_sizes, w.row_to_token))
@@ -431,6 +465,8 @@ def run_ours(args, cfg):
                 "bound": "hbm", "achieved": ut_bytes / (ut_avg / 1e3) / 1e9, "peak": hbm, "unit": "GB/s",
                 "frac": ut_bytes / (ut_avg / 1e3) / 1e9 / hbm, "bytes": ut_bytes, "kernel": "untile_kernel (gated)"}
             line["config"]["step"] += " + un-tiling with gate"
+        if bwd_line is not None:
+            line["bwd"] = bwd_line
         if not args.no_cpu_baseline and world == 1:
             line["cpu_baseline"] = cpu_oracle_run(w, args.cpu_seconds)
         print(json.dumps(line), flush=True)
@@ -449,6 +485,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tile", type=int, default=None, choices=[128, 256],
                     help="dense-limit workload only: tile size (default 128)")
+    ap.add_argument("--bwd", action="store_true",
+                    help="also time the backward pass (reported under \"bwd\", outside the step)")
     ap.add_argument("--untile", action="store_true",
                     help="end the step with the un-tiling of the output times a gate")
     ap.add_argument("--select", action="store_true",
