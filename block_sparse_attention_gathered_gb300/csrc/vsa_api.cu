@@ -387,16 +387,17 @@ vsa_status vsa_tile_layout(const void *q_tok, const void *k_tok, const void *v_t
 
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-// Workspace of the backward: [header | delta | k2q offsets | k2q lists].
+// Workspace of the backward: [header | -delta | -lse*log2(e) | k2q offsets | k2q lists].
 struct BwdWs {
-    size_t delta, offs, list, total;
+    size_t delta, lse2, offs, list, total;
 };
 
 static BwdWs bwd_ws(const vsa_dims *d) {
     const size_t BH = (size_t)d->B * d->H, NT = (size_t)d->num_tiles, Sp = NT * d->tile;
     BwdWs w;
     w.delta = kWsHeader;
-    w.offs = w.delta + align256(4 * BH * Sp);
+    w.lse2 = w.delta + align256(4 * BH * Sp);
+    w.offs = w.lse2 + align256(4 * BH * Sp);
     w.list = w.offs + align256(4 * BH * (NT + 1));
     w.total = w.list + align256(4 * BH * NT * (size_t)(d->max_kv > 0 ? d->max_kv : 1));
     return w;
@@ -452,7 +453,8 @@ vsa_status vsa_block_sparse_bwd(const void *q, const void *k, const void *v, con
     L.out = out;
     L.dout = dout;
     L.lse = lse;
-    L.delta = reinterpret_cast<float *>(ws + w.delta);
+    L.ndelta = reinterpret_cast<float *>(ws + w.delta);
+    L.nlse2 = reinterpret_cast<float *>(ws + w.lse2);
     L.q2k_idx = q2k_idx;
     L.q2k_num = q2k_num;
     L.block_sizes = block_sizes;

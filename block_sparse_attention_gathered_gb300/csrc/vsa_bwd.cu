@@ -10,7 +10,9 @@
 //   dv_e = sum_i p_ie dout_i.
 //
 // Kernels (128-token tiles):
-//   delta_kernel   delta = rowsum(dout * out) in fp32, one pass over both.
+//   delta_kernel   per row -delta = -rowsum(dout * out) in fp32 (one pass over
+//                  both) and -lse in log2 units, the two per-row terms the
+//                  elementwise step adds.
 //   k2q_kernel     per (batch, head) the transposed selection: for every key
 //                  tile, the query tiles that select it, in ascending order
 //                  (one CTA per (batch, head), deterministic).
@@ -18,10 +20,12 @@
 //                  stay in shared memory; the query tiles t that select j
 //                  stream through two buffers (the next pair's copies overlap
 //                  this pair's work).  S^T = K_j Q_t^T and dP^T = V_j dO_t^T
-//                  go to TMEM; four elementwise warps (one thread per key row)
-//                  write P^T and dS^T as bf16 back into TMEM over the columns
-//                  they read; dV += P^T dO_t and dK += dS^T Q_t accumulate in
-//                  TMEM with the A operand taken from TMEM.
+//                  go to TMEM; eight elementwise warps (two threads per key
+//                  row) write P^T and dS^T as bf16 back into TMEM over the
+//                  columns they read, one 64-column half after the other;
+//                  dV += P^T dO_t and dK += dS^T Q_t accumulate in TMEM with
+//                  the A operand taken from TMEM, the first half's MMAs
+//                  running while the second half is computed.
 //   bwd_kernel<D, false>  one CTA per (batch, head, query tile t): Q_t and dO_t
 //                  stay; for every selected key tile, S and dP again, dS back
 //                  into TMEM, dQ += dS K_j.  Recomputing S and dP keeps dQ
@@ -43,8 +47,9 @@ namespace {
 using namespace ptx;
 
 constexpr int kBT = 128;            // tile rows (queries or keys)
-constexpr int kEwThreads = 128;     // elementwise warps 0..3, one thread per row
-constexpr int kCtlWarp = 4;         // TMA + MMA issue (lane 0)
+constexpr int kEwThreads = 256;     // elementwise warps 0..7: two threads per row
+constexpr int kCtlWarp = 8;         // TMA + MMA issue (lane 0)
+constexpr int kThreads = kEwThreads + 32;
 constexpr uint32_t kChunkBytes = kBT * 128;  // one 64-column (128-byte) chunk of a 128-row tile
 
 template <int D>
@@ -79,7 +84,8 @@ __device__ __forceinline__ void mma_sq(uint32_t tdst, uint32_t a_saddr, uint32_t
 
 // ---------------------------------------------------------------- delta
 __global__ void __launch_bounds__(256) delta_kernel(const uint4 *__restrict__ out, const uint4 *__restrict__ dout,
-                                                   float *__restrict__ delta, int64_t rows, int Dv) {
+                                                   const float *__restrict__ lse, float *__restrict__ ndelta,
+                                                   float *__restrict__ nlse2, int64_t rows, int Dv) {
     // one 8-lane group per row (Dv <= 16 vectors of 8 bf16)
     const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t row = gid >> 3;
@@ -98,7 +104,10 @@ __global__ void __launch_bounds__(256) delta_kernel(const uint4 *__restrict__ ou
     }
 #pragma unroll
     for (int o = 4; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    if (row < rows && sub == 0) delta[row] = acc;
+    if (row < rows && sub == 0) {
+        ndelta[row] = -acc;
+        nlse2[row] = -__ldg(lse + row) * 1.4426950408889634f;
+    }
 }
 
 // ---------------------------------------------------------------- k2q
@@ -169,8 +178,8 @@ struct BwdSmem {
 };
 
 struct BwdArgs {
-    const float *lse;           // [B*H*Sp] natural log
-    const float *delta;         // [B*H*Sp]
+    const float *nlse2;         // [B*H*Sp] -lse * log2(e)
+    const float *ndelta;        // [B*H*Sp] -rowsum(dout * out)
     const int32_t *q2k_idx, *q2k_num, *block_sizes;
     const int32_t *k2q_offs, *k2q_list;
     void *dq, *dk, *dv;         // bf16 [B*H*Sp, D]
@@ -181,26 +190,39 @@ struct BwdArgs {
 };
 
 // mbarriers: resident tiles loaded, per-buffer tiles loaded (two), S and dP in
-// TMEM, P/dS written back to TMEM, the pair's accumulations done, the
-// issuer's final drain
-enum { kBarRes = 0, kBarBuf0 = 1, kBarBuf1 = 2, kBarS = 3, kBarEw = 4, kBarPair = 5, kBarDrain = 6 };
+// TMEM, P/dS of the first and of the second 64 columns written back to TMEM,
+// the pair's accumulations done, the issuer's final drain
+enum { kBarRes = 0, kBarBuf0 = 1, kBarBuf1 = 2, kBarS = 3, kBarEw0 = 4, kBarEw1 = 5, kBarPair = 6, kBarDrain = 7 };
+constexpr int kNumBars = 8;
 
-// Issues the 8 MMAs of acc(128 x D) += A(128 x 128, bf16 pairs in TMEM) x
-// tile(128 x D, MN-major in shared memory: the tile's rows are summed).
+// Where the bf16 pairs of S/dP columns [16kk, 16kk + 16) sit in TMEM: the
+// thread that read the 32 columns [32m, 32m + 32) writes their 16 packed
+// columns back over the first 16 of them, so no thread overwrites columns
+// another thread may still be reading.
+__device__ __forceinline__ uint32_t packed_col(int kk) { return 32u * (uint32_t)(kk >> 1) + 8u * (uint32_t)(kk & 1); }
+
+// Issues the 4 MMAs of one half (64 of the 128 summed rows) of
+// acc(128 x D) += A(128 x 128, bf16 pairs in TMEM) x tile(128 x D, MN-major in
+// shared memory: the tile's rows are summed).
 template <int D>
-__device__ __forceinline__ void mma_acc_ts(uint32_t tacc, uint32_t ta, uint32_t tile_saddr, bool accumulate) {
+__device__ __forceinline__ void mma_acc_half(uint32_t tacc, uint32_t ta, uint32_t tile_saddr, int half,
+                                             bool accumulate) {
     const uint64_t b = sdesc_sw128(tile_saddr, kChunkBytes, 1024);
 #pragma unroll
-    for (int kk = 0; kk < kBT / 16; ++kk)
-        mma_ts(tacc, ta + kk * 8, b + kk * (2048 >> 4), BwdCfg<D>::kIdescAcc, (accumulate || kk > 0) ? 1u : 0u);
+    for (int q = 0; q < kBT / 32; ++q) {
+        const int kk = half * (kBT / 32) + q;
+        mma_ts(tacc, ta + packed_col(kk), b + kk * (2048 >> 4), BwdCfg<D>::kIdescAcc,
+               (accumulate || kk > 0) ? 1u : 0u);
+    }
 }
 
 // Common shape of both kernels: one resident tile pair, a list of partner
 // tiles streamed through two buffers, per pair two 128 x 128 products into
-// TMEM (S-like and dP-like), an elementwise step by 128 threads that writes
-// bf16 operands back into TMEM, and one or two accumulations from TMEM.
+// TMEM (S-like and dP-like), an elementwise step by 256 threads that writes
+// bf16 operands back into TMEM in two column halves, and one or two
+// accumulations from TMEM, each issued half by half as the halves are ready.
 template <int D, bool KV>
-__global__ void __launch_bounds__(160, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                const BwdArgs A) {
@@ -239,7 +261,7 @@ __global__ void __launch_bounds__(160, 1)
     };
 
     if (threadIdx.x == 0) {
-        for (int b = 0; b < 7; ++b) mbar_init(BAR(b), b == kBarEw ? kEwThreads : 1);
+        for (int b = 0; b < kNumBars; ++b) mbar_init(BAR(b), (b == kBarEw0 || b == kBarEw1) ? kEwThreads : 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -273,8 +295,8 @@ __global__ void __launch_bounds__(160, 1)
                                 c * 64, (int32_t)yrow, bar, l2_policy_evict_last());
                 }
                 if (KV) {
-                    bulk_load(base + L::kVec + b * 2 * kBT * 4, A.lse + yrow, kBT * 4, bar);
-                    bulk_load(base + L::kVec + b * 2 * kBT * 4 + kBT * 4, A.delta + yrow, kBT * 4, bar);
+                    bulk_load(base + L::kVec + b * 2 * kBT * 4, A.nlse2 + yrow, kBT * 4, bar);
+                    bulk_load(base + L::kVec + b * 2 * kBT * 4 + kBT * 4, A.ndelta + yrow, kBT * 4, bar);
                 }
                 ++issued[b];
             };
@@ -301,14 +323,18 @@ __global__ void __launch_bounds__(160, 1)
                 mma_sq<D>(tS, base + L::kRes0, base + L::buf(b, 0));
                 mma_sq<D>(tdP, base + L::kRes1, base + L::buf(b, 1));
                 mma_commit(BAR(kBarS));
-                if (!(ok = wait_bar(BAR(kBarEw), i & 1u, abort_flag, A.status))) break;
-                tc_fence_after();
-                if (KV) {
-                    mma_acc_ts<D>(tAcc0, tS, base + L::buf(b, 1), i > 0);   // dV += P^T dO_t
-                    mma_acc_ts<D>(tAcc1, tdP, base + L::buf(b, 0), i > 0);  // dK += dS^T Q_t
-                } else {
-                    mma_acc_ts<D>(tAcc0, tS, base + L::buf(b, 0), i > 0);   // dQ += dS K_j
+                // each half of the accumulations starts as soon as its 64 columns are written
+                for (int hv = 0; hv < 2 && ok; ++hv) {
+                    if (!(ok = wait_bar(BAR(kBarEw0 + hv), i & 1u, abort_flag, A.status))) break;
+                    tc_fence_after();
+                    if (KV) {
+                        mma_acc_half<D>(tAcc0, tS, base + L::buf(b, 1), hv, i > 0);   // dV += P^T dO_t
+                        mma_acc_half<D>(tAcc1, tdP, base + L::buf(b, 0), hv, i > 0);  // dK += dS^T Q_t
+                    } else {
+                        mma_acc_half<D>(tAcc0, tS, base + L::buf(b, 0), hv, i > 0);   // dQ += dS K_j
+                    }
                 }
+                if (!ok) break;
                 mma_commit(BAR(kBarPair));
             }
             if (!ok) {
@@ -324,13 +350,16 @@ __global__ void __launch_bounds__(160, 1)
         __syncwarp();
     } else {
         // ------------------------------------------------------------ elementwise
-        // thread r owns TMEM lane r: a key row (KV) or a query row
-        const int r = threadIdx.x;
-        const uint32_t tl = (uint32_t)(warp * 32) << 16;
+        // threads r and r + 128 share TMEM lane r (a key row (KV) or a query
+        // row); within each 64-column half, thread r takes the first 32
+        // columns and thread r + 128 the second
+        const int r = threadIdx.x & (kBT - 1);
+        const int h = threadIdx.x / kBT;
+        const uint32_t tl = (uint32_t)((warp & 3) * 32) << 16;
         const float c1 = A.scale * 1.4426950408889634f;
         const int64_t xrow_r = bh * A.Sp + (int64_t)x * kBT + r;
-        const float lse2_r = KV ? 0.f : __ldg(A.lse + xrow_r) * 1.4426950408889634f;
-        const float dl_r = KV ? 0.f : __ldg(A.delta + xrow_r);
+        const float nl2_r = KV ? 0.f : __ldg(A.nlse2 + xrow_r);
+        const float ndl_r = KV ? 0.f : __ldg(A.ndelta + xrow_r);
         bool ok = true;
         for (int i = 0; i < n; ++i) {
             const int b = i & 1, y = partner(i);
@@ -339,57 +368,68 @@ __global__ void __launch_bounds__(160, 1)
             // the pair's copies are complete and visible here
             if (!(ok = wait_warp(BAR(kBarBuf0 + b), (i >> 1) & 1u, abort_flag, A.status))) break;
             tc_fence_after();
-            // operands summed over their rows next get their padding rows cleared:
-            // Q_t and dO_t (KV), K_j (dQ)
-            zero_row_if<D>(g + L::buf(b, 0), r, n_y);
-            if (KV) zero_row_if<D>(g + L::buf(b, 1), r, n_y);
-            const float *s_lse = reinterpret_cast<const float *>(g + L::kVec + b * 2 * kBT * 4);
-            const float *s_dl = s_lse + kBT;
+            // operands summed over their rows next get their padding rows cleared
+            // (before the first half's arrival): Q_t and dO_t (KV), K_j (dQ)
+            if (h == 0) zero_row_if<D>(g + L::buf(b, 0), r, n_y);
+            if (KV && h == 1) zero_row_if<D>(g + L::buf(b, 1), r, n_y);
+            const float2 *s_nl2 = reinterpret_cast<const float2 *>(g + L::kVec + b * 2 * kBT * 4);
+            const float2 *s_ndl = s_nl2 + kBT / 2;
 #pragma unroll 1
-            for (int cb = 0; cb < kBT / 32; ++cb) {
+            for (int hv = 0; hv < 2; ++hv) {
+                const int c0 = hv * 64 + h * 32;  // this thread's 32 columns of the half
                 float sv[32], dp[32];
-                tmem_ld32(tS + tl + cb * 32, sv);
-                tmem_ld32(tdP + tl + cb * 32, dp);
+                tmem_ld32(tS + tl + c0, sv);
+                tmem_ld32(tdP + tl + c0, dp);
                 uint32_t pw[16], dw[16];
 #pragma unroll
                 for (int e = 0; e < 32; e += 2) {
-                    float pv[2], dv[2];
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int c = cb * 32 + e + h;  // column: query (KV) or key
-                        const bool live = r < n_x && c < n_y;
-                        const float lse2 = KV ? s_lse[c] * 1.4426950408889634f : lse2_r;
-                        const float dl = KV ? s_dl[c] : dl_r;
-                        const float p = live ? ex2(fmaf(c1, sv[e + h], -lse2)) : 0.f;
-                        pv[h] = p;
-                        dv[h] = live ? p * (dp[e + h] - dl) : 0.f;
+                    const int c = c0 + e;  // column pair c, c+1: queries (KV) or keys
+                    float2 nl2, ndl;
+                    if (KV) {
+                        nl2 = s_nl2[c >> 1];
+                        ndl = s_ndl[c >> 1];
+                    } else {
+                        nl2 = make_float2(nl2_r, nl2_r);
+                        ndl = make_float2(ndl_r, ndl_r);
                     }
-                    pw[e >> 1] = pack_bf16x2(pv[0], pv[1]);
-                    dw[e >> 1] = pack_bf16x2(dv[0], dv[1]);
+                    float x0, x1, t0, t1, d0, d1;
+                    fma2v(x0, x1, sv[e], sv[e + 1], c1, c1, nl2.x, nl2.y);  // scale*s*log2e - lse*log2e
+                    float p0 = ex2(x0), p1 = ex2(x1);
+                    fma2v(t0, t1, dp[e], dp[e + 1], 1.f, 1.f, ndl.x, ndl.y);  // dp - delta
+                    fma2v(d0, d1, p0, p1, t0, t1, 0.f, 0.f);                   // p * (dp - delta)
+                    // set, not multiplied: padding may hold non-finite values
+                    const bool l0 = r < n_x && c < n_y, l1 = r < n_x && c + 1 < n_y;
+                    p0 = l0 ? p0 : 0.f;
+                    p1 = l1 ? p1 : 0.f;
+                    d0 = l0 ? d0 : 0.f;
+                    d1 = l1 ? d1 : 0.f;
+                    pw[e >> 1] = pack_bf16x2(p0, p1);
+                    dw[e >> 1] = pack_bf16x2(d0, d1);
                 }
-                // bf16 pairs back over columns that were already read
-                if (KV) tmem_st16(tS + tl + cb * 16, pw);
-                tmem_st16((KV ? tdP : tS) + tl + cb * 16, dw);
+                // bf16 pairs back over the first 16 of the 32 columns just read
+                if (KV) tmem_st16(tS + tl + c0, pw);
+                tmem_st16((KV ? tdP : tS) + tl + c0, dw);
+                if (hv == 0) fence_proxy_async_smem();  // the zeroed rows, for the MMAs
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(BAR(kBarEw0 + hv));
             }
-            fence_proxy_async_smem();
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(BAR(kBarEw));
         }
         // ------------------------------------------------------------ epilogue
         if (ok && n > 0 && !wait_warp(BAR(kBarPair), (n - 1) & 1u, abort_flag, A.status)) ok = false;
         if (ok) {
             tc_fence_after();
             const bool live = n > 0 && r < n_x;
-#pragma unroll 1
-            for (int which = 0; which < (KV ? 2 : 1); ++which) {
-                // KV: which 0 = dV, 1 = dK; else dQ
+            {
+                // KV: thread half h writes dV (0) or dK (1); dQ: column half h
+                const int which = KV ? h : 0;
                 void *dst_base = KV ? (which ? A.dk : A.dv) : A.dq;
                 const float mul = (KV && which == 0) ? 1.f : A.scale;
                 uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(dst_base) + xrow_r * D);
                 const uint32_t tacc = which ? tAcc1 : tAcc0;
+                const int cb0 = KV ? 0 : h * (D / 64), cb1 = KV ? D / 32 : (h + 1) * (D / 64);
 #pragma unroll 1
-                for (int cb = 0; cb < D / 32; ++cb) {
+                for (int cb = cb0; cb < cb1; ++cb) {
                     float a[32] = {};
                     if (n > 0) tmem_ld32(tacc + tl + cb * 32, a);
                     uint32_t w[16];
@@ -429,15 +469,16 @@ cudaError_t launch_bwd(const BwdLaunch &L, cudaStream_t stream) {
     const int64_t rows = (int64_t)L.BH * L.Sp;
     const int Dv = L.D / 8;
     delta_kernel<<<(unsigned)((rows * 8 + 255) / 256), 256, 0, stream>>>(
-        reinterpret_cast<const uint4 *>(L.out), reinterpret_cast<const uint4 *>(L.dout), L.delta, rows, Dv);
+        reinterpret_cast<const uint4 *>(L.out), reinterpret_cast<const uint4 *>(L.dout), L.lse, L.ndelta, L.nlse2,
+        rows, Dv);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     k2q_kernel<<<(unsigned)L.BH, 1024, (size_t)(L.NT + 1) * 4, stream>>>(L.q2k_idx, L.q2k_num, L.NT, L.max_kv,
                                                                          L.k2q_offs, L.k2q_list, L.status);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     BwdArgs A;
-    A.lse = L.lse;
-    A.delta = L.delta;
+    A.nlse2 = L.nlse2;
+    A.ndelta = L.ndelta;
     A.q2k_idx = L.q2k_idx;
     A.q2k_num = L.q2k_num;
     A.block_sizes = L.block_sizes;
@@ -453,13 +494,13 @@ cudaError_t launch_bwd(const BwdLaunch &L, cudaStream_t stream) {
     A.scale = L.scale;
     const unsigned grid = (unsigned)((int64_t)L.BH * L.NT);
     if (L.D == 128) {
-        bwd_kernel<128, true><<<grid, 160, BwdSmem<128>::kTotal, stream>>>(*L.tm_q, *L.tm_k, *L.tm_v, *L.tm_do, A);
+        bwd_kernel<128, true><<<grid, kThreads, BwdSmem<128>::kTotal, stream>>>(*L.tm_q, *L.tm_k, *L.tm_v, *L.tm_do, A);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        bwd_kernel<128, false><<<grid, 160, BwdSmem<128>::kTotal, stream>>>(*L.tm_q, *L.tm_k, *L.tm_v, *L.tm_do, A);
+        bwd_kernel<128, false><<<grid, kThreads, BwdSmem<128>::kTotal, stream>>>(*L.tm_q, *L.tm_k, *L.tm_v, *L.tm_do, A);
     } else {
-        bwd_kernel<64, true><<<grid, 160, BwdSmem<64>::kTotal, stream>>>(*L.tm_q, *L.tm_k, *L.tm_v, *L.tm_do, A);
+        bwd_kernel<64, true><<<grid, kThreads, BwdSmem<64>::kTotal, stream>>>(*L.tm_q, *L.tm_k, *L.tm_v, *L.tm_do, A);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        bwd_kernel<64, false><<<grid, 160, BwdSmem<64>::kTotal, stream>>>(*L.tm_q, *L.tm_k, *L.tm_v, *L.tm_do, A);
+        bwd_kernel<64, false><<<grid, kThreads, BwdSmem<64>::kTotal, stream>>>(*L.tm_q, *L.tm_k, *L.tm_v, *L.tm_do, A);
     }
     return cudaGetLastError();
 }

@@ -83,7 +83,7 @@ struct BwdLaunch {
     const CUtensorMap *tm_q, *tm_k, *tm_v, *tm_do;  // rows of D bf16, box {64, 128}
     const void *out, *dout;                           // bf16 [B*H*Sp, D]
     const float *lse;                                 // [B*H*Sp]
-    float *delta;                                     // workspace [B*H*Sp]
+    float *ndelta, *nlse2;                            // workspace [B*H*Sp] each: -delta, -lse*log2(e)
     const int32_t *q2k_idx, *q2k_num, *block_sizes;
     int32_t *k2q_offs, *k2q_list;                     // workspace [B*H, NT+1], [B*H, NT*max_kv]
     void *dq, *dk, *dv;                               // bf16 [B*H*Sp, D]

@@ -402,6 +402,19 @@ __device__ __forceinline__ void fma2_scalar(float &x0, float &x1, float a0, floa
         : "f"(a0), "f"(a1), "f"(c), "f"(b));
 }
 
+// (x0, x1) = (a0 * b0 + c0, a1 * b1 + c1) as one packed f32x2 FMA.
+__device__ __forceinline__ void fma2v(float &x0, float &x1, float a0, float a1, float b0, float b1, float c0,
+                                      float c1) {
+    asm("{\n\t.reg .b64 av, bv, cv, dv;\n\t"
+        "mov.b64 av, {%2, %3};\n\t"
+        "mov.b64 bv, {%4, %5};\n\t"
+        "mov.b64 cv, {%6, %7};\n\t"
+        "fma.rn.f32x2 dv, av, bv, cv;\n\t"
+        "mov.b64 {%0, %1}, dv;\n\t}"
+        : "=f"(x0), "=f"(x1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+
 // l0 += lo(pk), l1 += hi(pk) where pk holds two bf16 values (exact widening).
 __device__ __forceinline__ void add_bf16x2_f32(float &l0, float &l1, uint32_t pk) {
     asm("{\n\t.reg .b16 lo, hi;\n\t"
