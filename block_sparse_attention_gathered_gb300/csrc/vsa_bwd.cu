@@ -47,8 +47,10 @@ namespace {
 using namespace ptx;
 
 constexpr int kBT = 128;            // tile rows (queries or keys)
-constexpr int kEwThreads = 256;     // elementwise warps 0..7: two threads per row
-constexpr int kCtlWarp = 8;         // TMA + MMA issue (lane 0)
+constexpr int kEwSplit = 2;                 // elementwise threads per row
+constexpr int kEwThreads = kEwSplit * kBT;  // elementwise warps first
+constexpr int kEwCols = 64 / kEwSplit;      // columns per thread in each 64-column half
+constexpr int kCtlWarp = kEwThreads / 32;   // TMA + MMA issue (lane 0)
 constexpr int kThreads = kEwThreads + 32;
 constexpr uint32_t kChunkBytes = kBT * 128;  // one 64-column (128-byte) chunk of a 128-row tile
 
@@ -196,10 +198,27 @@ enum { kBarRes = 0, kBarBuf0 = 1, kBarBuf1 = 2, kBarS = 3, kBarEw0 = 4, kBarEw1 
 constexpr int kNumBars = 8;
 
 // Where the bf16 pairs of S/dP columns [16kk, 16kk + 16) sit in TMEM: the
-// thread that read the 32 columns [32m, 32m + 32) writes their 16 packed
-// columns back over the first 16 of them, so no thread overwrites columns
+// thread that read the kEwCols columns [c0, c0 + kEwCols) writes their packed
+// columns back over the first half of them, so no thread overwrites columns
 // another thread may still be reading.
-__device__ __forceinline__ uint32_t packed_col(int kk) { return 32u * (uint32_t)(kk >> 1) + 8u * (uint32_t)(kk & 1); }
+__device__ __forceinline__ uint32_t packed_col(int kk) {
+    const int c0 = (16 * kk / kEwCols) * kEwCols;
+    return (uint32_t)(c0 + (16 * kk - c0) / 2);
+}
+
+// TMEM loads of 32 or 16 columns (waited for) and stores of 16 or 8.
+template <int N>
+__device__ __forceinline__ void ld_cols(uint32_t taddr, float (&r)[N]) {
+    static_assert(N == 32 || N == 16, "columns");
+    if constexpr (N == 32) tmem_ld32(taddr, r);
+    else tmem_ld16(taddr, r);
+}
+template <int N>
+__device__ __forceinline__ void st_cols(uint32_t taddr, const uint32_t (&v)[N]) {
+    static_assert(N == 16 || N == 8, "columns");
+    if constexpr (N == 16) tmem_st16(taddr, v);
+    else tmem_st8(taddr, v);
+}
 
 // Issues the 4 MMAs of one half (64 of the 128 summed rows) of
 // acc(128 x D) += A(128 x 128, bf16 pairs in TMEM) x tile(128 x D, MN-major in
@@ -314,7 +333,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int b = i & 1;
                 // the previous pair is done: its TMEM operands and its buffer are free
                 if (i > 0 && !(ok = wait_bar(BAR(kBarPair), (i - 1) & 1u, abort_flag, A.status))) break;
-                if (i + 1 < n) load_pair(i + 1);
                 if (i == 0 && !(ok = wait_bar(BAR(kBarRes), 0u, abort_flag, A.status))) break;
                 if (!(ok = wait_bar(BAR(kBarBuf0 + b), (i >> 1) & 1u, abort_flag, A.status))) break;
                 ++seen[b];
@@ -323,6 +341,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_sq<D>(tS, base + L::kRes0, base + L::buf(b, 0));
                 mma_sq<D>(tdP, base + L::kRes1, base + L::buf(b, 1));
                 mma_commit(BAR(kBarS));
+                // the next pair's copies go to the buffer the previous pair
+                // released, off the path from one pair's MMAs to the next
+                if (i + 1 < n) load_pair(i + 1);
                 // each half of the accumulations starts as soon as its 64 columns are written
                 for (int hv = 0; hv < 2 && ok; ++hv) {
                     if (!(ok = wait_bar(BAR(kBarEw0 + hv), i & 1u, abort_flag, A.status))) break;
@@ -350,9 +371,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else {
         // ------------------------------------------------------------ elementwise
-        // threads r and r + 128 share TMEM lane r (a key row (KV) or a query
-        // row); within each 64-column half, thread r takes the first 32
-        // columns and thread r + 128 the second
+        // threads r + 128h (h < kEwSplit) share TMEM lane r (a key row (KV) or
+        // a query row); within each 64-column half thread r + 128h takes
+        // columns [h kEwCols, (h + 1) kEwCols)
         const int r = threadIdx.x & (kBT - 1);
         const int h = threadIdx.x / kBT;
         const uint32_t tl = (uint32_t)((warp & 3) * 32) << 16;
@@ -376,13 +397,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float2 *s_ndl = s_nl2 + kBT / 2;
 #pragma unroll 1
             for (int hv = 0; hv < 2; ++hv) {
-                const int c0 = hv * 64 + h * 32;  // this thread's 32 columns of the half
-                float sv[32], dp[32];
-                tmem_ld32(tS + tl + c0, sv);
-                tmem_ld32(tdP + tl + c0, dp);
-                uint32_t pw[16], dw[16];
+                const int c0 = hv * 64 + h * kEwCols;  // this thread's columns of the half
+                float sv[kEwCols], dp[kEwCols];
+                ld_cols(tS + tl + c0, sv);
+                ld_cols(tdP + tl + c0, dp);
+                uint32_t pw[kEwCols / 2], dw[kEwCols / 2];
 #pragma unroll
-                for (int e = 0; e < 32; e += 2) {
+                for (int e = 0; e < kEwCols; e += 2) {
                     const int c = c0 + e;  // column pair c, c+1: queries (KV) or keys
                     float2 nl2, ndl;
                     if (KV) {
@@ -406,9 +427,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     pw[e >> 1] = pack_bf16x2(p0, p1);
                     dw[e >> 1] = pack_bf16x2(d0, d1);
                 }
-                // bf16 pairs back over the first 16 of the 32 columns just read
-                if (KV) tmem_st16(tS + tl + c0, pw);
-                tmem_st16((KV ? tdP : tS) + tl + c0, dw);
+                // bf16 pairs back over the first half of the columns just read
+                if (KV) st_cols(tS + tl + c0, pw);
+                st_cols((KV ? tdP : tS) + tl + c0, dw);
                 if (hv == 0) fence_proxy_async_smem();  // the zeroed rows, for the MMAs
                 tmem_wait_st();
                 tc_fence_before();
@@ -421,15 +442,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const bool live = n > 0 && r < n_x;
             {
-                // KV: thread half h writes dV (0) or dK (1); dQ: column half h
-                const int which = KV ? h : 0;
+                // KV: threads of even h write dV, odd h dK; dQ: every h a share of the columns
+                const int which = KV ? (h & 1) : 0;
                 void *dst_base = KV ? (which ? A.dk : A.dv) : A.dq;
                 const float mul = (KV && which == 0) ? 1.f : A.scale;
                 uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(dst_base) + xrow_r * D);
                 const uint32_t tacc = which ? tAcc1 : tAcc0;
-                const int cb0 = KV ? 0 : h * (D / 64), cb1 = KV ? D / 32 : (h + 1) * (D / 64);
+                const int cb0 = KV ? (h >> 1) : h, cstep = KV ? kEwSplit / 2 : kEwSplit;
 #pragma unroll 1
-                for (int cb = cb0; cb < cb1; ++cb) {
+                for (int cb = cb0; cb < D / 32; cb += cstep) {
                     float a[32] = {};
                     if (n > 0) tmem_ld32(tacc + tl + cb * 32, a);
                     uint32_t w[16];
