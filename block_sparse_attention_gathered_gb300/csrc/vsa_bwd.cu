@@ -31,10 +31,12 @@
 //                  into TMEM, dQ += dS K_j.  Recomputing S and dP keeps dQ
 //                  free of atomics and the result deterministic.
 // Padding rows are kept out of every product: P and dS are set (not
-// multiplied) to 0 outside the valid rows and columns, and padding rows of an
-// operand that is summed over (Q and dO in dk/dv, K in dq) are zeroed in shared
-// memory first, so NaN/Inf padding never meets a zero weight.  Every wait is
-// bounded; on expiry the CTA flags VSA_ERR_TIMEOUT and returns.
+// multiplied) to 0 in the columns past the partner tile's valid count, and
+// padding rows of an operand that is summed over (Q and dO in dk/dv, K in dq)
+// are zeroed in shared memory first, so NaN/Inf padding never meets a zero
+// weight.  Padding rows of the resident tile reach only their own rows of the
+// accumulators, which the epilogue writes as 0.  Every wait is bounded; on
+// expiry the CTA flags VSA_ERR_TIMEOUT and returns.
 #include <cuda_bf16.h>
 
 #include "vsa_internal.h"
@@ -220,6 +222,45 @@ __device__ __forceinline__ void st_cols(uint32_t taddr, const uint32_t (&v)[N]) 
     else tmem_st8(taddr, v);
 }
 
+// P and dS of kEwCols columns [c0, c0 + kEwCols) of one row, as bf16 pairs:
+//   p = 2^(scale log2(e) s - lse log2(e)),  ds = p (dp - delta),
+// with the per-column terms from shared memory (KV: columns are queries) or
+// this row's (dQ).  MASK sets p and ds (not multiplies them) to 0 in columns
+// past the partner tile's valid count n_y, whose S and dP may be non-finite.
+// Rows are not masked: a padding row's values reach only its own row of the
+// accumulators, which the epilogue writes as 0.
+template <bool KV, bool MASK>
+__device__ __forceinline__ void ew_cols(const float (&sv)[kEwCols], const float (&dp)[kEwCols],
+                                        uint32_t (&pw)[kEwCols / 2], uint32_t (&dw)[kEwCols / 2], int c0, int n_y,
+                                        float c1, const float2 *s_nl2, const float2 *s_ndl, float nl2_r,
+                                        float ndl_r) {
+#pragma unroll
+    for (int e = 0; e < kEwCols; e += 2) {
+        const int c = c0 + e;  // column pair c, c+1: queries (KV) or keys
+        float2 nl2, ndl;
+        if (KV) {
+            nl2 = s_nl2[c >> 1];
+            ndl = s_ndl[c >> 1];
+        } else {
+            nl2 = make_float2(nl2_r, nl2_r);
+            ndl = make_float2(ndl_r, ndl_r);
+        }
+        float x0, x1, t0, t1, d0, d1;
+        fma2v(x0, x1, sv[e], sv[e + 1], c1, c1, nl2.x, nl2.y);  // scale*s*log2e - lse*log2e
+        float p0 = ex2(x0), p1 = ex2(x1);
+        fma2v(t0, t1, dp[e], dp[e + 1], 1.f, 1.f, ndl.x, ndl.y);  // dp - delta
+        fma2v(d0, d1, p0, p1, t0, t1, 0.f, 0.f);                   // p * (dp - delta)
+        if (MASK) {
+            p0 = c < n_y ? p0 : 0.f;
+            d0 = c < n_y ? d0 : 0.f;
+            p1 = c + 1 < n_y ? p1 : 0.f;
+            d1 = c + 1 < n_y ? d1 : 0.f;
+        }
+        pw[e >> 1] = pack_bf16x2(p0, p1);
+        dw[e >> 1] = pack_bf16x2(d0, d1);
+    }
+}
+
 // Issues the 4 MMAs of one half (64 of the 128 summed rows) of
 // acc(128 x D) += A(128 x 128, bf16 pairs in TMEM) x tile(128 x D, MN-major in
 // shared memory: the tile's rows are summed).
@@ -402,35 +443,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ld_cols(tS + tl + c0, sv);
                 ld_cols(tdP + tl + c0, dp);
                 uint32_t pw[kEwCols / 2], dw[kEwCols / 2];
-#pragma unroll
-                for (int e = 0; e < kEwCols; e += 2) {
-                    const int c = c0 + e;  // column pair c, c+1: queries (KV) or keys
-                    float2 nl2, ndl;
-                    if (KV) {
-                        nl2 = s_nl2[c >> 1];
-                        ndl = s_ndl[c >> 1];
-                    } else {
-                        nl2 = make_float2(nl2_r, nl2_r);
-                        ndl = make_float2(ndl_r, ndl_r);
-                    }
-                    float x0, x1, t0, t1, d0, d1;
-                    fma2v(x0, x1, sv[e], sv[e + 1], c1, c1, nl2.x, nl2.y);  // scale*s*log2e - lse*log2e
-                    float p0 = ex2(x0), p1 = ex2(x1);
-                    fma2v(t0, t1, dp[e], dp[e + 1], 1.f, 1.f, ndl.x, ndl.y);  // dp - delta
-                    fma2v(d0, d1, p0, p1, t0, t1, 0.f, 0.f);                   // p * (dp - delta)
-                    // set, not multiplied: padding may hold non-finite values
-                    const bool l0 = r < n_x && c < n_y, l1 = r < n_x && c + 1 < n_y;
-                    p0 = l0 ? p0 : 0.f;
-                    p1 = l1 ? p1 : 0.f;
-                    d0 = l0 ? d0 : 0.f;
-                    d1 = l1 ? d1 : 0.f;
-                    pw[e >> 1] = pack_bf16x2(p0, p1);
-                    dw[e >> 1] = pack_bf16x2(d0, d1);
-                }
+                // warp-uniform: only a tail partner tile needs the column mask
+                if (n_y >= c0 + kEwCols) ew_cols<KV, false>(sv, dp, pw, dw, c0, n_y, c1, s_nl2, s_ndl, nl2_r, ndl_r);
+                else ew_cols<KV, true>(sv, dp, pw, dw, c0, n_y, c1, s_nl2, s_ndl, nl2_r, ndl_r);
                 // bf16 pairs back over the first half of the columns just read
                 if (KV) st_cols(tS + tl + c0, pw);
                 st_cols((KV ? tdP : tS) + tl + c0, dw);
-                if (hv == 0) fence_proxy_async_smem();  // the zeroed rows, for the MMAs
+                if (hv == 0 && r >= n_y) fence_proxy_async_smem();  // this thread's zeroed rows, for the MMAs
                 tmem_wait_st();
                 tc_fence_before();
                 mbar_arrive(BAR(kBarEw0 + hv));
