@@ -387,24 +387,31 @@ vsa_status vsa_tile_layout(const void *q_tok, const void *k_tok, const void *v_t
 
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-// Workspace of the backward: [header | -delta | -lse*log2(e) | k2q offsets | k2q lists].
+// Workspace of the backward, per (b, h) over NTk kernel tiles of 128 rows:
+// [header | -delta | -lse*log2(e) | partner counts | partner lists |
+//  transposed offsets | transposed lists].
 struct BwdWs {
-    size_t delta, lse2, offs, list, total;
+    BwdGeo geo;
+    size_t delta, lse2, pc, pl, offs, list, total;
 };
 
 static BwdWs bwd_ws(const vsa_dims *d) {
-    const size_t BH = (size_t)d->B * d->H, NT = (size_t)d->num_tiles, Sp = NT * d->tile;
     BwdWs w;
+    w.geo = bwd_geo(d->tile, d->num_tiles, d->max_kv);
+    const size_t BH = (size_t)d->B * d->H, NTk = (size_t)w.geo.NTk, Spk = NTk * 128;
+    const size_t lists = 4 * BH * NTk * (size_t)w.geo.maxlen;
     w.delta = kWsHeader;
-    w.lse2 = w.delta + align256(4 * BH * Sp);
-    w.offs = w.lse2 + align256(4 * BH * Sp);
-    w.list = w.offs + align256(4 * BH * (NT + 1));
-    w.total = w.list + align256(4 * BH * NT * (size_t)(d->max_kv > 0 ? d->max_kv : 1));
+    w.lse2 = w.delta + align256(4 * BH * Spk);
+    w.pc = w.lse2 + align256(4 * BH * Spk);
+    w.pl = w.pc + align256(4 * BH * NTk);
+    w.offs = w.pl + align256(lists);
+    w.list = w.offs + align256(4 * BH * (NTk + 1));
+    w.total = w.list + align256(lists);
     return w;
 }
 
 size_t vsa_block_sparse_bwd_workspace_size(const vsa_dims *dims) {
-    if (check_dims(dims) != VSA_OK || dims->tile != 128) return 0;
+    if (check_dims(dims) != VSA_OK) return 0;
     return bwd_ws(dims).total;
 }
 
@@ -414,7 +421,6 @@ vsa_status vsa_block_sparse_bwd(const void *q, const void *k, const void *v, con
                                 void *workspace, size_t workspace_bytes, vsa_stream_t stream) {
     vsa_status st = check_dims(dims);
     if (st != VSA_OK) return st;
-    if (dims->tile != 128) return VSA_ERR_ARG;
     if (!q || !k || !v || !out || !dout || !lse || !q2k_num || !block_sizes || !dq || !dk || !dv ||
         (!q2k_idx && dims->max_kv > 0))
         return VSA_ERR_ARG;
@@ -437,7 +443,7 @@ vsa_status vsa_block_sparse_bwd(const void *q, const void *k, const void *v, con
         dc.attn_prepared.fetch_or(kBwdBit, std::memory_order_acq_rel);
     }
     const int D = dims->head_dim, NT = dims->num_tiles;
-    const int64_t Sp = (int64_t)NT * 128;
+    const int64_t Sp = (int64_t)NT * dims->tile;
     const int64_t rows = (int64_t)dims->B * dims->H * Sp;
     CUtensorMap tm_q, tm_k, tm_v, tm_do;
     if ((st = encode_rows_map(&tm_q, q, rows, D, 128)) != VSA_OK) return st;
@@ -458,6 +464,8 @@ vsa_status vsa_block_sparse_bwd(const void *q, const void *k, const void *v, con
     L.q2k_idx = q2k_idx;
     L.q2k_num = q2k_num;
     L.block_sizes = block_sizes;
+    L.pc = reinterpret_cast<int32_t *>(ws + w.pc);
+    L.pl = reinterpret_cast<int32_t *>(ws + w.pl);
     L.k2q_offs = reinterpret_cast<int32_t *>(ws + w.offs);
     L.k2q_list = reinterpret_cast<int32_t *>(ws + w.list);
     L.dq = dq;
@@ -465,10 +473,14 @@ vsa_status vsa_block_sparse_bwd(const void *q, const void *k, const void *v, con
     L.dv = dv;
     L.status = dc.status_ptr.load(std::memory_order_acquire);
     L.BH = dims->B * dims->H;
-    L.NT = NT;
+    L.T = dims->tile;
+    L.NTc = NT;
+    L.NTk = w.geo.NTk;
     L.D = D;
     L.max_kv = dims->max_kv;
+    L.maxlen = w.geo.maxlen;
     L.Sp = Sp;
+    L.Spk = (int64_t)w.geo.NTk * 128;
     L.scale = dims->scale > 0.f ? dims->scale : 1.0f / std::sqrt((float)D);
     if (launch_bwd(L, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
         cudaGetLastError();
@@ -476,11 +488,11 @@ vsa_status vsa_block_sparse_bwd(const void *q, const void *k, const void *v, con
     }
     t_route = vsa_route{};
     t_route.kernel = VSA_KERNEL_BWD;
-    t_route.tile = 128;
+    t_route.tile = dims->tile;
     t_route.head_dim = D;
-    t_route.grid = (int32_t)((int64_t)L.BH * NT);
-    t_route.block = 160;
-    t_route.work_items = (int64_t)L.BH * NT;
+    t_route.grid = (int32_t)((int64_t)L.BH * L.NTk);
+    t_route.block = bwd_threads();
+    t_route.work_items = (int64_t)L.BH * L.NTk;
     t_route.smem_bytes = (int32_t)bwd_smem_bytes(D);
     return VSA_OK;
 }

@@ -9,13 +9,23 @@
 //   dq_i = scale * sum_e ds_ie k_e,  dk_e = scale * sum_i ds_ie q_i,
 //   dv_e = sum_i p_ie dout_i.
 //
-// Kernels (128-token tiles):
+// The kernels work on 128-row "kernel tiles" whatever the caller's tile T:
+// with T = 128 a kernel tile is a caller tile; with T = 256 it is one half of
+// one (tile_size clamps the valid count); with T = 64 it holds two caller
+// tiles, rows 0-63 and 64-127.  A pair of kernel tiles carries a 4-bit mask of
+// which (64-row sub-tile, 64-row sub-tile) blocks are selected, so 64-token
+// selections need no other change; with T >= 128 every mask is full.
+//
+// Kernels:
 //   delta_kernel   per row -delta = -rowsum(dout * out) in fp32 (one pass over
 //                  both) and -lse in log2 units, the two per-row terms the
-//                  elementwise step adds.
-//   k2q_kernel     per (batch, head) the transposed selection: for every key
-//                  tile, the query tiles that select it, in ascending order
-//                  (one CTA per (batch, head), deterministic).
+//                  elementwise step adds, stored with a row stride of whole
+//                  kernel tiles.
+//   pairs_kernel   per (batch, head, query kernel tile) the selected key kernel
+//                  tiles, ascending, each with its block mask (one warp each).
+//   k2q_kernel     per (batch, head) the transposed lists: for every key
+//                  kernel tile, the query kernel tiles that select it, in
+//                  ascending order (one CTA per (batch, head), deterministic).
 //   bwd_kernel<D, true>   one CTA per (batch, head, key tile j): K_j and V_j
 //                  stay in shared memory; the query tiles t that select j
 //                  stream through two buffers (the next pair's copies overlap
@@ -31,9 +41,9 @@
 //                  into TMEM, dQ += dS K_j.  Recomputing S and dP keeps dQ
 //                  free of atomics and the result deterministic.
 // Padding rows are kept out of every product: P and dS are set (not
-// multiplied) to 0 in the columns past the partner tile's valid count, and
-// padding rows of an operand that is summed over (Q and dO in dk/dv, K in dq)
-// are zeroed in shared memory first, so NaN/Inf padding never meets a zero
+// multiplied) to 0 in the partner's padding columns and in unselected blocks,
+// and padding rows of an operand that is summed over (Q and dO in dk/dv, K in
+// dq) are zeroed in shared memory first, so NaN/Inf padding never meets a zero
 // weight.  Padding rows of the resident tile reach only their own rows of the
 // accumulators, which the epilogue writes as 0.  Every wait is bounded; on
 // expiry the CTA flags VSA_ERR_TIMEOUT and returns.
@@ -63,11 +73,10 @@ struct BwdCfg {
     static constexpr uint32_t kIdescAcc = idesc_bf16(128, D, true);    // accumulations, B MN-major
 };
 
-// Zeroes rows [from, 128) of a tile of D columns (whole rows, so the swizzle
-// does not matter); thread `row` clears its own row.
+// Zeroes row `row` of a 128-row tile of D columns (a whole row, so the
+// swizzle does not matter).
 template <int D>
-__device__ __forceinline__ void zero_row_if(uint8_t *tile, int row, int from) {
-    if (row < from) return;
+__device__ __forceinline__ void zero_row(uint8_t *tile, int row) {
 #pragma unroll
     for (int c = 0; c < D / 64; ++c) {
         uint4 *p = reinterpret_cast<uint4 *>(tile + c * kChunkBytes + row * 128);
@@ -87,9 +96,11 @@ __device__ __forceinline__ void mma_sq(uint32_t tdst, uint32_t a_saddr, uint32_t
 }
 
 // ---------------------------------------------------------------- delta
+// Caller row (bh, s), s < Sp, goes to vector entry bh * Spk + s.
 __global__ void __launch_bounds__(256) delta_kernel(const uint4 *__restrict__ out, const uint4 *__restrict__ dout,
                                                    const float *__restrict__ lse, float *__restrict__ ndelta,
-                                                   float *__restrict__ nlse2, int64_t rows, int Dv) {
+                                                   float *__restrict__ nlse2, int64_t rows, int Dv, int64_t Sp,
+                                                   int64_t Spk) {
     // one 8-lane group per row (Dv <= 16 vectors of 8 bf16)
     const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t row = gid >> 3;
@@ -109,57 +120,148 @@ __global__ void __launch_bounds__(256) delta_kernel(const uint4 *__restrict__ ou
 #pragma unroll
     for (int o = 4; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
     if (row < rows && sub == 0) {
-        ndelta[row] = -acc;
-        nlse2[row] = -__ldg(lse + row) * 1.4426950408889634f;
+        const int64_t o = (row / Sp) * Spk + row % Sp;
+        ndelta[o] = -acc;
+        nlse2[o] = -__ldg(lse + row) * 1.4426950408889634f;
     }
 }
 
-// ---------------------------------------------------------------- k2q
-// offs [B*H, NT+1] and list [B*H, NT*max_kv]: list[bh][offs[bh][j] ...] are the
-// query tiles selecting key tile j, ascending.  Entries out of range are
-// skipped and flagged.
+// Kernel-tile geometry of a caller tiling: T caller tile rows, NTc caller tiles.
+struct Geo {
+    int32_t T, NTc, NTk;
+};
+
+// Valid rows of kernel tile z in its two 64-row halves: row r is valid iff
+// r < 64 ? r < lo : r - 64 < hi.
+struct Rows {
+    int lo, hi;
+    __device__ __forceinline__ bool valid(int r) const { return r < 64 ? r < lo : r - 64 < hi; }
+};
+
+__device__ __forceinline__ Rows ktile_rows(const int32_t *bs, const Geo &G, int z) {
+    int n;
+    if (G.T == 64) {
+        const int a = 2 * z < G.NTc ? __ldg(bs + 2 * z) : 0, b = 2 * z + 1 < G.NTc ? __ldg(bs + 2 * z + 1) : 0;
+        return Rows{a < 0 ? 0 : (a > 64 ? 64 : a), b < 0 ? 0 : (b > 64 ? 64 : b)};
+    }
+    if (G.T == 128) {
+        n = __ldg(bs + z);
+    } else {
+        n = __ldg(bs + (z >> 1)) - 128 * (z & 1);
+    }
+    n = n < 0 ? 0 : (n > 128 ? 128 : n);
+    return Rows{n < 64 ? n : 64, n > 64 ? n - 64 : 0};
+}
+
+// One warp per (bh, query kernel tile X): the key kernel tiles its caller
+// tiles select, ascending, as (Y << 4) | mask with mask bit 2a + b set when
+// query half a selects key half b.  Key tiles without valid rows are left out.
+// list [BH*NTk, maxlen], cnt [BH*NTk].  Entries out of range are skipped and
+// flagged.
+__global__ void __launch_bounds__(128)
+    pairs_kernel(const int32_t *__restrict__ q2k_idx, const int32_t *__restrict__ q2k_num,
+                 const int32_t *__restrict__ bs, Geo G, int max_kv, int maxlen, int64_t BH,
+                 int32_t *__restrict__ list, int32_t *__restrict__ cnt, int32_t *status) {
+    extern __shared__ uint32_t mw[];  // [4 warps][NTk / 4 + 1] words of 4 mask bytes
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int words = G.NTk / 4 + 1;
+    uint32_t *m = mw + warp * words;
+    const int64_t gx = (int64_t)blockIdx.x * 4 + warp;  // bh * NTk + X
+    if (gx >= BH * G.NTk) return;
+    const int64_t bh = gx / G.NTk;
+    const int X = (int)(gx - bh * G.NTk);
+    for (int w = lane; w < words; w += 32) m[w] = 0u;
+    __syncwarp();
+    bool bad = false;
+    // caller query tiles of X: (t, the mask bits of its rows' halves)
+    const int nsrc = G.T == 64 ? 2 : 1;
+    for (int a = 0; a < nsrc; ++a) {
+        const int t = G.T == 64 ? 2 * X + a : (G.T == 128 ? X : X >> 1);
+        if (t >= G.NTc) continue;
+        int K = __ldg(q2k_num + bh * G.NTc + t);
+        if (K < 0 || K > max_kv) {
+            bad = true;
+            K = K < 0 ? 0 : max_kv;
+        }
+        const int32_t *sel = q2k_idx + (bh * G.NTc + t) * (int64_t)max_kv;
+        for (int i = lane; i < K; i += 32) {
+            const int jc = __ldg(sel + i);
+            if (jc < 0 || jc >= G.NTc) {
+                bad = true;
+                continue;
+            }
+            const int n = __ldg(bs + jc);
+            if (G.T == 64) {
+                if (n <= 0) continue;
+                const int Y = jc >> 1;
+                atomicOr(&m[Y >> 2], (1u << (2 * a + (jc & 1))) << ((Y & 3) * 8));
+            } else if (G.T == 128) {
+                if (n <= 0) continue;
+                atomicOr(&m[jc >> 2], 0xFu << ((jc & 3) * 8));
+            } else {
+                for (int hb = 0; hb < 2; ++hb) {
+                    if (n - 128 * hb <= 0) continue;
+                    const int Y = 2 * jc + hb;
+                    atomicOr(&m[Y >> 2], 0xFu << ((Y & 3) * 8));
+                }
+            }
+        }
+    }
+    __syncwarp();
+    int32_t *out = list + gx * maxlen;
+    int c = 0;
+    for (int base = 0; base < G.NTk; base += 32) {
+        const int Y = base + lane;
+        const uint32_t mk = Y < G.NTk ? (m[Y >> 2] >> ((Y & 3) * 8)) & 0xFu : 0u;
+        const uint32_t bal = __ballot_sync(0xffffffffu, mk != 0u);
+        const int pos = c + __popc(bal & ((1u << lane) - 1u));
+        if (mk != 0u && pos < maxlen) out[pos] = (Y << 4) | (int)mk;
+        c += __popc(bal);
+    }
+    if (lane == 0) cnt[gx] = c < maxlen ? c : maxlen;
+    if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(status, kFlagIndex);
+}
+
+// Mask with the roles of the two sides swapped: bit 2a + b -> bit 2b + a.
+__device__ __forceinline__ int swap_mask(int m) { return (m & 9) | ((m & 2) << 1) | ((m & 4) >> 1); }
+
+// offs [B*H, NTk+1] and list [B*H, NTk*maxlen]: list[bh][offs[bh][Y] ...] are
+// (X << 4) | mask for the query kernel tiles X selecting key kernel tile Y,
+// ascending in X, with mask bit 2a + b set when key half a meets query half b.
 __global__ void __launch_bounds__(1024)
-    k2q_kernel(const int32_t *__restrict__ q2k_idx, const int32_t *__restrict__ q2k_num, int NT, int max_kv,
-               int32_t *__restrict__ offs, int32_t *__restrict__ list, int32_t *status) {
-    extern __shared__ int32_t cnt[];  // [NT + 1]
+    k2q_kernel(const int32_t *__restrict__ pl, const int32_t *__restrict__ pc, int NTk, int maxlen,
+               int32_t *__restrict__ offs, int32_t *__restrict__ list) {
+    extern __shared__ int32_t cur[];  // [NTk + 1]
     const int64_t bh = blockIdx.x;
     const int tid = threadIdx.x;
-    for (int j = tid; j <= NT; j += blockDim.x) cnt[j] = 0;
+    for (int j = tid; j <= NTk; j += blockDim.x) cur[j] = 0;
     __syncthreads();
-    bool bad = false;
-    for (int64_t e = tid; e < (int64_t)NT * max_kv; e += blockDim.x) {
-        const int t = (int)(e / max_kv), i = (int)(e - (int64_t)t * max_kv);
-        int K = __ldg(q2k_num + bh * NT + t);
-        K = K < 0 ? 0 : (K > max_kv ? max_kv : K);
-        if (i >= K) continue;
-        const int j = __ldg(q2k_idx + (bh * NT + t) * max_kv + i);
-        if (j < 0 || j >= NT) {
-            bad = true;
-            continue;
-        }
-        atomicAdd(&cnt[j + 1], 1);
+    const int32_t *plb = pl + bh * (int64_t)NTk * maxlen;
+    const int32_t *pcb = pc + bh * (int64_t)NTk;
+    for (int64_t e = tid; e < (int64_t)NTk * maxlen; e += blockDim.x) {
+        const int X = (int)(e / maxlen), i = (int)(e - (int64_t)X * maxlen);
+        if (i < __ldg(pcb + X)) atomicAdd(&cur[(__ldg(plb + e) >> 4) + 1], 1);
     }
     __syncthreads();
-    if (tid == 0) {  // exclusive scan (NT <= 8192: a short serial pass)
-        for (int j = 1; j <= NT; ++j) cnt[j] += cnt[j - 1];
+    if (tid == 0) {  // exclusive scan (NTk <= 8192: a short serial pass)
+        for (int j = 1; j <= NTk; ++j) cur[j] += cur[j - 1];
     }
     __syncthreads();
-    for (int j = tid; j <= NT; j += blockDim.x) offs[bh * (NT + 1) + j] = cnt[j];
+    for (int j = tid; j <= NTk; j += blockDim.x) offs[bh * (NTk + 1) + j] = cur[j];
     __syncthreads();
-    // fill in ascending t: one row t per round, each key tile appears at most
-    // once per row (distinct selections), so its cursor advances in t order
-    int32_t *lst = list + bh * (int64_t)NT * max_kv;
-    for (int t = 0; t < NT; ++t) {
-        int K = __ldg(q2k_num + bh * NT + t);
-        K = K < 0 ? 0 : (K > max_kv ? max_kv : K);
-        for (int i = tid; i < K; i += blockDim.x) {
-            const int j = __ldg(q2k_idx + (bh * NT + t) * max_kv + i);
-            if (j < 0 || j >= NT) continue;
-            lst[atomicAdd(&cnt[j], 1)] = t;
+    // fill in ascending X: one list per round; a key tile appears at most once
+    // per list, so its cursor advances in X order
+    int32_t *lst = list + bh * (int64_t)NTk * maxlen;
+    int nxt = __ldg(pcb);
+    for (int X = 0; X < NTk; ++X) {
+        const int c = nxt;
+        if (X + 1 < NTk) nxt = __ldg(pcb + X + 1);
+        for (int i = tid; i < c; i += blockDim.x) {
+            const int e = __ldg(plb + (int64_t)X * maxlen + i);
+            lst[atomicAdd(&cur[e >> 4], 1)] = (X << 4) | swap_mask(e & 15);
         }
         __syncthreads();
     }
-    if (bad) atomicOr(status, kFlagIndex);
 }
 
 // ---------------------------------------------------------------- shared memory
@@ -182,14 +284,16 @@ struct BwdSmem {
 };
 
 struct BwdArgs {
-    const float *nlse2;         // [B*H*Sp] -lse * log2(e)
-    const float *ndelta;        // [B*H*Sp] -rowsum(dout * out)
-    const int32_t *q2k_idx, *q2k_num, *block_sizes;
+    const float *nlse2;         // [B*H*Spk] -lse * log2(e)
+    const float *ndelta;        // [B*H*Spk] -rowsum(dout * out)
+    const int32_t *block_sizes;
+    const int32_t *pl, *pc;     // pairs_kernel lists and counts
     const int32_t *k2q_offs, *k2q_list;
     void *dq, *dk, *dv;         // bf16 [B*H*Sp, D]
     int32_t *status;
-    int32_t NT, max_kv;
-    int64_t Sp;
+    Geo G;
+    int32_t maxlen;
+    int64_t Sp, Spk;            // caller rows per (b, h); NTk * 128
     float scale;
 };
 
@@ -226,7 +330,7 @@ __device__ __forceinline__ void st_cols(uint32_t taddr, const uint32_t (&v)[N]) 
 //   p = 2^(scale log2(e) s - lse log2(e)),  ds = p (dp - delta),
 // with the per-column terms from shared memory (KV: columns are queries) or
 // this row's (dQ).  MASK sets p and ds (not multiplies them) to 0 in columns
-// past the partner tile's valid count n_y, whose S and dP may be non-finite.
+// c >= n_y (the partner's padding, whose S and dP may be non-finite).
 // Rows are not masked: a padding row's values reach only its own row of the
 // accumulators, which the epilogue writes as 0.
 template <bool KV, bool MASK>
@@ -300,25 +404,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the resident tile x and its list of partners: key tile j and the query
     // tiles selecting it (KV), or query tile t and its selected key tiles
     const int64_t bhx = blockIdx.x;
-    const int NT = A.NT;
-    const int x = (int)(bhx % NT);
-    const int64_t bh = bhx / NT;
-    const int n_x = __ldg(A.block_sizes + x);
+    const int NTk = A.G.NTk;
+    const int x = (int)(bhx % NTk);
+    const int64_t bh = bhx / NTk;
+    const Rows rx = ktile_rows(A.block_sizes, A.G, x);
     const int32_t *lst;
     int n;
     if (KV) {
-        const int32_t off0 = __ldg(A.k2q_offs + bh * (NT + 1) + x), off1 = __ldg(A.k2q_offs + bh * (NT + 1) + x + 1);
-        lst = A.k2q_list + bh * (int64_t)NT * A.max_kv + off0;
+        const int32_t off0 = __ldg(A.k2q_offs + bh * (NTk + 1) + x), off1 = __ldg(A.k2q_offs + bh * (NTk + 1) + x + 1);
+        lst = A.k2q_list + bh * (int64_t)NTk * A.maxlen + off0;
         n = off1 - off0;
     } else {
-        lst = A.q2k_idx + bhx * A.max_kv;
-        n = __ldg(A.q2k_num + bhx);
-        n = n < 0 ? 0 : (n > A.max_kv ? A.max_kv : n);
+        lst = A.pl + bhx * A.maxlen;
+        n = __ldg(A.pc + bhx);
     }
-    auto partner = [&](int i) -> int {
-        const int y = __ldg(lst + i);
-        return (y < 0 || y >= NT) ? -1 : y;  // bad entries were flagged by k2q_kernel
-    };
+    // pair i: partner kernel tile (entry >> 4) and block mask (entry & 15)
+    auto entry = [&](int i) -> int { return __ldg(lst + i); };
 
     if (threadIdx.x == 0) {
         for (int b = 0; b < kNumBars; ++b) mbar_init(BAR(b), (b == kBarEw0 || b == kBarEw1) ? kEwThreads : 1);
@@ -344,8 +445,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             int issued[2] = {0, 0}, seen[2] = {0, 0};  // per-buffer loads issued / waited for
             const int32_t xrow = (int32_t)(bh * A.Sp + (int64_t)x * kBT);
             auto load_pair = [&](int i) {
-                const int b = i & 1, y = partner(i);
-                const int64_t yrow = bh * A.Sp + (int64_t)(y < 0 ? 0 : y) * kBT;
+                const int b = i & 1, y = entry(i) >> 4;
+                const int64_t yrow = bh * A.Sp + (int64_t)y * kBT;
+                const int64_t yvec = bh * A.Spk + (int64_t)y * kBT;
                 const uint32_t bar = BAR(kBarBuf0 + b);
                 mbar_arrive_expect_tx(bar, 2 * C::kTile + (KV ? 2 * kBT * 4 : 0));
                 for (int c = 0; c < D / 64; ++c) {
@@ -355,8 +457,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 c * 64, (int32_t)yrow, bar, l2_policy_evict_last());
                 }
                 if (KV) {
-                    bulk_load(base + L::kVec + b * 2 * kBT * 4, A.nlse2 + yrow, kBT * 4, bar);
-                    bulk_load(base + L::kVec + b * 2 * kBT * 4 + kBT * 4, A.ndelta + yrow, kBT * 4, bar);
+                    bulk_load(base + L::kVec + b * 2 * kBT * 4, A.nlse2 + yvec, kBT * 4, bar);
+                    bulk_load(base + L::kVec + b * 2 * kBT * 4 + kBT * 4, A.ndelta + yvec, kBT * 4, bar);
                 }
                 ++issued[b];
             };
@@ -419,37 +521,49 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int h = threadIdx.x / kBT;
         const uint32_t tl = (uint32_t)((warp & 3) * 32) << 16;
         const float c1 = A.scale * 1.4426950408889634f;
-        const int64_t xrow_r = bh * A.Sp + (int64_t)x * kBT + r;
-        const float nl2_r = KV ? 0.f : __ldg(A.nlse2 + xrow_r);
-        const float ndl_r = KV ? 0.f : __ldg(A.ndelta + xrow_r);
+        const int64_t xrow_r = bh * A.Sp + (int64_t)x * kBT + r;   // caller row
+        const int64_t xvec_r = bh * A.Spk + (int64_t)x * kBT + r;  // per-row vectors
+        const float nl2_r = KV ? 0.f : __ldg(A.nlse2 + xvec_r);
+        const float ndl_r = KV ? 0.f : __ldg(A.ndelta + xvec_r);
+        const int ra = r >> 6;  // this row's 64-row half of the resident tile (warp-uniform)
         bool ok = true;
         for (int i = 0; i < n; ++i) {
-            const int b = i & 1, y = partner(i);
-            const int n_y = y < 0 ? 0 : __ldg(A.block_sizes + y);
+            const int b = i & 1, e_i = entry(i), mk = e_i & 15;
+            const Rows ry = ktile_rows(A.block_sizes, A.G, e_i >> 4);
             if (!(ok = wait_warp(BAR(kBarS), i & 1u, abort_flag, A.status))) break;
             // the pair's copies are complete and visible here
             if (!(ok = wait_warp(BAR(kBarBuf0 + b), (i >> 1) & 1u, abort_flag, A.status))) break;
             tc_fence_after();
             // operands summed over their rows next get their padding rows cleared
             // (before the first half's arrival): Q_t and dO_t (KV), K_j (dQ)
-            if (h == 0) zero_row_if<D>(g + L::buf(b, 0), r, n_y);
-            if (KV && h == 1) zero_row_if<D>(g + L::buf(b, 1), r, n_y);
+            const bool zr = !ry.valid(r);
+            if (zr && h == 0) zero_row<D>(g + L::buf(b, 0), r);
+            if (zr && KV && h == 1) zero_row<D>(g + L::buf(b, 1), r);
             const float2 *s_nl2 = reinterpret_cast<const float2 *>(g + L::kVec + b * 2 * kBT * 4);
             const float2 *s_ndl = s_nl2 + kBT / 2;
 #pragma unroll 1
             for (int hv = 0; hv < 2; ++hv) {
                 const int c0 = hv * 64 + h * kEwCols;  // this thread's columns of the half
-                float sv[kEwCols], dp[kEwCols];
-                ld_cols(tS + tl + c0, sv);
-                ld_cols(tdP + tl + c0, dp);
+                const int nyh = hv ? ry.hi : ry.lo;     // valid columns of this half
                 uint32_t pw[kEwCols / 2], dw[kEwCols / 2];
-                // warp-uniform: only a tail partner tile needs the column mask
-                if (n_y >= c0 + kEwCols) ew_cols<KV, false>(sv, dp, pw, dw, c0, n_y, c1, s_nl2, s_ndl, nl2_r, ndl_r);
-                else ew_cols<KV, true>(sv, dp, pw, dw, c0, n_y, c1, s_nl2, s_ndl, nl2_r, ndl_r);
+                if ((mk >> (2 * ra + hv)) & 1) {  // warp-uniform
+                    float sv[kEwCols], dp[kEwCols];
+                    ld_cols(tS + tl + c0, sv);
+                    ld_cols(tdP + tl + c0, dp);
+                    // only a partner half with padding needs the column mask
+                    if (nyh >= h * kEwCols + kEwCols)
+                        ew_cols<KV, false>(sv, dp, pw, dw, c0, 0, c1, s_nl2, s_ndl, nl2_r, ndl_r);
+                    else
+                        ew_cols<KV, true>(sv, dp, pw, dw, c0, hv * 64 + nyh, c1, s_nl2, s_ndl, nl2_r, ndl_r);
+                } else {
+                    // a block the selection leaves out: P = dS = 0
+#pragma unroll
+                    for (int w = 0; w < kEwCols / 2; ++w) pw[w] = dw[w] = 0u;
+                }
                 // bf16 pairs back over the first half of the columns just read
                 if (KV) st_cols(tS + tl + c0, pw);
                 st_cols((KV ? tdP : tS) + tl + c0, dw);
-                if (hv == 0 && r >= n_y) fence_proxy_async_smem();  // this thread's zeroed rows, for the MMAs
+                if (hv == 0 && zr) fence_proxy_async_smem();  // this thread's zeroed rows, for the MMAs
                 tmem_wait_st();
                 tc_fence_before();
                 mbar_arrive(BAR(kBarEw0 + hv));
@@ -459,7 +573,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok && n > 0 && !wait_warp(BAR(kBarPair), (n - 1) & 1u, abort_flag, A.status)) ok = false;
         if (ok) {
             tc_fence_after();
-            const bool live = n > 0 && r < n_x;
+            const bool live = n > 0 && rx.valid(r);
+            const bool exists = (int64_t)x * kBT + r < A.Sp;  // the last half of an odd 64-tile count is not
             {
                 // KV: threads of even h write dV, odd h dK; dQ: every h a share of the columns
                 const int which = KV ? (h & 1) : 0;
@@ -475,8 +590,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t w[16];
 #pragma unroll
                     for (int e = 0; e < 16; ++e) w[e] = live ? pack_bf16x2(a[2 * e] * mul, a[2 * e + 1] * mul) : 0u;
+                    if (exists)
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) dst[cb * 4 + q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+                        for (int q = 0; q < 4; ++q)
+                            dst[cb * 4 + q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
                 }
             }
         }
@@ -490,6 +607,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 size_t bwd_smem_bytes(int D) { return D == 128 ? BwdSmem<128>::kTotal : BwdSmem<64>::kTotal; }
+int bwd_threads() { return kThreads; }
 
 template <int D, bool KV>
 static cudaError_t bwd_attr() {
@@ -510,29 +628,35 @@ cudaError_t launch_bwd(const BwdLaunch &L, cudaStream_t stream) {
     const int Dv = L.D / 8;
     delta_kernel<<<(unsigned)((rows * 8 + 255) / 256), 256, 0, stream>>>(
         reinterpret_cast<const uint4 *>(L.out), reinterpret_cast<const uint4 *>(L.dout), L.lse, L.ndelta, L.nlse2,
-        rows, Dv);
+        rows, Dv, L.Sp, L.Spk);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    k2q_kernel<<<(unsigned)L.BH, 1024, (size_t)(L.NT + 1) * 4, stream>>>(L.q2k_idx, L.q2k_num, L.NT, L.max_kv,
-                                                                         L.k2q_offs, L.k2q_list, L.status);
+    const Geo G{L.T, L.NTc, L.NTk};
+    const int64_t nx = (int64_t)L.BH * L.NTk;
+    pairs_kernel<<<(unsigned)((nx + 3) / 4), 128, (size_t)4 * (L.NTk / 4 + 1) * 4, stream>>>(
+        L.q2k_idx, L.q2k_num, L.block_sizes, G, L.max_kv, L.maxlen, (int64_t)L.BH, L.pl, L.pc, L.status);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    k2q_kernel<<<(unsigned)L.BH, 1024, (size_t)(L.NTk + 1) * 4, stream>>>(L.pl, L.pc, L.NTk, L.maxlen, L.k2q_offs,
+                                                                          L.k2q_list);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     BwdArgs A;
     A.nlse2 = L.nlse2;
     A.ndelta = L.ndelta;
-    A.q2k_idx = L.q2k_idx;
-    A.q2k_num = L.q2k_num;
     A.block_sizes = L.block_sizes;
+    A.pl = L.pl;
+    A.pc = L.pc;
     A.k2q_offs = L.k2q_offs;
     A.k2q_list = L.k2q_list;
     A.dq = L.dq;
     A.dk = L.dk;
     A.dv = L.dv;
     A.status = L.status;
-    A.NT = L.NT;
-    A.max_kv = L.max_kv;
+    A.G = G;
+    A.maxlen = L.maxlen;
     A.Sp = L.Sp;
+    A.Spk = L.Spk;
     A.scale = L.scale;
-    const unsigned grid = (unsigned)((int64_t)L.BH * L.NT);
+    const unsigned grid = (unsigned)nx;
     if (L.D == 128) {
         bwd_kernel<128, true><<<grid, kThreads, BwdSmem<128>::kTotal, stream>>>(*L.tm_q, *L.tm_k, *L.tm_v, *L.tm_do, A);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;

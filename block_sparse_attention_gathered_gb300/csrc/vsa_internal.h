@@ -78,22 +78,40 @@ struct UntileParams {
 
 cudaError_t launch_untile(const UntileParams &p, int num_sms, cudaStream_t stream);
 
-// Backward pass (vsa_bwd.cu), 128-token tiles.
+// Backward pass (vsa_bwd.cu).  It works on 128-row kernel tiles: a caller
+// tile of 128, one half of a caller tile of 256, or two caller tiles of 64.
+struct BwdGeo {
+    int32_t NTk;     // kernel tiles per (b, h)
+    int32_t maxlen;  // longest partner list of a kernel tile
+};
+
+inline BwdGeo bwd_geo(int T, int NTc, int max_kv) {
+    BwdGeo g;
+    g.NTk = T == 64 ? (NTc + 1) / 2 : (T == 128 ? NTc : 2 * NTc);
+    const int per = (T == 128) ? 1 : 2;  // kernel tiles one selection entry can reach
+    const int64_t m = (int64_t)per * (max_kv > 0 ? max_kv : 1);
+    g.maxlen = (int32_t)(m < g.NTk ? m : g.NTk);
+    if (g.maxlen < 1) g.maxlen = 1;
+    return g;
+}
+
 struct BwdLaunch {
     const CUtensorMap *tm_q, *tm_k, *tm_v, *tm_do;  // rows of D bf16, box {64, 128}
     const void *out, *dout;                           // bf16 [B*H*Sp, D]
     const float *lse;                                 // [B*H*Sp]
-    float *ndelta, *nlse2;                            // workspace [B*H*Sp] each: -delta, -lse*log2(e)
+    float *ndelta, *nlse2;                            // workspace [B*H*Spk] each: -delta, -lse*log2(e)
     const int32_t *q2k_idx, *q2k_num, *block_sizes;
-    int32_t *k2q_offs, *k2q_list;                     // workspace [B*H, NT+1], [B*H, NT*max_kv]
+    int32_t *pl, *pc;                                 // workspace [B*H*NTk, maxlen], [B*H*NTk]
+    int32_t *k2q_offs, *k2q_list;                     // workspace [B*H, NTk+1], [B*H, NTk*maxlen]
     void *dq, *dk, *dv;                               // bf16 [B*H*Sp, D]
     int32_t *status;
-    int32_t BH, NT, D, max_kv;
-    int64_t Sp;
+    int32_t BH, T, NTc, NTk, D, max_kv, maxlen;
+    int64_t Sp, Spk;                                  // NTc * T; NTk * 128
     float scale;
 };
 
 size_t bwd_smem_bytes(int D);
+int bwd_threads();
 cudaError_t bwd_prepare();
 cudaError_t launch_bwd(const BwdLaunch &L, cudaStream_t stream);
 

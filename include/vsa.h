@@ -187,14 +187,20 @@ vsa_status vsa_tile_layout(const void *q_tok, const void *k_tok, const void *v_t
  * Rows with no keys get dq = 0, keys no row selects get dk = dv = 0, padding
  * rows are +0; a NaN row of the forward gives NaN gradients on its keys.
  *
- *   q, k, v, out, dout  bf16 [B, H, NT*128, D] tile-major (out and lse as
+ *   q, k, v, out, dout  bf16 [B, H, NT*tile, D] tile-major (out and lse as
  *                       vsa_block_sparse_fwd wrote them; lse is required)
  *   q2k_idx, q2k_num, block_sizes  the forward's selection (distinct,
  *                       in-range tiles; out-of-range entries are skipped and
- *                       flagged, repeated ones count twice)
- *   dq, dk, dv          bf16 [B, H, NT*128, D] outputs, written completely
- *   dims                tile must be 128; head_dim 64 or 128
+ *                       flagged, a repeated one counts once)
+ *   dq, dk, dv          bf16 [B, H, NT*tile, D] outputs, written completely
+ *   dims                tile 64, 128 or 256; head_dim 64 or 128
  *   workspace           vsa_block_sparse_bwd_workspace_size(dims) bytes
+ *                       (0 for invalid dims)
+ * The kernels work on 128-row tiles: a 256-token tile as two halves, two
+ * 64-token tiles together with a mask of which 64 x 64 blocks are selected.
+ * As in the forward with tile == 64, a non-finite value in a VALID row of
+ * one 64-token tile can then reach the gradients of the paired tile through
+ * a zero weight (padding rows are zeroed first and never do).
  * Deterministic: dQ is recomputed per query tile instead of accumulated with
  * atomics, and dK/dV sum their query tiles in ascending order.
  */

@@ -50,14 +50,34 @@ def _case(seed, B, H, NT, D, T=128, full=False, pad="naninf", empty_frac=0.1):
     return q, k, v, do, idx, counts, bs
 
 
-def _check(name, got, ref, bs, T):
+def _structural_zero_tiles(idx, counts, bs):
+    """[B, H, NT] masks of the tiles whose gradient rows are 0 by the selection
+    alone: query tiles with no non-empty key tile (dq), and key tiles that no
+    non-empty query tile selects (dk, dv).  Rows whose reference is 0 only by
+    cancellation (one key: dout.v = delta) are held to the tolerance instead."""
+    B, H, NT, _ = idx.shape
+    n = bs.numpy()
+    q_zero = np.ones((B, H, NT), dtype=bool)
+    k_zero = np.ones((B, H, NT), dtype=bool)
+    for b in range(B):
+        for h in range(H):
+            for t in range(NT):
+                for j in idx[b, h, t, :int(counts[b, h, t])].tolist():
+                    if n[j] > 0 and n[t] > 0:
+                        q_zero[b, h, t] = False
+                        k_zero[b, h, j] = False
+    return q_zero, k_zero
+
+
+def _check(name, got, ref, bs, T, zero_tiles):
     g = got.float().cpu().numpy().astype(np.float64)
     B, H, Sp, D = g.shape
     valid = (np.arange(Sp) % T) < bs.numpy()[np.arange(Sp) // T]
     assert (got[:, :, ~torch.from_numpy(valid)].view(torch.int16) == 0).all(), f"{name}: padding rows not +0"
     gv, rv = g[:, :, valid], ref[:, :, valid]
-    zero_ref = (rv == 0).all(-1)
-    assert (gv[zero_ref] == 0).all(), f"{name}: rows that must be 0 are not"
+    zero_rows = np.repeat(zero_tiles, T, axis=2)[:, :, valid]
+    assert (rv[zero_rows] == 0).all(), f"{name}: oracle rows not 0 where the selection makes them 0"
+    assert (gv[zero_rows] == 0).all(), f"{name}: rows that must be 0 are not"
     err = gv - rv
     rel = float(np.linalg.norm(err) / max(np.linalg.norm(rv), 1e-30))
     mx = float(np.abs(err).max())
@@ -66,10 +86,15 @@ def _check(name, got, ref, bs, T):
     assert rel <= REL_RMS and mx <= MAX_REL * max(scale, 1e-30), f"{name}: rel rms {rel:.3e}, max abs {mx:.3e}"
 
 
-@pytest.mark.parametrize("B,H,NT,D,full", [(1, 2, 3, 128, True), (2, 2, 5, 64, False), (1, 3, 6, 128, False)])
-def test_bwd_matches_oracle(vsa, oracle_mod, B, H, NT, D, full):
-    T = 128
-    q, k, v, do, idx, counts, bs = _case(50 + NT + D, B, H, NT, D, full=full)
+@pytest.mark.parametrize("B,H,NT,D,full,T", [
+    (1, 2, 3, 128, True, 128), (2, 2, 5, 64, False, 128), (1, 3, 6, 128, False, 128),
+    # 64-token tiles: two per kernel tile with a block mask; odd counts leave a half-empty last one
+    (1, 2, 7, 64, False, 64), (2, 2, 9, 128, False, 64), (1, 2, 4, 64, True, 64),
+    # 256-token tiles: two kernel tiles each
+    (1, 2, 3, 128, False, 256), (1, 1, 2, 64, True, 256),
+])
+def test_bwd_matches_oracle(vsa, oracle_mod, B, H, NT, D, full, T):
+    q, k, v, do, idx, counts, bs = _case(50 + NT + D + T, B, H, NT, D, T=T, full=full)
     dev = "cuda"
     qd, kd, vd, dod = (x.to(dev) for x in (q, k, v, do))
     idd, cd, bsd = idx.to(dev), counts.to(dev), bs.to(dev)
@@ -78,22 +103,46 @@ def test_bwd_matches_oracle(vsa, oracle_mod, B, H, NT, D, full):
     torch.cuda.synchronize()
     assert vsa.vsa_check_device_status() == 0
     r = vsa.vsa_last_route()
-    assert r["kernel"] == vsa.VSA_KERNEL_BWD and r["tile"] == 128 and r["head_dim"] == D
+    assert r["kernel"] == vsa.VSA_KERNEL_BWD and r["tile"] == T and r["head_dim"] == D
     rq, rk, rv = oracle_mod.block_sparse_attention_bwd(q, k, v, do, idx, counts, bs, T, 1.0 / math.sqrt(D))
-    label = f"B{B}H{H}NT{NT}D{D}{'dense' if full else 'ragged'}"
-    _check(label + " dq", dq, rq, bs, T)
-    _check(label + " dk", dk, rk, bs, T)
-    _check(label + " dv", dv, rv, bs, T)
+    label = f"B{B}H{H}NT{NT}D{D}T{T}{'dense' if full else 'ragged'}"
+    q_zero, k_zero = _structural_zero_tiles(idx, counts, bs)
+    _check(label + " dq", dq, rq, bs, T, q_zero)
+    _check(label + " dk", dk, rk, bs, T, k_zero)
+    _check(label + " dv", dv, rv, bs, T, k_zero)
 
 
-def test_bwd_deterministic(vsa):
-    q, k, v, do, idx, counts, bs = _case(77, 1, 2, 6, 128)
+@pytest.mark.parametrize("T", [64, 128])
+def test_bwd_deterministic(vsa, T):
+    q, k, v, do, idx, counts, bs = _case(77, 1, 2, 6, 128, T=T)
     dev = "cuda"
     args = [x.to(dev) for x in (q, k, v)]
     idd, cd, bsd = idx.to(dev), counts.to(dev), bs.to(dev)
-    out, lse = vsa.block_sparse_attention(*args, idd, cd, bsd, 128, want_lse=True)
-    a = vsa.block_sparse_attention_bwd(*args, out, do.to(dev), lse, idd, cd, bsd, 128)
-    b = vsa.block_sparse_attention_bwd(*args, out, do.to(dev), lse, idd, cd, bsd, 128)
+    out, lse = vsa.block_sparse_attention(*args, idd, cd, bsd, T, want_lse=True)
+    a = vsa.block_sparse_attention_bwd(*args, out, do.to(dev), lse, idd, cd, bsd, T)
+    b = vsa.block_sparse_attention_bwd(*args, out, do.to(dev), lse, idd, cd, bsd, T)
     torch.cuda.synchronize()
     for x, y in zip(a, b):
         assert torch.equal(x.view(torch.int16), y.view(torch.int16))
+
+
+def test_bwd_odd_64_tiles_leave_next_head_alone(vsa):
+    """With an odd count of 64-token tiles the last kernel tile of a head
+    reaches 64 rows into the next head's rows; they must stay untouched."""
+    B, H, NT, D, T = 1, 3, 5, 64, 64
+    q, k, v, do, idx, counts, bs = _case(91, B, H, NT, D, T=T, full=True)
+    dev = "cuda"
+    qd, kd, vd, dod = (x.to(dev) for x in (q, k, v, do))
+    idd, cd, bsd = idx.to(dev), counts.to(dev), bs.to(dev)
+    out, lse = vsa.block_sparse_attention(qd, kd, vd, idd, cd, bsd, T, want_lse=True)
+    dq, dk, dv = vsa.block_sparse_attention_bwd(qd, kd, vd, out, dod, lse, idd, cd, bsd, T)
+    # per-head results must not depend on the other heads: run each head alone
+    for h in range(H):
+        sl = slice(h, h + 1)
+        o1, l1 = vsa.block_sparse_attention(qd[:, sl].contiguous(), kd[:, sl].contiguous(), vd[:, sl].contiguous(),
+                                            idd[:, sl].contiguous(), cd[:, sl].contiguous(), bsd, T, want_lse=True)
+        g1 = vsa.block_sparse_attention_bwd(qd[:, sl].contiguous(), kd[:, sl].contiguous(), vd[:, sl].contiguous(),
+                                            o1, dod[:, sl].contiguous(), l1, idd[:, sl].contiguous(),
+                                            cd[:, sl].contiguous(), bsd, T)
+        for full_g, one in zip((dq, dk, dv), g1):
+            assert torch.equal(full_g[:, sl].view(torch.int16), one.view(torch.int16)), f"head {h}"
