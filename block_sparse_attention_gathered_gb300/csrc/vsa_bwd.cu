@@ -153,9 +153,18 @@ __device__ __forceinline__ Rows ktile_rows(const int32_t *bs, const Geo &G, int 
     return Rows{n < 64 ? n : 64, n > 64 ? n - 64 : 0};
 }
 
-// One warp per (bh, query kernel tile X): the key kernel tiles its caller
-// tiles select, ascending, as (Y << 4) | mask with mask bit 2a + b set when
-// query half a selects key half b.  Key tiles without valid rows are left out.
+// A partner list entry: partner kernel tile y (13 bits), its valid rows per
+// half (7 bits each) and the block mask (4 bits).
+__device__ __forceinline__ int32_t pack_entry(int y, Rows rw, int mask) {
+    return (int32_t)(((uint32_t)y << 18) | ((uint32_t)rw.lo << 11) | ((uint32_t)rw.hi << 4) | (uint32_t)mask);
+}
+__device__ __forceinline__ int entry_y(int32_t e) { return (int)((uint32_t)e >> 18); }
+__device__ __forceinline__ Rows entry_rows(int32_t e) { return Rows{(e >> 11) & 127, (e >> 4) & 127}; }
+
+// One warp per (bh, query kernel tile X): the key kernel tiles Y its caller
+// tiles select, ascending, as pack_entry(Y, rows of Y, mask) with mask bit
+// 2a + b set when query half a selects key half b.  Key tiles without valid
+// rows are left out.
 // list [BH*NTk, maxlen], cnt [BH*NTk].  Entries out of range are skipped and
 // flagged.
 __global__ void __launch_bounds__(128)
@@ -215,7 +224,7 @@ __global__ void __launch_bounds__(128)
         const uint32_t mk = Y < G.NTk ? (m[Y >> 2] >> ((Y & 3) * 8)) & 0xFu : 0u;
         const uint32_t bal = __ballot_sync(0xffffffffu, mk != 0u);
         const int pos = c + __popc(bal & ((1u << lane) - 1u));
-        if (mk != 0u && pos < maxlen) out[pos] = (Y << 4) | (int)mk;
+        if (mk != 0u && pos < maxlen) out[pos] = pack_entry(Y, ktile_rows(bs, G, Y), (int)mk);
         c += __popc(bal);
     }
     if (lane == 0) cnt[gx] = c < maxlen ? c : maxlen;
@@ -226,11 +235,13 @@ __global__ void __launch_bounds__(128)
 __device__ __forceinline__ int swap_mask(int m) { return (m & 9) | ((m & 2) << 1) | ((m & 4) >> 1); }
 
 // offs [B*H, NTk+1] and list [B*H, NTk*maxlen]: list[bh][offs[bh][Y] ...] are
-// (X << 4) | mask for the query kernel tiles X selecting key kernel tile Y,
-// ascending in X, with mask bit 2a + b set when key half a meets query half b.
+// pack_entry(X, rows of X, mask) for the query kernel tiles X selecting key
+// kernel tile Y, ascending in X, with mask bit 2a + b set when key half a
+// meets query half b.
 __global__ void __launch_bounds__(1024)
-    k2q_kernel(const int32_t *__restrict__ pl, const int32_t *__restrict__ pc, int NTk, int maxlen,
-               int32_t *__restrict__ offs, int32_t *__restrict__ list) {
+    k2q_kernel(const int32_t *__restrict__ pl, const int32_t *__restrict__ pc, const int32_t *__restrict__ bs,
+               Geo G, int maxlen, int32_t *__restrict__ offs, int32_t *__restrict__ list) {
+    const int NTk = G.NTk;
     extern __shared__ int32_t cur[];  // [NTk + 1]
     const int64_t bh = blockIdx.x;
     const int tid = threadIdx.x;
@@ -240,7 +251,7 @@ __global__ void __launch_bounds__(1024)
     const int32_t *pcb = pc + bh * (int64_t)NTk;
     for (int64_t e = tid; e < (int64_t)NTk * maxlen; e += blockDim.x) {
         const int X = (int)(e / maxlen), i = (int)(e - (int64_t)X * maxlen);
-        if (i < __ldg(pcb + X)) atomicAdd(&cur[(__ldg(plb + e) >> 4) + 1], 1);
+        if (i < __ldg(pcb + X)) atomicAdd(&cur[entry_y(__ldg(plb + e)) + 1], 1);
     }
     __syncthreads();
     if (tid == 0) {  // exclusive scan (NTk <= 8192: a short serial pass)
@@ -256,9 +267,12 @@ __global__ void __launch_bounds__(1024)
     for (int X = 0; X < NTk; ++X) {
         const int c = nxt;
         if (X + 1 < NTk) nxt = __ldg(pcb + X + 1);
-        for (int i = tid; i < c; i += blockDim.x) {
-            const int e = __ldg(plb + (int64_t)X * maxlen + i);
-            lst[atomicAdd(&cur[e >> 4], 1)] = (X << 4) | swap_mask(e & 15);
+        if (c > 0) {
+            const Rows rx = ktile_rows(bs, G, X);
+            for (int i = tid; i < c; i += blockDim.x) {
+                const int32_t e = __ldg(plb + (int64_t)X * maxlen + i);
+                lst[atomicAdd(&cur[entry_y(e)], 1)] = pack_entry(X, rx, swap_mask(e & 15));
+            }
         }
         __syncthreads();
     }
@@ -385,7 +399,8 @@ __device__ __forceinline__ void mma_acc_half(uint32_t tacc, uint32_t ta, uint32_
 // TMEM (S-like and dP-like), an elementwise step by 256 threads that writes
 // bf16 operands back into TMEM in two column halves, and one or two
 // accumulations from TMEM, each issued half by half as the halves are ready.
-template <int D, bool KV>
+// BM: pairs carry block masks (64-token tiles); otherwise every mask is full.
+template <int D, bool KV, bool BM>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -418,8 +433,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         lst = A.pl + bhx * A.maxlen;
         n = __ldg(A.pc + bhx);
     }
-    // pair i: partner kernel tile (entry >> 4) and block mask (entry & 15)
-    auto entry = [&](int i) -> int { return __ldg(lst + i); };
+    // pair i: partner kernel tile, its valid rows and the block mask
+    auto entry = [&](int i) -> int32_t { return __ldg(lst + i); };
 
     if (threadIdx.x == 0) {
         for (int b = 0; b < kNumBars; ++b) mbar_init(BAR(b), (b == kBarEw0 || b == kBarEw1) ? kEwThreads : 1);
@@ -445,7 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int issued[2] = {0, 0}, seen[2] = {0, 0};  // per-buffer loads issued / waited for
             const int32_t xrow = (int32_t)(bh * A.Sp + (int64_t)x * kBT);
             auto load_pair = [&](int i) {
-                const int b = i & 1, y = entry(i) >> 4;
+                const int b = i & 1, y = entry_y(entry(i));
                 const int64_t yrow = bh * A.Sp + (int64_t)y * kBT;
                 const int64_t yvec = bh * A.Spk + (int64_t)y * kBT;
                 const uint32_t bar = BAR(kBarBuf0 + b);
@@ -528,8 +543,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int ra = r >> 6;  // this row's 64-row half of the resident tile (warp-uniform)
         bool ok = true;
         for (int i = 0; i < n; ++i) {
-            const int b = i & 1, e_i = entry(i), mk = e_i & 15;
-            const Rows ry = ktile_rows(A.block_sizes, A.G, e_i >> 4);
+            const int b = i & 1;
+            const int32_t e_i = entry(i);
+            const int mk = e_i & 15;
+            const Rows ry = entry_rows(e_i);
             if (!(ok = wait_warp(BAR(kBarS), i & 1u, abort_flag, A.status))) break;
             // the pair's copies are complete and visible here
             if (!(ok = wait_warp(BAR(kBarBuf0 + b), (i >> 1) & 1u, abort_flag, A.status))) break;
@@ -546,7 +563,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int c0 = hv * 64 + h * kEwCols;  // this thread's columns of the half
                 const int nyh = hv ? ry.hi : ry.lo;     // valid columns of this half
                 uint32_t pw[kEwCols / 2], dw[kEwCols / 2];
-                if ((mk >> (2 * ra + hv)) & 1) {  // warp-uniform
+                if (!BM || ((mk >> (2 * ra + hv)) & 1)) {  // warp-uniform
                     float sv[kEwCols], dp[kEwCols];
                     ld_cols(tS + tl + c0, sv);
                     ld_cols(tdP + tl + c0, dp);
@@ -609,18 +626,34 @@ __global__ void __launch_bounds__(kThreads, 1)
 size_t bwd_smem_bytes(int D) { return D == 128 ? BwdSmem<128>::kTotal : BwdSmem<64>::kTotal; }
 int bwd_threads() { return kThreads; }
 
-template <int D, bool KV>
+template <int D, bool KV, bool BM>
 static cudaError_t bwd_attr() {
-    return cudaFuncSetAttribute(bwd_kernel<D, KV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    return cudaFuncSetAttribute(bwd_kernel<D, KV, BM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 (int)BwdSmem<D>::kTotal);
+}
+
+template <int D, bool BM>
+static cudaError_t bwd_attr2() {
+    cudaError_t e = bwd_attr<D, true, BM>();
+    return e != cudaSuccess ? e : bwd_attr<D, false, BM>();
 }
 
 cudaError_t bwd_prepare() {
     cudaError_t e;
-    if ((e = bwd_attr<64, true>()) != cudaSuccess) return e;
-    if ((e = bwd_attr<64, false>()) != cudaSuccess) return e;
-    if ((e = bwd_attr<128, true>()) != cudaSuccess) return e;
-    return bwd_attr<128, false>();
+    if ((e = bwd_attr2<64, false>()) != cudaSuccess) return e;
+    if ((e = bwd_attr2<64, true>()) != cudaSuccess) return e;
+    if ((e = bwd_attr2<128, false>()) != cudaSuccess) return e;
+    return bwd_attr2<128, true>();
+}
+
+// The dK/dV kernel, then the dQ kernel.
+template <int D, bool BM>
+static cudaError_t launch_pair(const BwdLaunch &L, const BwdArgs &A, unsigned grid, cudaStream_t stream) {
+    bwd_kernel<D, true, BM><<<grid, kThreads, BwdSmem<D>::kTotal, stream>>>(*L.tm_q, *L.tm_k, *L.tm_v, *L.tm_do, A);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    bwd_kernel<D, false, BM><<<grid, kThreads, BwdSmem<D>::kTotal, stream>>>(*L.tm_q, *L.tm_k, *L.tm_v, *L.tm_do, A);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_bwd(const BwdLaunch &L, cudaStream_t stream) {
@@ -636,8 +669,8 @@ cudaError_t launch_bwd(const BwdLaunch &L, cudaStream_t stream) {
     pairs_kernel<<<(unsigned)((nx + 3) / 4), 128, (size_t)4 * (L.NTk / 4 + 1) * 4, stream>>>(
         L.q2k_idx, L.q2k_num, L.block_sizes, G, L.max_kv, L.maxlen, (int64_t)L.BH, L.pl, L.pc, L.status);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    k2q_kernel<<<(unsigned)L.BH, 1024, (size_t)(L.NTk + 1) * 4, stream>>>(L.pl, L.pc, L.NTk, L.maxlen, L.k2q_offs,
-                                                                          L.k2q_list);
+    k2q_kernel<<<(unsigned)L.BH, 1024, (size_t)(L.NTk + 1) * 4, stream>>>(L.pl, L.pc, L.block_sizes, G, L.maxlen,
+                                                                          L.k2q_offs, L.k2q_list);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     BwdArgs A;
     A.nlse2 = L.nlse2;
@@ -657,16 +690,9 @@ cudaError_t launch_bwd(const BwdLaunch &L, cudaStream_t stream) {
     A.Spk = L.Spk;
     A.scale = L.scale;
     const unsigned grid = (unsigned)nx;
-    if (L.D == 128) {
-        bwd_kernel<128, true><<<grid, kThreads, BwdSmem<128>::kTotal, stream>>>(*L.tm_q, *L.tm_k, *L.tm_v, *L.tm_do, A);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        bwd_kernel<128, false><<<grid, kThreads, BwdSmem<128>::kTotal, stream>>>(*L.tm_q, *L.tm_k, *L.tm_v, *L.tm_do, A);
-    } else {
-        bwd_kernel<64, true><<<grid, kThreads, BwdSmem<64>::kTotal, stream>>>(*L.tm_q, *L.tm_k, *L.tm_v, *L.tm_do, A);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        bwd_kernel<64, false><<<grid, kThreads, BwdSmem<64>::kTotal, stream>>>(*L.tm_q, *L.tm_k, *L.tm_v, *L.tm_do, A);
-    }
-    return cudaGetLastError();
+    const bool bm = L.T == 64;
+    if (L.D == 128) return bm ? launch_pair<128, true>(L, A, grid, stream) : launch_pair<128, false>(L, A, grid, stream);
+    return bm ? launch_pair<64, true>(L, A, grid, stream) : launch_pair<64, false>(L, A, grid, stream);
 }
 
 }  // namespace vsa
