@@ -62,14 +62,15 @@ constexpr int kBT = 128;            // tile rows (queries or keys)
 constexpr int kEwSplit = 2;                 // elementwise threads per row
 constexpr int kEwThreads = kEwSplit * kBT;  // elementwise warps first
 constexpr int kEwCols = 64 / kEwSplit;      // columns per thread in each 64-column half
-constexpr int kCtlWarp = kEwThreads / 32;   // TMA + MMA issue (lane 0)
-constexpr int kThreads = kEwThreads + 32;
+constexpr int kCtlWarp = kEwThreads / 32;   // lane 0 issues the accumulation MMAs
+constexpr int kSdpWarp = kCtlWarp + 1;      // lane 0 issues the TMA copies and the S/dP MMAs
+constexpr int kThreads = kEwThreads + 64;
 constexpr uint32_t kChunkBytes = kBT * 128;  // one 64-column (128-byte) chunk of a 128-row tile
 
 template <int D>
 struct BwdCfg {
     static constexpr uint32_t kTile = kBT * D * 2;   // one Q/K/V/dO tile in shared memory
-    static constexpr uint32_t kIdescSq = idesc_bf16(128, kBT, false);  // S-like products, N = 128
+    static constexpr uint32_t kIdescHalf = idesc_bf16(128, 64, false);  // S-like products, N = 64
     static constexpr uint32_t kIdescAcc = idesc_bf16(128, D, true);    // accumulations, B MN-major
 };
 
@@ -85,14 +86,16 @@ __device__ __forceinline__ void zero_row(uint8_t *tile, int row) {
     }
 }
 
-// Issues the D/16 MMAs of a 128 x 128 product over D (both operands K-major).
+// Issues the D/16 MMAs of a 128 x 64 product over D: the 128 resident rows
+// times 64 rows of a partner tile (both operands K-major; b_saddr points at
+// the first of the 64 rows inside the tile's first column chunk).
 template <int D>
-__device__ __forceinline__ void mma_sq(uint32_t tdst, uint32_t a_saddr, uint32_t b_saddr) {
+__device__ __forceinline__ void mma_half(uint32_t tdst, uint32_t a_saddr, uint32_t b_saddr) {
     const uint64_t a = sdesc_sw128(a_saddr, 16, 1024), b = sdesc_sw128(b_saddr, 16, 1024);
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk)
         mma_ss(tdst, a + (kk >> 2) * (kChunkBytes >> 4) + (kk & 3) * 2, b + (kk >> 2) * (kChunkBytes >> 4) + (kk & 3) * 2,
-               BwdCfg<D>::kIdescSq, kk > 0 ? 1u : 0u);
+               BwdCfg<D>::kIdescHalf, kk > 0 ? 1u : 0u);
 }
 
 // ---------------------------------------------------------------- delta
@@ -311,11 +314,13 @@ struct BwdArgs {
     float scale;
 };
 
-// mbarriers: resident tiles loaded, per-buffer tiles loaded (two), S and dP in
-// TMEM, P/dS of the first and of the second 64 columns written back to TMEM,
-// the pair's accumulations done, the issuer's final drain
-enum { kBarRes = 0, kBarBuf0 = 1, kBarBuf1 = 2, kBarS = 3, kBarEw0 = 4, kBarEw1 = 5, kBarPair = 6, kBarDrain = 7 };
-constexpr int kNumBars = 8;
+// mbarriers: resident tiles loaded, per-buffer tiles loaded (two), and per
+// TMEM slot (one 64-column half of a pair): S and dP in the slot, P/dS written
+// back to it, its accumulations done (the slot is free); the final drain.
+enum { kBarRes = 0, kBarBuf0 = 1, kBarBuf1 = 2, kBarS0 = 3, kBarS1 = 4, kBarEw0 = 5, kBarEw1 = 6, kBarFree0 = 7,
+       kBarFree1 = 8, kBarDrain = 9 };
+constexpr int kNumBars = 10;
+constexpr uint32_t kHalfBytes = 64 * 128;  // 64 rows of one 128-byte column chunk
 
 // Where the bf16 pairs of S/dP columns [16kk, 16kk + 16) sit in TMEM: the
 // thread that read the kEwCols columns [c0, c0 + kEwCols) writes their packed
@@ -381,15 +386,16 @@ __device__ __forceinline__ void ew_cols(const float (&sv)[kEwCols], const float 
 
 // Issues the 4 MMAs of one half (64 of the 128 summed rows) of
 // acc(128 x D) += A(128 x 128, bf16 pairs in TMEM) x tile(128 x D, MN-major in
-// shared memory: the tile's rows are summed).
+// shared memory: the tile's rows are summed).  ta is the half's TMEM slot,
+// which holds the bf16 pairs of its 64 columns.
 template <int D>
 __device__ __forceinline__ void mma_acc_half(uint32_t tacc, uint32_t ta, uint32_t tile_saddr, int half,
                                              bool accumulate) {
     const uint64_t b = sdesc_sw128(tile_saddr, kChunkBytes, 1024);
 #pragma unroll
-    for (int q = 0; q < kBT / 32; ++q) {
-        const int kk = half * (kBT / 32) + q;
-        mma_ts(tacc, ta + packed_col(kk), b + kk * (2048 >> 4), BwdCfg<D>::kIdescAcc,
+    for (int q = 0; q < 4; ++q) {
+        const int kk = half * 4 + q;
+        mma_ts(tacc, ta + packed_col(q), b + kk * (2048 >> 4), BwdCfg<D>::kIdescAcc,
                (accumulate || kk > 0) ? 1u : 0u);
     }
 }
@@ -437,7 +443,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto entry = [&](int i) -> int32_t { return __ldg(lst + i); };
 
     if (threadIdx.x == 0) {
-        for (int b = 0; b < kNumBars; ++b) mbar_init(BAR(b), (b == kBarEw0 || b == kBarEw1) ? kEwThreads : 1);
+        for (int b = 0; b < kNumBars; ++b)
+            mbar_init(BAR(b), (b == kBarEw0 || b == kBarEw1) ? kEwThreads : (b == kBarDrain ? 2 : 1));
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -449,12 +456,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(g + L::kSlot);
-    // TMEM: accumulators first (dV, dK) or (dQ), then S-like and dP-like; the
-    // bf16 P / dS operands are written back over the first half of those
+    // TMEM: accumulators first (dV, dK) or (dQ), then two slots of 128
+    // columns, one per 64-column half of a pair: S-like in the first 64, dP-like
+    // in the other 64; the bf16 P / dS operands are written back over them
     const uint32_t tAcc0 = tmem, tAcc1 = tmem + D;
-    const uint32_t tS = tmem + (KV ? 2 * D : D), tdP = tS + kBT;
+    const uint32_t tSlot0 = tmem + (KV ? 2 * D : D);
+    auto slot = [&](int hv) -> uint32_t { return tSlot0 + 128u * (uint32_t)hv; };
 
-    if (warp == kCtlWarp) {
+    if (warp == kSdpWarp) {
+        // ------------------------------------------------------------ copies, S and dP
         if (lane == 0) {
             bool ok = true;
             int issued[2] = {0, 0}, seen[2] = {0, 0};  // per-buffer loads issued / waited for
@@ -477,6 +487,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 ++issued[b];
             };
+            // S and dP of the half hv of pair i into slot hv
+            auto issue_sdp = [&](int i, int hv) {
+                const int b = i & 1;
+                // KV: S^T = K_j Q_t^T, dP^T = V_j dO_t^T; else S = Q_t K_j^T, dP = dO_t V_j^T
+                mma_half<D>(slot(hv), base + L::kRes0, base + L::buf(b, 0) + hv * kHalfBytes);
+                mma_half<D>(slot(hv) + 64, base + L::kRes1, base + L::buf(b, 1) + hv * kHalfBytes);
+                mma_commit(BAR(kBarS0 + hv));
+            };
             if (n > 0) {
                 mbar_arrive_expect_tx(BAR(kBarRes), 2 * C::kTile);
                 for (int c = 0; c < D / 64; ++c) {
@@ -486,35 +504,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 c * 64, xrow, BAR(kBarRes), l2_policy_evict_first());
                 }
                 load_pair(0);
-            }
-            for (int i = 0; i < n && ok; ++i) {
-                const int b = i & 1;
-                // the previous pair is done: its TMEM operands and its buffer are free
-                if (i > 0 && !(ok = wait_bar(BAR(kBarPair), (i - 1) & 1u, abort_flag, A.status))) break;
-                if (i == 0 && !(ok = wait_bar(BAR(kBarRes), 0u, abort_flag, A.status))) break;
-                if (!(ok = wait_bar(BAR(kBarBuf0 + b), (i >> 1) & 1u, abort_flag, A.status))) break;
-                ++seen[b];
-                tc_fence_after();
-                // KV: S^T = K_j Q_t^T, dP^T = V_j dO_t^T; else S = Q_t K_j^T, dP = dO_t V_j^T
-                mma_sq<D>(tS, base + L::kRes0, base + L::buf(b, 0));
-                mma_sq<D>(tdP, base + L::kRes1, base + L::buf(b, 1));
-                mma_commit(BAR(kBarS));
-                // the next pair's copies go to the buffer the previous pair
-                // released, off the path from one pair's MMAs to the next
-                if (i + 1 < n) load_pair(i + 1);
-                // each half of the accumulations starts as soon as its 64 columns are written
-                for (int hv = 0; hv < 2 && ok; ++hv) {
-                    if (!(ok = wait_bar(BAR(kBarEw0 + hv), i & 1u, abort_flag, A.status))) break;
+                ok = wait_bar(BAR(kBarRes), 0u, abort_flag, A.status) &&
+                     wait_bar(BAR(kBarBuf0), 0u, abort_flag, A.status);
+                if (ok) {
+                    ++seen[0];
                     tc_fence_after();
-                    if (KV) {
-                        mma_acc_half<D>(tAcc0, tS, base + L::buf(b, 1), hv, i > 0);   // dV += P^T dO_t
-                        mma_acc_half<D>(tAcc1, tdP, base + L::buf(b, 0), hv, i > 0);  // dK += dS^T Q_t
-                    } else {
-                        mma_acc_half<D>(tAcc0, tS, base + L::buf(b, 0), hv, i > 0);   // dQ += dS K_j
-                    }
+                    issue_sdp(0, 0);
+                    issue_sdp(0, 1);
+                    if (n > 1) load_pair(1);
                 }
-                if (!ok) break;
-                mma_commit(BAR(kBarPair));
+            }
+            // S and dP of half hv of pair i + 1 go into slot hv once the
+            // accumulations of half hv of pair i have read it, so the next
+            // pair's products run while this pair's other half is in the
+            // elementwise step.
+            for (int i = 0; i + 1 < n && ok; ++i) {
+                for (int hv = 0; hv < 2 && ok; ++hv) {
+                    if (!(ok = wait_bar(BAR(kBarFree0 + hv), i & 1u, abort_flag, A.status))) break;
+                    if (hv == 0) {
+                        const int b1 = (i + 1) & 1;
+                        if (!(ok = wait_bar(BAR(kBarBuf0 + b1), ((i + 1) >> 1) & 1u, abort_flag, A.status))) break;
+                        ++seen[b1];
+                    }
+                    tc_fence_after();
+                    issue_sdp(i + 1, hv);
+                    // pair i's accumulations are done: its buffer takes pair i + 2
+                    if (hv == 1 && i + 2 < n) load_pair(i + 2);
+                }
             }
             if (!ok) {
                 // copies in flight must land before the CTA leaves
@@ -522,7 +538,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int b = 0; b < 2; ++b)
                     if (issued[b] > seen[b]) drain_wait(BAR(kBarBuf0 + b), (issued[b] - 1) & 1u);
             }
-            // every MMA this thread issued completes before TMEM is released
+            // every MMA of both issuers completes before TMEM is released
+            mma_commit(BAR(kBarDrain));
+            drain_wait(BAR(kBarDrain), 0u);
+        }
+        __syncwarp();
+    } else if (warp == kCtlWarp) {
+        // ------------------------------------------------------------ accumulations
+        if (lane == 0) {
+            bool ok = true;
+            // the accumulations over the half hv of pair i, from slot hv, as soon
+            // as the elementwise step has written it
+            for (int i = 0; i < n && ok; ++i) {
+                const int b = i & 1;
+                for (int hv = 0; hv < 2 && ok; ++hv) {
+                    if (!(ok = wait_bar(BAR(kBarEw0 + hv), i & 1u, abort_flag, A.status))) break;
+                    tc_fence_after();
+                    if (KV) {
+                        mma_acc_half<D>(tAcc0, slot(hv), base + L::buf(b, 1), hv, i > 0);       // dV += P^T dO_t
+                        mma_acc_half<D>(tAcc1, slot(hv) + 64, base + L::buf(b, 0), hv, i > 0);  // dK += dS^T Q_t
+                    } else {
+                        mma_acc_half<D>(tAcc0, slot(hv), base + L::buf(b, 0), hv, i > 0);       // dQ += dS K_j
+                    }
+                    mma_commit(BAR(kBarFree0 + hv));
+                }
+            }
             mma_commit(BAR(kBarDrain));
             drain_wait(BAR(kBarDrain), 0u);
         }
@@ -547,26 +587,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int32_t e_i = entry(i);
             const int mk = e_i & 15;
             const Rows ry = entry_rows(e_i);
-            if (!(ok = wait_warp(BAR(kBarS), i & 1u, abort_flag, A.status))) break;
-            // the pair's copies are complete and visible here
-            if (!(ok = wait_warp(BAR(kBarBuf0 + b), (i >> 1) & 1u, abort_flag, A.status))) break;
-            tc_fence_after();
-            // operands summed over their rows next get their padding rows cleared
-            // (before the first half's arrival): Q_t and dO_t (KV), K_j (dQ)
-            const bool zr = !ry.valid(r);
-            if (zr && h == 0) zero_row<D>(g + L::buf(b, 0), r);
-            if (zr && KV && h == 1) zero_row<D>(g + L::buf(b, 1), r);
             const float2 *s_nl2 = reinterpret_cast<const float2 *>(g + L::kVec + b * 2 * kBT * 4);
             const float2 *s_ndl = s_nl2 + kBT / 2;
 #pragma unroll 1
             for (int hv = 0; hv < 2; ++hv) {
-                const int c0 = hv * 64 + h * kEwCols;  // this thread's columns of the half
-                const int nyh = hv ? ry.hi : ry.lo;     // valid columns of this half
+                if (!(ok = wait_warp(BAR(kBarS0 + hv), i & 1u, abort_flag, A.status))) break;
+                // the pair's copies are complete and visible here
+                if (hv == 0 && !(ok = wait_warp(BAR(kBarBuf0 + b), (i >> 1) & 1u, abort_flag, A.status))) break;
+                tc_fence_after();
+                // padding rows of this half of the operands summed over their rows
+                // (Q_t and dO_t for KV, K_j for dQ) are cleared before the half's
+                // accumulations; the S/dP MMAs of the other half do not read them
+                const int pr = hv * 64 + (threadIdx.x & 63), grp = threadIdx.x >> 6;
+                const bool zr = !ry.valid(pr) && (grp == 0 || (KV && grp == 1));
+                if (zr) zero_row<D>(g + L::buf(b, grp), pr);
+                const uint32_t ts = slot(hv) + tl + h * kEwCols;  // this thread's S columns of the slot
+                const int c0 = hv * 64 + h * kEwCols;              // the pair column of the first
+                const int nyh = hv ? ry.hi : ry.lo;                // valid columns of this half
                 uint32_t pw[kEwCols / 2], dw[kEwCols / 2];
                 if (!BM || ((mk >> (2 * ra + hv)) & 1)) {  // warp-uniform
                     float sv[kEwCols], dp[kEwCols];
-                    ld_cols(tS + tl + c0, sv);
-                    ld_cols(tdP + tl + c0, dp);
+                    ld_cols(ts, sv);
+                    ld_cols(ts + 64, dp);
                     // only a partner half with padding needs the column mask
                     if (nyh >= h * kEwCols + kEwCols)
                         ew_cols<KV, false>(sv, dp, pw, dw, c0, 0, c1, s_nl2, s_ndl, nl2_r, ndl_r);
@@ -578,16 +620,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int w = 0; w < kEwCols / 2; ++w) pw[w] = dw[w] = 0u;
                 }
                 // bf16 pairs back over the first half of the columns just read
-                if (KV) st_cols(tS + tl + c0, pw);
-                st_cols((KV ? tdP : tS) + tl + c0, dw);
-                if (hv == 0 && zr) fence_proxy_async_smem();  // this thread's zeroed rows, for the MMAs
+                if (KV) st_cols(ts, pw);
+                st_cols(KV ? ts + 64 : ts, dw);
+                if (zr) fence_proxy_async_smem();  // this thread's zeroed row, for the MMAs
                 tmem_wait_st();
                 tc_fence_before();
                 mbar_arrive(BAR(kBarEw0 + hv));
             }
+            if (!ok) break;
         }
         // ------------------------------------------------------------ epilogue
-        if (ok && n > 0 && !wait_warp(BAR(kBarPair), (n - 1) & 1u, abort_flag, A.status)) ok = false;
+        // the last accumulation (of the last pair's second half) is done
+        if (ok && n > 0 && !wait_warp(BAR(kBarFree1), (n - 1) & 1u, abort_flag, A.status)) ok = false;
         if (ok) {
             tc_fence_after();
             const bool live = n > 0 && rx.valid(r);
