@@ -29,13 +29,17 @@
 //   bwd_kernel<D, true>   one CTA per (batch, head, key tile j): K_j and V_j
 //                  stay in shared memory; the query tiles t that select j
 //                  stream through two buffers (the next pair's copies overlap
-//                  this pair's work).  S^T = K_j Q_t^T and dP^T = V_j dO_t^T
-//                  go to TMEM; eight elementwise warps (two threads per key
-//                  row) write P^T and dS^T as bf16 back into TMEM over the
-//                  columns they read, one 64-column half after the other;
+//                  this pair's work).  A pair is done in two 64-column halves
+//                  (64 of the query tile's rows), each in its own TMEM slot:
+//                  S^T = K_j Q_t^T and dP^T = V_j dO_t^T of the half go to the
+//                  slot; eight elementwise warps (two threads per key row)
+//                  write P^T and dS^T as bf16 back over the columns they read;
 //                  dV += P^T dO_t and dK += dS^T Q_t accumulate in TMEM with
-//                  the A operand taken from TMEM, the first half's MMAs
-//                  running while the second half is computed.
+//                  the A operand taken from the slot.  One thread issues the
+//                  accumulations, another the copies and S/dP, which go into
+//                  a slot as soon as the previous pair's accumulations have
+//                  read it: the next pair's products overlap this pair's
+//                  elementwise step.
 //   bwd_kernel<D, false>  one CTA per (batch, head, query tile t): Q_t and dO_t
 //                  stay; for every selected key tile, S and dP again, dS back
 //                  into TMEM, dQ += dS K_j.  Recomputing S and dP keeps dQ
@@ -401,10 +405,10 @@ __device__ __forceinline__ void mma_acc_half(uint32_t tacc, uint32_t ta, uint32_
 }
 
 // Common shape of both kernels: one resident tile pair, a list of partner
-// tiles streamed through two buffers, per pair two 128 x 128 products into
-// TMEM (S-like and dP-like), an elementwise step by 256 threads that writes
-// bf16 operands back into TMEM in two column halves, and one or two
-// accumulations from TMEM, each issued half by half as the halves are ready.
+// tiles streamed through two buffers, per pair and 64-column half two
+// 128 x 64 products into a TMEM slot (S-like and dP-like), an elementwise step
+// by 256 threads that writes bf16 operands back into the slot, and one or two
+// accumulations from it.
 // BM: pairs carry block masks (64-token tiles); otherwise every mask is full.
 template <int D, bool KV, bool BM>
 __global__ void __launch_bounds__(kThreads, 1)
