@@ -106,6 +106,32 @@ def test_workspace_size(vsa):
     assert vsa.vsa_block_sparse_workspace_size(d) == 256 + 4 * 16 * 16
 
 
+def _align256(x):
+    return (x + 255) // 256 * 256
+
+
+@pytest.mark.parametrize("B,H,NT,T,D,max_kv", [(1, 6, 244, 128, 128, 244), (2, 8, 63, 64, 64, 32),
+                                              (1, 2, 3, 256, 128, 3), (1, 1, 1, 64, 64, 0)])
+def test_bwd_workspace_size(vsa, B, H, NT, T, D, max_kv):
+    """The backward workspace: -delta and -lse*log2(e) per row of whole 128-row
+    kernel tiles, partner counts and lists, transposed offsets and lists."""
+    d = vsa.make_dims(B, H, NT, T, D, max_kv)
+    BH = B * H
+    NTk = (NT + 1) // 2 if T == 64 else (NT if T == 128 else 2 * NT)
+    maxlen = max(1, min(NTk, (1 if T == 128 else 2) * max(max_kv, 1)))
+    Spk = NTk * 128
+    lists = 4 * BH * NTk * maxlen
+    want = (256 + 2 * _align256(4 * BH * Spk) + _align256(4 * BH * NTk) + _align256(lists)
+            + _align256(4 * BH * (NTk + 1)) + _align256(lists))
+    assert vsa.vsa_block_sparse_bwd_workspace_size(d) == want
+
+
+def test_bwd_workspace_size_invalid(vsa):
+    assert vsa.vsa_block_sparse_bwd_workspace_size(vsa.make_dims(1, 1, 4, 96, 64, 2)) == 0    # tile
+    assert vsa.vsa_block_sparse_bwd_workspace_size(vsa.make_dims(1, 1, 4, 128, 96, 2)) == 0   # head_dim
+    assert vsa.vsa_block_sparse_bwd_workspace_size(vsa.make_dims(256, 256, 4, 64, 64, 2)) == 0  # B*H
+
+
 def test_layout_argument_errors(vsa):
     P = ctypes.c_void_p
     L = vsa.library().vsa_tile_layout
