@@ -16,7 +16,8 @@ namespace vsa {
 namespace {
 
 constexpr int kLayoutThreads = 256;
-constexpr int kRowsInFlight = 2;
+constexpr int kRowsInFlight = 2;   // layout: three tensors, so six loads in flight per thread
+constexpr int kUntileRows = 4;     // un-tiling: two loads per row
 
 __global__ void __launch_bounds__(kLayoutThreads)
     layout_kernel(const LayoutParams P, int rows_per_block, int hv_per_block) {
@@ -84,12 +85,12 @@ __global__ void __launch_bounds__(kLayoutThreads)
     const int64_t tok_b = (int64_t)b * P.S * HV + hv;  // + s*HV
     const int64_t step = (int64_t)gridDim.x * rows_per_block;
     bool bad = false;
-    for (int64_t row0 = (int64_t)blockIdx.x * rows_per_block + rl; row0 < Sp; row0 += step * kRowsInFlight) {
-        int64_t rows[kRowsInFlight];
-        int32_t tok[kRowsInFlight];
-        uint4 o[kRowsInFlight], gt[kRowsInFlight];
+    for (int64_t row0 = (int64_t)blockIdx.x * rows_per_block + rl; row0 < Sp; row0 += step * kUntileRows) {
+        int64_t rows[kUntileRows];
+        int32_t tok[kUntileRows];
+        uint4 o[kUntileRows], gt[kUntileRows];
 #pragma unroll
-        for (int i = 0; i < kRowsInFlight; ++i) {
+        for (int i = 0; i < kUntileRows; ++i) {
             rows[i] = row0 + i * step;
             tok[i] = rows[i] < Sp ? __ldg(P.row_to_token + rows[i]) : -1;
             if (tok[i] >= P.S || tok[i] < -1) {
@@ -102,7 +103,7 @@ __global__ void __launch_bounds__(kLayoutThreads)
             }
         }
 #pragma unroll
-        for (int i = 0; i < kRowsInFlight; ++i) {
+        for (int i = 0; i < kUntileRows; ++i) {
             if (tok[i] < 0) continue;
             uint4 v = o[i];
             if (P.gate) {
