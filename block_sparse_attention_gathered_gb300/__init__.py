@@ -70,6 +70,7 @@ def _load() -> ctypes.CDLL:
         "vsa_coarse_select_workspace_size": ([dims_p], sz),
         "vsa_coarse_select": ([P, P, P, i32, P, P, dims_p, P, sz, P], i32),
         "vsa_check_device_status": ([P], i32),
+        "vsa_wait_probe": ([i32, ctypes.c_uint32, P], i32),
         "vsa_last_route": ([ctypes.POINTER(VsaRoute)], i32),
         "vsa_status_string": ([i32], ctypes.c_char_p),
         "vsa_version": ([], i32),
@@ -82,9 +83,9 @@ def _load() -> ctypes.CDLL:
 
 _lib = _load()
 EXPORTED = ("vsa_block_sparse_workspace_size", "vsa_block_sparse_fwd", "vsa_block_sparse_fwd_noalloc",
-            "vsa_block_sparse_bwd_workspace_size", "vsa_block_sparse_bwd", "vsa_tile_layout", "vsa_untile", "vsa_coarse_select_workspace_size", "vsa_coarse_select",
-            "vsa_validate_indices", "vsa_check_device_status", "vsa_last_route",
-            "vsa_status_string", "vsa_version")
+            "vsa_block_sparse_bwd_workspace_size", "vsa_block_sparse_bwd", "vsa_tile_layout", "vsa_untile",
+            "vsa_coarse_select_workspace_size", "vsa_coarse_select", "vsa_validate_indices",
+            "vsa_check_device_status", "vsa_wait_probe", "vsa_last_route", "vsa_status_string", "vsa_version")
 
 
 def library() -> ctypes.CDLL:
@@ -112,6 +113,12 @@ def vsa_status_string(status: int) -> str:
 
 def vsa_version() -> int:
     return int(_lib.vsa_version())
+
+
+def vsa_wait_probe(arrive: bool, limit_us: int, stream=None) -> int:
+    """Launches the bounded-wait probe; returns the launch status (the
+    timeout, if any, shows in ``vsa_check_device_status``)."""
+    return int(_lib.vsa_wait_probe(1 if arrive else 0, int(limit_us), _stream(stream)))
 
 
 def vsa_block_sparse_workspace_size(dims: VsaDims) -> int:

@@ -17,7 +17,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libvsa.so")
-SOURCES = ["vsa_api.cu", "vsa_attn.cu", "vsa_bwd.cu", "vsa_layout.cu", "vsa_noalloc.cu", "vsa_select.cu"]
+SOURCES = ["vsa_api.cu", "vsa_attn.cu", "vsa_bwd.cu", "vsa_check.cu", "vsa_layout.cu", "vsa_noalloc.cu",
+           "vsa_select.cu"]
 GENCODE = "arch=compute_103a,code=sm_103a"
 
 

@@ -229,7 +229,7 @@ using namespace vsa;
 
 extern "C" {
 
-int32_t vsa_version(void) { return 1001; }
+int32_t vsa_version(void) { return 1002; }
 
 const char *vsa_status_string(vsa_status s) {
     switch (s) {
@@ -616,6 +616,19 @@ vsa_status vsa_coarse_select(const void *q, const void *k, const int32_t *block_
     t_route.block = 32 * select_warps(p.NT, p.D);
     t_route.work_items = (int64_t)p.B * p.H * p.NT;
     t_route.smem_bytes = (int32_t)select_smem_bytes(p.NT, p.D, rows);
+    return VSA_OK;
+}
+
+vsa_status vsa_wait_probe(int32_t arrive, uint32_t limit_us, vsa_stream_t stream) {
+    if (limit_us < 1 || limit_us > 2000000u) return VSA_ERR_ARG;
+    int dev = 0;
+    vsa_status st = current_device(&dev);
+    if (st != VSA_OK) return st;
+    if (launch_wait_probe(arrive, (uint64_t)limit_us * 1000ull, g_dev[dev].status_ptr.load(std::memory_order_acquire),
+                          reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return VSA_ERR_CUDA;
+    }
     return VSA_OK;
 }
 

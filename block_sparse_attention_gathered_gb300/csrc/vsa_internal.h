@@ -135,4 +135,7 @@ size_t select_smem_bytes(int NT, int D, int rows);
 cudaError_t select_prepare();
 cudaError_t launch_select(const SelectParams &p, cudaStream_t stream);
 
+// Bounded-wait probe (vsa_check.cu).
+cudaError_t launch_wait_probe(int32_t arrive, uint64_t limit_ns, int32_t *status, cudaStream_t stream);
+
 }  // namespace vsa

@@ -30,9 +30,11 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
 }
 
 // Bounded wait on an mbarrier phase.  Returns false when the CTA is aborting
-// (another role gave up) or when this wait itself ran past the limit.
+// (another role gave up) or when this wait itself ran past the limit; in the
+// latter case it raises the CTA's abort flag and sets the timeout bit of the
+// device status word.
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                         int32_t *status) {
+                                         int32_t *status, uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     uint64_t t0 = 0;
     for (uint32_t it = 1;; ++it) {
@@ -44,7 +46,7 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
             const uint64_t now = globaltimer_ns();
             if (t0 == 0) {
                 t0 = now;
-            } else if (now - t0 > kWaitLimitNs) {
+            } else if (now - t0 > limit_ns) {
                 *abort_flag = 1;
                 atomicOr(status, kFlagTimeout);
                 return false;
@@ -57,8 +59,8 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
 // .sync.aligned tcgen05 instructions that follow are never reached by part of
 // a warp.
 __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                          int32_t *status) {
-    return __all_sync(0xffffffffu, wait_bar(bar, parity, abort_flag, status));
+                                          int32_t *status, uint64_t limit_ns = kWaitLimitNs) {
+    return __all_sync(0xffffffffu, wait_bar(bar, parity, abort_flag, status, limit_ns));
 }
 
 // Wait used only while draining after an abort: ignores the abort flag, gives

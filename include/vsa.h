@@ -284,6 +284,20 @@ vsa_status vsa_coarse_select(const void *q, const void *k, const int32_t *block_
  * the last check). */
 vsa_status vsa_check_device_status(vsa_stream_t stream);
 
+/*
+ * Probe of the failure path behind VSA_ERR_TIMEOUT (sm_121a hardening commit:
+ * failures are reported, never left as a hung GPU).  Launches one warp that
+ * waits, with the same bounded wait every kernel uses, on a barrier phase
+ * that completes only when `arrive` is nonzero.  With arrive == 0 nothing
+ * completes it: after limit_us microseconds the wait gives up, sets
+ * VSA_ERR_TIMEOUT in the device status word (read it with
+ * vsa_check_device_status) and the kernel returns; the context stays usable.
+ *   arrive     nonzero: the phase completes and the status word is untouched
+ *   limit_us   1 .. 2000000 (the kernels' own limit is about 2 s)
+ * Returns VSA_ERR_ARG for a limit outside that range; asynchronous otherwise.
+ */
+vsa_status vsa_wait_probe(int32_t arrive, uint32_t limit_us, vsa_stream_t stream);
+
 /* Route of the last successful launch on the calling host thread. */
 vsa_status vsa_last_route(vsa_route *route);
 

@@ -38,7 +38,7 @@ def test_exports_every_declared_symbol(vsa):
     for name in declared:
         assert hasattr(lib, name), name
     assert set(declared) == set(vsa.EXPORTED)
-    assert vsa.vsa_version() == 1001
+    assert vsa.vsa_version() == 1002
 
 
 def test_status_strings(vsa):
@@ -194,3 +194,10 @@ def test_no_device_is_an_error_not_a_launch(vsa):
     st = _fwd(vsa, vsa.make_dims(1, 2, 4, 64, 64, 2))
     assert st in (vsa.VSA_ERR_CUDA, vsa.VSA_ERR_ARCH)
     assert vsa.vsa_check_device_status(0) in (vsa.VSA_ERR_CUDA, vsa.VSA_ERR_ARCH)
+
+
+def test_wait_probe_argument_errors(vsa):
+    # limit checked before any device work (no GPU here)
+    assert vsa.library().vsa_wait_probe(0, 0, None) == vsa.VSA_ERR_ARG
+    assert vsa.library().vsa_wait_probe(0, 2000001, None) == vsa.VSA_ERR_ARG
+    assert vsa.library().vsa_wait_probe(0, 1000, None) in (vsa.VSA_ERR_CUDA, vsa.VSA_ERR_ARCH)
