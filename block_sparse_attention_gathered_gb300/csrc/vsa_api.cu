@@ -109,9 +109,14 @@ int64_t items_per_seq(const vsa_dims *d) { return ((int64_t)d->num_tiles * d->ti
 
 constexpr size_t kWsHeader = 256;  // work counter, padded
 
+// Work items of the last, partly filled wave may run as two one-unit items
+// on two CTAs (at most kMaxSplit of them): the order list grows by one entry
+// per split item.
+constexpr int kMaxSplit = 256;
+
 size_t workspace_bytes_for(const vsa_dims *d) {
     const int64_t n_items = (int64_t)d->B * d->H * items_per_seq(d);
-    return kWsHeader + (size_t)n_items * sizeof(int32_t);
+    return kWsHeader + (size_t)(n_items + kMaxSplit) * sizeof(int32_t);
 }
 
 vsa_status encode_rows_map(CUtensorMap *m, const void *ptr, int64_t rows, int D, int box_rows) {
@@ -136,7 +141,7 @@ constexpr int kSchedThreads = 1024;
 
 __global__ void __launch_bounds__(kSchedThreads)
     schedule_kernel(const int32_t *__restrict__ q2k_num, int NT, int T, int max_kv, int G, int n_items, int bins,
-                    int32_t *__restrict__ order, int32_t *__restrict__ counter) {
+                    int split, int32_t *__restrict__ order, int32_t *__restrict__ counter) {
     extern __shared__ int32_t sh[];
     int32_t *hist = sh;          // [bins], indexed by descending rank
     int32_t *cursor = sh + bins;  // [bins]
@@ -191,7 +196,20 @@ __global__ void __launch_bounds__(kSchedThreads)
         pos += hist[i];
     }
     __syncthreads();
-    for (int i = tid; i < n_items; i += kSchedThreads) order[atomicAdd(&cursor[rank_of(i)], 1)] = i;
+    // entries are item << 2 | units: 0 both; the last `split` positions (the
+    // shortest items) become two entries each, unit 0 only (1) and unit 1
+    // only (2), so the last partial wave spreads over twice the CTAs
+    const int whole = n_items - split;
+    for (int i = tid; i < n_items; i += kSchedThreads) {
+        const int pos = atomicAdd(&cursor[rank_of(i)], 1);
+        if (pos < whole) {
+            order[pos] = i << 2;
+        } else {
+            const int q = whole + 2 * (pos - whole);
+            order[q] = (i << 2) | 1;
+            order[q + 1] = (i << 2) | 2;
+        }
+    }
     if (tid == 0) *counter = 0;
 }
 
@@ -297,8 +315,14 @@ vsa_status vsa_block_sparse_fwd(const void *q, const void *k, const void *v, con
     int32_t *order = reinterpret_cast<int32_t *>(reinterpret_cast<char *>(workspace) + kWsHeader);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
+    // One persistent CTA per SM.  When the last wave would fill at most half
+    // of them, its items are split into one-unit items.
+    const int sms = dc.sm_count.load(std::memory_order_acquire);
+    const int grid = n_items < sms ? n_items : sms;
+    const int rem = n_items > grid ? n_items % grid : 0;
+    const int split = (rem > 0 && 2 * rem <= grid && rem <= kMaxSplit) ? rem : 0;
     schedule_kernel<<<1, kSchedThreads, 2 * bins * sizeof(int32_t), s>>>(q2k_num, NT, T, dims->max_kv, G, n_items,
-                                                                        bins, order, counter);
+                                                                        bins, split, order, counter);
     if (cudaGetLastError() != cudaSuccess) return VSA_ERR_CUDA;
 
     AttnParams p;
@@ -315,12 +339,10 @@ vsa_status vsa_block_sparse_fwd(const void *q, const void *k, const void *v, con
     p.max_kv = dims->max_kv;
     p.G = G;
     p.bm_words = (NT * sub + 31) / 32;
-    p.n_items = n_items;
+    p.n_items = n_items + split;
     p.Sp = Sp;
     const float scale = dims->scale > 0.f ? dims->scale : 1.0f / std::sqrt((float)D);
     p.scale_log2 = scale * 1.4426950408889634f;
-    const int sms = dc.sm_count.load(std::memory_order_acquire);
-    const int grid = n_items < sms ? n_items : sms;
     if (launch_attn(Tk, D, tm_q, tm_k, tm_v, p, grid, s) != cudaSuccess) return VSA_ERR_CUDA;
 
     const AttnLaunchInfo info = attn_launch_info(Tk, D, p.bm_words);

@@ -266,7 +266,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             int slot = 0;
             if (lane == 0) slot = atomicAdd(P.work_counter, 1);
             slot = __shfl_sync(0xffffffffu, slot, 0);
-            const int item = (slot < P.n_items) ? __ldg(P.order + slot) : -1;
+            // order entries: work item << 2 | which units run (0 both, 1 or 2 one)
+            const int entry = (slot < P.n_items) ? __ldg(P.order + slot) : -1;
+            const int item = entry < 0 ? -1 : entry >> 2, mode = entry < 0 ? 0 : entry & 3;
             uint32_t *bmp = bm + p * 4 * W;
             int bad = 0;
             if (item >= 0) {
@@ -280,6 +282,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 for (int s = 0; s < 4; ++s) {
                     const int t = tile_of_slot<T>(g, s);
                     if (t < 0 || t >= NT) continue;
+                    if (mode != 0 && mode != (s >> 1) + 1) continue;  // unit s/2 runs elsewhere
                     const int64_t row = (int64_t)bh * NTc + t / sub;
                     int K = __ldg(P.q2k_num + row);
                     if (K < 0 || K > P.max_kv) {
@@ -302,7 +305,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         }
                     }
                 }
-                if (lane == 0) hdr[p * 4] = item;
+                if (lane == 0) {
+                    hdr[p * 4] = item;
+                    hdr[p * 4 + 1] = mode;
+                }
             } else if (lane == 0) {
                 hdr[p * 4] = -1;
             }
@@ -555,6 +561,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             const int p = it & 1;
             if (!wait_warp(BAR(BI.bm_full(p)), (it >> 1) & 1u, abort_flag, P.status)) break;
             const int item = hdr[p * 4];
+            const int mode = hdr[p * 4 + 1];
             if (item < 0) break;
             const uint32_t *bmp = bm + p * 4 * W;
             const int bh = item / P.G, g = item - (item / P.G) * P.G;
@@ -669,7 +676,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             }
             float l = l0 + l1;
             l += __shfl_xor_sync(0xffffffffu, l, 16);
-            const bool write_row = t < NT;
+            // a unit that another CTA runs (a split item) leaves its rows alone
+            const bool write_row = t < NT && (mode == 0 || mode == u + 1);
             const bool valid = r < n_t;
             const bool use_o = (n_mine > 0) && valid && (l != 0.f);  // NaN l keeps use_o: NaN row
             const float inv = use_o ? 1.f / l : 0.f;

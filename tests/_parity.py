@@ -13,10 +13,13 @@ import torch
 
 MAX_ABS = 2e-2
 REL_RMS = 5e-3
-# LSE: the scores are accumulated in FP32 over D products, so their error grows
-# with the score's size (about D * 2^-24 * sum|q_d k_d|); bound it as an
-# absolute part plus a part relative to |lse|.
-LSE_ABS = 2e-3
+# LSE = m + log(l) with l the sum of the bf16-rounded P that P V uses (so the
+# output weights P / l are exactly normalised).  One bf16 rounding is at most
+# 2^-8 relative, so when one key dominates a row log(l) is off by up to
+# ln(1 + 2^-8) = 3.9e-3.  The scores are accumulated in FP32 over D products,
+# so their error grows with the score's size (about D * 2^-24 * sum|q_d k_d|):
+# the bound is an absolute part plus a part relative to |lse|.
+LSE_ABS = 4e-3
 LSE_REL = 8e-6
 
 RESULTS = []  # (label, max_abs, rel_rms, lse_max_abs) of every passing comparison

@@ -129,15 +129,16 @@ def test_dense_limit_sampled(vsa, oracle_mod):
     assert r["grid"] == min(6 * 122, torch.cuda.get_device_properties(0).multi_processor_count)
 
 
-def _random_case(seed, B, H, NT, T, D, pad="naninf", empty_frac=0.15, full=False):
+def _random_case(seed, B, H, NT, T, D, pad="naninf", empty_frac=0.15, full=False, max_kv=None):
     g = torch.Generator().manual_seed(seed)
+    max_kv = NT if max_kv is None else max_kv
     bs = torch.full((NT,), T, dtype=torch.int32) if full else torch.randint(1, T + 1, (NT,), generator=g).int()
     if not full:
         bs[torch.rand(NT, generator=g) < 0.1] = 0           # a few empty tiles
         bs[NT // 2] = T
-    counts = torch.randint(0, NT + 1, (B, H, NT), generator=g).int()
+    counts = torch.randint(0, max_kv + 1, (B, H, NT), generator=g).int()
     counts[torch.rand((B, H, NT), generator=g) < empty_frac] = 0
-    idx = W.random_selection(g, B, H, NT, counts, NT)
+    idx = W.random_selection(g, B, H, NT, counts, max_kv)
     q, k, v = (torch.randn((B, H, NT * T, D), generator=g).to(torch.bfloat16) for _ in range(3))
     if not full:
         q, k, v = (W.pad_tile_major(x, bs, T, pad) for x in (q, k, v))
@@ -161,6 +162,24 @@ def test_many_waves(vsa, oracle_mod):
     assert vsa.vsa_last_route()["work_items"] == 4 * 48 * 3
     units = PT.sample_units(w.B, w.H, w.NT, 64, seed=8)
     _check(w, out, lse, refs, oracle_mod, units, "waves")
+
+
+@pytest.mark.parametrize("T", [64, 128, 256])
+def test_split_last_wave(vsa, oracle_mod, T):
+    """One work item per SM plus a few: the last wave's items run as one-unit
+    items on two CTAs each, and each CTA writes only its unit's rows."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    n_items = sms + 5
+    NT = n_items * 256 // T
+    w = _random_case(300 + T, 1, 1, NT, T, 64, max_kv=3)
+    (q, k, v), refs = _to_tile_major(w, vsa, oracle_mod)
+    out, lse = _run(vsa, q, k, v, w)
+    assert vsa.vsa_last_route()["work_items"] == n_items
+    _check(w, out, lse, refs, oracle_mod, list(range(w.B * w.H * w.NT)), f"split T{T}")
+    # bit-identical across runs, although which items are split may differ
+    # (items of equal length take their places in any order)
+    again, _ = _run(vsa, q, k, v, w)
+    assert torch.equal(out.view(torch.int16), again.view(torch.int16))
 
 
 def test_all_empty_and_zero_max_kv(vsa):

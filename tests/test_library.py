@@ -95,15 +95,16 @@ def test_tile_256_limits(vsa):
     assert _fwd(vsa, vsa.make_dims(1, 2, 4097, 256, 128, 2)) == vsa.VSA_ERR_LIMITS
     assert _fwd(vsa, vsa.make_dims(1, 2, 4, 512, 128, 2)) == vsa.VSA_ERR_ARG
     # one 256-row work item per 256-token tile
-    assert vsa.vsa_block_sparse_workspace_size(vsa.make_dims(2, 3, 10, 256, 64, 4)) == 256 + 4 * 6 * 10
+    assert vsa.vsa_block_sparse_workspace_size(vsa.make_dims(2, 3, 10, 256, 64, 4)) == 256 + 4 * (6 * 10 + 256)
 
 
 def test_workspace_size(vsa):
-    # header (256 bytes) + one int32 per 256-query-row work item
+    # header (256 bytes) + one int32 per 256-query-row work item, + 256 for
+    # items of a partial last wave split into one-unit items
     d = vsa.make_dims(1, 6, 244, 128, 128, 244)
-    assert vsa.vsa_block_sparse_workspace_size(d) == 256 + 4 * 6 * 122
+    assert vsa.vsa_block_sparse_workspace_size(d) == 256 + 4 * (6 * 122 + 256)
     d = vsa.make_dims(2, 8, 63, 64, 64, 31)
-    assert vsa.vsa_block_sparse_workspace_size(d) == 256 + 4 * 16 * 16
+    assert vsa.vsa_block_sparse_workspace_size(d) == 256 + 4 * (16 * 16 + 256)
 
 
 def _align256(x):
