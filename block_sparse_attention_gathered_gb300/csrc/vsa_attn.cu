@@ -148,8 +148,9 @@ __device__ __forceinline__ bool wait_count(uint32_t addr, uint32_t target, volat
                                            int32_t *status) {
     uint64_t t0 = 0;
     for (uint32_t it = 0;; ++it) {
+        // tight polling: the S hand-off is on the critical path (measured
+        // 2.17 vs 2.22 ms dense against a 32 ns sleep between polls)
         if ((int32_t)(ld_acquire(addr) - target) >= 0) return true;
-        __nanosleep(32);
         if ((it & 63u) == 63u) {
             if (*abort_flag) return false;
             const uint64_t now = globaltimer_ns();
@@ -457,7 +458,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 auto pv = [&]() -> bool {
                     if (!wait_bar(BAR(pend_tail ? BI.vz(pend_v) : BI.kv_full(pend_v)), pend_ph, abort_flag, P.status))
                         return false;
-                    if (!wait_bar(BAR(BI.p_full(u)), pcnt & 1u, abort_flag, P.status)) return false;
+                    if (!wait_bar_spin(BAR(BI.p_full(u)), pcnt & 1u, abort_flag, P.status)) return false;
                     ++pcnt;
                     tc_fence_after();
                     const uint64_t b = dv + pend_v * kStage16;

@@ -55,6 +55,28 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
     }
 }
 
+// Same bound, but polling without sleeping: for a single thread whose wait
+// sits on the critical path (the MMA issuer waiting for P), where the wake-up
+// delay of a sleeping wait costs more than the issue slots polling takes.
+__device__ __forceinline__ bool wait_bar_spin(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                              int32_t *status) {
+    uint64_t t0 = 0;
+    for (uint32_t it = 0;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 255u) == 255u) {
+            if (*abort_flag) return false;
+            const uint64_t now = globaltimer_ns();
+            if (t0 == 0) {
+                t0 = now;
+            } else if (now - t0 > kWaitLimitNs) {
+                *abort_flag = 1;
+                atomicOr(status, kFlagTimeout);
+                return false;
+            }
+        }
+    }
+}
+
 // Warp-uniform form: every lane of the warp gets the same answer, so the
 // .sync.aligned tcgen05 instructions that follow are never reached by part of
 // a warp.
