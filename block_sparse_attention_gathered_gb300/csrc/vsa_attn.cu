@@ -495,7 +495,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         if ((mw >> b) & 1u) {
                             // S first: it needs only K and the softmax having loaded
                             // the previous S; then the pending P V.
-                            if (!(ok = wait_bar(BAR(BI.kv_full(kst)), kph, abort_flag, P.status))) break;
+                            if (!(ok = wait_bar_spin(BAR(BI.kv_full(kst)), kph, abort_flag, P.status))) break;
                             // every earlier S tile has left the shared S buffer
                             if (!(ok = wait_count(sFree, (uint32_t)kUnitWarps * g, abort_flag, P.status))) break;
                             tc_fence_after();
