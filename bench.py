@@ -436,7 +436,9 @@ def run_ours(args, cfg):
             "attn_ms": attn_avg, "layout_ms": lay_avg,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                          "frac": achieved / peak, "traffic": traffic,
-                         "peak_source": f"{src} bf16 burst (cuBLAS)", "kernel": f"attn_fwd_kernel<{min(T, 128)},{D}>"},
+                         "peak_source": f"{src} bf16 burst (cuBLAS)",
+                         "kernel": f"attn_fwd_kernel<{min(T, 128)},{D},"
+                                   f"{'paired' if route.get('layout') == vsa.VSA_LAYOUT_PAIRED else 'split'}>"},
             "layout_roofline": {"bound": "hbm", "achieved": lay_gbs, "peak": hbm, "unit": "GB/s",
                                 "frac": lay_gbs / hbm, "bytes": layout_bytes(w),
                                 "peak_source": f"{src} HBM copy", "kernel": "layout_kernel"},

@@ -26,6 +26,7 @@ VSA_OK, VSA_ERR_ARG, VSA_ERR_ALIGN, VSA_ERR_LIMITS, VSA_ERR_ARCH = 0, -1, -2, -3
 VSA_ERR_CUDA, VSA_ERR_TIMEOUT, VSA_ERR_INDEX, VSA_ERR_WORKSPACE = -5, -6, -7, -8
 VSA_KERNEL_NONE, VSA_KERNEL_ATTN_TCGEN05, VSA_KERNEL_LAYOUT, VSA_KERNEL_VALIDATE = 0, 1, 2, 3
 VSA_KERNEL_SELECT, VSA_KERNEL_UNTILE, VSA_KERNEL_BWD = 4, 5, 6
+VSA_LAYOUT_SPLIT, VSA_LAYOUT_PAIRED = 0, 1  # vsa_route.layout: MMA-issue layout of the attention kernel
 VSA_MAX_BATCH_HEADS, VSA_MAX_TILES = 65535, 8192
 
 
@@ -39,7 +40,7 @@ class VsaRoute(ctypes.Structure):
     _fields_ = [("kernel", ctypes.c_int32), ("tile", ctypes.c_int32), ("head_dim", ctypes.c_int32),
                 ("grid", ctypes.c_int32), ("block", ctypes.c_int32), ("stages", ctypes.c_int32),
                 ("work_items", ctypes.c_int64), ("sort_bins", ctypes.c_int32),
-                ("smem_bytes", ctypes.c_int32)]
+                ("smem_bytes", ctypes.c_int32), ("layout", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
     def as_dict(self):
         return {k: getattr(self, k) for k, _ in self._fields_}

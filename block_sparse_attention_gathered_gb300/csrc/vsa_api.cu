@@ -343,7 +343,14 @@ vsa_status vsa_block_sparse_fwd(const void *q, const void *k, const void *v, con
     p.Sp = Sp;
     const float scale = dims->scale > 0.f ? dims->scale : 1.0f / std::sqrt((float)D);
     p.scale_log2 = scale * 1.4426950408889634f;
-    if (launch_attn(Tk, D, tm_q, tm_k, tm_v, p, grid, s) != cudaSuccess) return VSA_ERR_CUDA;
+    // MMA-issue layout: paired when the rows of q2k_idx can hold at least
+    // three quarters of the key tiles (dense selections: most key tiles then
+    // serve both query units of a work item), or with 256-token tiles (both
+    // units are halves of one query tile and share its selection); split
+    // otherwise.  The host cannot see the selections without a sync, so the
+    // row length stands in for the density.  Results do not depend on it.
+    const bool paired = sub == 2 || 4ll * dims->max_kv >= 3ll * NT;
+    if (launch_attn(Tk, D, paired, tm_q, tm_k, tm_v, p, grid, s) != cudaSuccess) return VSA_ERR_CUDA;
 
     const AttnLaunchInfo info = attn_launch_info(Tk, D, p.bm_words);
     t_route.kernel = VSA_KERNEL_ATTN_TCGEN05;
@@ -355,6 +362,7 @@ vsa_status vsa_block_sparse_fwd(const void *q, const void *k, const void *v, con
     t_route.work_items = n_items;
     t_route.sort_bins = bins;
     t_route.smem_bytes = info.smem_bytes;
+    t_route.layout = paired ? VSA_LAYOUT_PAIRED : VSA_LAYOUT_SPLIT;
     return VSA_OK;
 }
 

@@ -16,11 +16,18 @@
 //     in ascending order, through a ring of K/V stages with TMA, so a key
 //     tile that both units select is fetched once ("gathered" fetch).  The
 //     ring is as deep as shared memory allows.
-//   * One MMA-issuing thread per unit issues S_u = Q_u K_j^T (tcgen05, smem x
-//     smem -> TMEM) for the key tiles the unit selects, and O_u += P_u V_j
-//     with P read from TMEM.  tcgen05.mma issue runs only ~2 instructions
-//     ahead of execution and every barrier wait costs the issuing thread ~100
-//     cycles, so two issuers let one unit's waits overlap the other's issue.
+//   * S_u = Q_u K_j^T (tcgen05, smem x smem -> TMEM) for the key tiles unit u
+//     selects, and O_u += P_u V_j with P read from TMEM, are issued in one of
+//     two layouts (a template parameter; the host picks it from the
+//     selection width).  One thread issues tcgen05.mma at about 88 cycles an
+//     instruction, while two threads issuing at once keep the tensor pipe at
+//     its full rate (64 cycles an M128 N128 K16 MMA):
+//       - paired (dense selections): one thread per unit issues both of its
+//         products, the next S before the current P V, which keeps P V out of
+//         the way of the S hand-off between the units;
+//       - split (sparse selections, where a key tile mostly serves one unit):
+//         one thread issues every S, and one thread per unit its P V as soon
+//         as P is stored, so S and P V issue overlap.
 //   * TMEM holds O of both units, ONE S buffer the units take turns on (a
 //     shared-memory counter tells an issuer when every earlier S has been
 //     copied out), and P of each unit as bf16 pairs.
@@ -33,12 +40,13 @@
 //     epilogue writes O / l and the natural-log LSE.
 //   * Masks are applied only on tail key tiles (valid count < tile).  For a
 //     tail tile P V runs only over the 16-key blocks that hold valid keys, and
-//     a fix-up warp zeroes the few padding rows inside the last block in
+//     one control warp zeroes the few padding rows inside the last block in
 //     shared memory first, so NaN/Inf padding in V never meets a zero weight
 //     (0 * NaN = NaN).
-//   * 20 warps: four softmax warpgroups, then a control warpgroup (two MMA
-//     issuers, the TMA producer, the V fix-up warp) that hands registers to
-//     the softmax warpgroups with setmaxnreg.
+//   * 20 warps: four softmax warpgroups, then a control warpgroup (three
+//     MMA-issuing warps, one of which zeroes tail V rows, and the TMA
+//     producer) that hands registers to the softmax warpgroups with
+//     setmaxnreg.
 //   * Every wait is bounded (about 2 s); on expiry the CTA sets the timeout
 //     flag, drains its outstanding copies and MMAs, frees TMEM and returns.
 #include <cuda_bf16.h>
@@ -54,9 +62,16 @@ using namespace ptx;
 
 constexpr int kSoftmaxWarps = 16;
 constexpr int kUnitWarps = 8;      // softmax warps per unit; each adds 1 to the S counter per S
-constexpr int kMmaWarp0 = 16;      // MMA issuer of unit 0; kMmaWarp0 + 1 issues for unit 1
+// Control warps (roles per layout, see the kernel):
+//   paired: 16 + u issues every MMA of unit u; 19 zeroes tail V rows.
+//   split:  16 issues every S; 17 issues P V of unit 0 and zeroes tail V rows;
+//           19 issues P V of unit 1.
+constexpr int kSWarp = 16;         // also allocates TMEM
+constexpr int kPvWarp0 = 17;
 constexpr int kProducerWarp = 18;
-constexpr int kFixupWarp = 19;     // zeroes V padding rows of tail key tiles
+constexpr int kPvWarp1 = 19;
+constexpr int kIssuers = 3;        // split layout: a ring fill is released by three arrivals
+constexpr int kPairedIssuers = 2;  // paired layout: by two
 constexpr int kMaxStages = 8;
 // Register split (control warpgroup, four softmax warpgroups); the sum stays
 // within the 640 x 96 registers the CTA is launched with.
@@ -99,12 +114,12 @@ struct Bars {
     __host__ __device__ int o_done(int u) const { return 3 * NS + 8 + u; }
     __host__ __device__ int bm_full(int p) const { return 3 * NS + 10 + p; }
     __host__ __device__ int bm_empty(int p) const { return 3 * NS + 12 + p; }
-    __host__ __device__ int done(int u) const { return 3 * NS + 14 + u; }
-    __host__ __device__ int count() const { return 3 * NS + 16; }
+    __host__ __device__ int done(int i) const { return 3 * NS + 14 + i; }  // one per issuer
+    __host__ __device__ int count() const { return 3 * NS + 14 + kIssuers; }
 };
 
 struct SmemPlan {
-    uint32_t q, ring, bm, hdr, bars, tslot, flag, sfree, total;
+    uint32_t q, ring, bm, hdr, bars, tslot, flag, sfree, sprog, total;
 };
 
 template <int T, int D>
@@ -119,7 +134,8 @@ __host__ __device__ inline SmemPlan smem_plan(int bm_words, int NS) {
     s.tslot = s.bars + 8u * (uint32_t)Bars{NS}.count();
     s.flag = s.tslot + 4;
     s.sfree = s.flag + 4;
-    s.total = ((s.sfree + 4 + 15) & ~15u) + 1024;  // + slack to align the base to 1024
+    s.sprog = s.sfree + 4;
+    s.total = ((s.sprog + 4 + 15) & ~15u) + 1024;  // + slack to align the base to 1024
     return s;
 }
 
@@ -181,7 +197,7 @@ __device__ __forceinline__ int tile_size(const int32_t *block_sizes, int jj, int
     return n < 0 ? 0 : (n > 128 ? 128 : n);
 }
 
-template <int T, int D>
+template <int T, int D, bool kPaired>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const AttnParams P) {
@@ -198,6 +214,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     // Count of S tiles the softmax warps have copied out of the shared S buffer
     // (each of the eight warps of a unit adds 1 per S).
     const uint32_t sFree = base + L.sfree;
+    // Count of ring fills the S issuer has seen land.  The S issuer waits for
+    // every fill in order; the P V issuers wait for V fills only, and a parity
+    // wait on a stage refers to the fill meant only once the stage's previous
+    // fill has landed, which this count tells them.
+    const uint32_t sProg = base + L.sprog;
     const uint32_t sRing = base + L.ring;
     uint32_t *bm = reinterpret_cast<uint32_t *>(gbase + L.bm);           // [2][4][W]
     volatile int32_t *hdr = reinterpret_cast<int32_t *>(gbase + L.hdr);  // [2][4]
@@ -212,7 +233,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < NS; ++s) {
             mbar_init(BAR(BI.kv_full(s)), 1);
-            mbar_init(BAR(BI.kv_empty(s)), 2);  // both MMA issuers release every fill
+            mbar_init(BAR(BI.kv_empty(s)), kPaired ? kPairedIssuers : kIssuers);  // arrivals per fill
             mbar_init(BAR(BI.vz(s)), 32);
         }
         #pragma unroll
@@ -223,15 +244,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             mbar_init(BAR(BI.p_full(u)), 32 * kUnitWarps);
             mbar_init(BAR(BI.o_done(u)), 1);
             mbar_init(BAR(BI.bm_full(u)), 32);
-            mbar_init(BAR(BI.bm_empty(u)), 2 + 32 + 32 * kSoftmaxWarps);  // issuers' lane 0, fix-up, softmax
-            mbar_init(BAR(BI.done(u)), 1);
+            // lane 0 of two issuing warps, all lanes of the warp that zeroes
+            // tail V rows, the softmax warps (either layout)
+            mbar_init(BAR(BI.bm_empty(u)), 2 + 32 + 32 * kSoftmaxWarps);
         }
+        for (int i = 0; i < kIssuers; ++i) mbar_init(BAR(BI.done(i)), 1);
         *abort_flag = 0;
         *reinterpret_cast<volatile uint32_t *>(gbase + L.sfree) = 0u;
+        *reinterpret_cast<volatile uint32_t *>(gbase + L.sprog) = 0u;
         fence_mbar_init();
         fence_proxy_async_smem();
     }
-    if (warp == kMmaWarp0) {
+    if (warp == kSWarp) {
         tmem_alloc(smem_u32(tslot), C::kTmemCols);
         tmem_relinquish();
     }
@@ -254,6 +278,22 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     // role branch so no code of one role runs under the other's limit.
     if (warp >= kSoftmaxWarps) {
       regs_dec<RegSplit<T>::kControl>();
+      // Role layout of the MMA issue (a template parameter; the host picks
+      // it from the selection width):
+      //   paired (dense selections: most key tiles serve both units): lane 0
+      //     of warp 16 + u issues every MMA of unit u, S_u of the next key
+      //     tile before O_u += P_u V of the current one; warp 19 zeroes tail
+      //     V rows.  The S hand-off between the units through the shared S
+      //     buffer is then the critical chain, and a P V queued behind the
+      //     next S keeps out of its way.
+      //   split (sparse selections, where a key tile mostly serves one unit):
+      //     lane 0 of warp 16 issues every S; warp 17 + 2u issues O_u += P_u V
+      //     as soon as P_u is stored; warp 17 zeroes tail V rows.  One thread
+      //     issues tcgen05.mma at about 88 cycles an instruction, while two
+      //     threads issuing at once keep the tensor pipe at its full rate (64
+      //     cycles an M128 N128 K16 MMA), so the S stream and the P V streams
+      //     overlap instead of queueing in one thread.
+      constexpr bool paired = kPaired;
       if (warp == kProducerWarp) {
         // ------------------------------------------------------------ producer
         const uint64_t pol_kv = l2_policy_evict_last();
@@ -370,7 +410,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 for (int u = 0; u < 2; ++u) drain_wait(BAR(BI.q_full(u)), (q_loads - 1) & 1u);
         }
         __syncwarp();
-      } else if (warp == kFixupWarp) {
+      } else if (paired && warp == kPvWarp1) {  // (paired is a compile-time constant)
+        // ============================================ paired layout
         // ------------------------------------------------------------ tail V fix-up
         // For a tail key tile (valid count not a multiple of 16) P V reads the
         // last 16-key block, whose padding rows may hold NaN/Inf: zero them
@@ -414,16 +455,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             __syncwarp();
             mbar_arrive(BAR(BI.bm_empty(p)));
         }
-      } else {
-        // ------------------------------------------------------------ MMA issuers
-        // Lane 0 of warp kMmaWarp0 + u issues every MMA of unit u: S_u = Q_u
+      } else if (paired) {
+        // ------------------------------------------------------------ MMA issuers (paired layout)
+        // Lane 0 of warp 16 + u issues every MMA of unit u: S_u = Q_u
         // K_j^T and O_u += P_u V_j.  tcgen05.mma issue runs only ~2
         // instructions ahead of execution and each barrier wait costs the
         // issuing thread ~100 cycles, so (a) two issuers let one unit's waits
         // overlap the other's issue, and (b) all waits of an entry come before
         // its MMAs, leaving nothing between a unit's P V and its next S.
         if (lane == 0) {
-            const int u = warp - kMmaWarp0;
+            const int u = warp - kSWarp;  // warps 16 and 17
             Ring ring;
             uint32_t pcnt = 0;    // P V issued (= p_full phases consumed)
             uint32_t gcnt = 0;    // S tiles of both units before this entry (union order, unit 0 first)
@@ -532,6 +573,189 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             // All MMAs of this issuer complete before TMEM is released.
             mma_commit(BAR(BI.done(u)));
             drain_wait(BAR(BI.done(u)), 0u);
+        }
+        __syncwarp();
+      } else if (warp == kSWarp) {
+        // ============================================ split layout
+        // ------------------------------------------------------------ S issuer
+        // Lane 0 issues S_u = Q_u K_j^T for both units, in the order the
+        // units take the shared S buffer (union order, unit 0 first), each
+        // once the softmax warps have copied every earlier S out.
+        if (lane == 0) {
+            Ring ring;
+            uint32_t g = 0;  // S tiles issued so far (both units, all items)
+            uint64_t dq[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) dq[u] = sdesc_sw128(sQ + u * C::kQBytes, 16, 1024);  // Q_u, K-major
+            const uint64_t dk = sdesc_sw128(sRing, 16, 1024);                              // stage 0 as K-major B
+            constexpr uint32_t kStage16 = C::kStageBytes >> 4;
+            const uint32_t tS = tmem + C::kTmemS;
+            bool ok = true;
+            for (uint32_t it = 0; ok; ++it) {
+                const int p = it & 1;
+                if (!(ok = wait_bar(BAR(BI.bm_full(p)), (it >> 1) & 1u, abort_flag, P.status))) break;
+                if (hdr[p * 4] < 0) break;
+                const uint32_t *bmp = bm + p * 4 * W;
+                // member entries per unit, so Q_u is released right after its last S
+                uint32_t n_mine[2] = {0u, 0u}, seen[2] = {0u, 0u};
+                for (int w = 0; w < W; ++w) {
+                    n_mine[0] += __popc(bmp[w] | bmp[W + w]);
+                    n_mine[1] += __popc(bmp[2 * W + w] | bmp[3 * W + w]);
+                }
+#pragma unroll
+                for (int u = 0; u < 2; ++u)
+                    if (ok) ok = wait_bar(BAR(BI.q_full(u)), it & 1u, abort_flag, P.status);
+                if (!ok) break;
+                tc_fence_after();
+                for (int w = 0; w < W && ok; ++w) {
+                    const uint32_t m0w = bmp[w] | bmp[W + w], m1w = bmp[2 * W + w] | bmp[3 * W + w];
+                    uint32_t bits = m0w | m1w;
+                    while (bits && ok) {
+                        const int b = __ffs(bits) - 1;
+                        bits &= bits - 1;
+                        const uint32_t kst = ring.st, kph = ring.ph;
+                        ring.next(NS);
+                        const uint32_t vst = ring.st, vph = ring.ph;
+                        ring.next(NS);
+                        if (!(ok = wait_bar_spin(BAR(BI.kv_full(kst)), kph, abort_flag, P.status))) break;
+                        red_add_release(sProg, 1u);
+#pragma unroll
+                        for (int u = 0; u < 2; ++u) {
+                            if (!ok || !((((u ? m1w : m0w) >> b) & 1u))) continue;
+                            // every earlier S tile has left the shared S buffer
+                            if (!(ok = wait_count(sFree, (uint32_t)kUnitWarps * g, abort_flag, P.status))) break;
+                            tc_fence_after();
+#pragma unroll
+                            for (int kk = 0; kk < D / 16; ++kk)
+                                mma_ss(tS, dq[u] + (kk >> 2) * (C::kQChunk >> 4) + (kk & 3) * 2,
+                                       dk + kst * kStage16 + (kk >> 2) * (C::kKVChunk >> 4) + (kk & 3) * 2,
+                                       C::kIdescQK, kk > 0 ? 1u : 0u);
+                            mma_commit(BAR(BI.s_full(u)));
+                            if (++seen[u] == n_mine[u]) mma_commit(BAR(BI.q_empty(u)));
+                            ++g;
+                        }
+                        if (!ok) break;
+                        // K fills are released by this thread alone (the P V
+                        // issuers never read them): two arrivals now, the
+                        // third when the S MMAs that read K have completed.
+                        mbar_arrive(BAR(BI.kv_empty(kst)));
+                        mbar_arrive(BAR(BI.kv_empty(kst)));
+                        mma_commit(BAR(BI.kv_empty(kst)));
+                        // V of the tile is not read here; its fill is still
+                        // waited for (and released: one of its three
+                        // arrivals) in order, so every parity wait of this
+                        // thread refers to the fill it means.
+                        if (!(ok = wait_bar(BAR(BI.kv_full(vst)), vph, abort_flag, P.status))) break;
+                        red_add_release(sProg, 1u);
+                        mbar_arrive(BAR(BI.kv_empty(vst)));
+                    }
+                }
+                if (!ok) break;
+#pragma unroll
+                for (int u = 0; u < 2; ++u)
+                    if (n_mine[u] == 0) mma_commit(BAR(BI.q_empty(u)));  // no S of this unit: release Q_u
+                mbar_arrive(BAR(BI.bm_empty(p)));
+            }
+            // All MMAs of this issuer complete before TMEM is released.
+            mma_commit(BAR(BI.done(0)));
+            drain_wait(BAR(BI.done(0)), 0u);
+        }
+        __syncwarp();
+      } else {
+        // ------------------------------------------------------------ P V issuers
+        // Warp kPvWarp0 + 2u issues O_u += P_u V_j (lane 0) as soon as the
+        // softmax has stored P_u.  Warp kPvWarp0 also zeroes the padding rows
+        // of a tail key tile's V inside its last 16-key block (rows of 128
+        // bytes; the swizzle permutes 16-byte chunks within a row only) once
+        // the tile has landed, so NaN/Inf padding never meets a zero weight;
+        // warp kPvWarp1 waits for that before its P V.
+        const int u = (warp == kPvWarp0) ? 0 : 1;
+        const bool fixer = (u == 0);
+        Ring ring;
+        uint32_t fills = 0;   // ring fills walked so far (K and V of every tile)
+        uint32_t pcnt = 0;    // P V issued (= p_full phases consumed)
+        uint32_t vz_par = 0;  // per stage: parity of its next tail-zeroing phase
+        const uint64_t dv = sdesc_sw128(sRing, C::kKVChunk, 1024);  // stage 0 as MN-major B
+        constexpr uint32_t kStage16 = C::kStageBytes >> 4;
+        const uint32_t tP = tmem + (u ? C::kTmemP1 : C::kTmemP0);
+        const uint32_t tO = tmem + (u ? C::kTmemO1 : C::kTmemO0);
+        bool ok = true;
+        for (uint32_t it = 0; ok; ++it) {
+            const int p = it & 1;
+            if (!(ok = wait_warp(BAR(BI.bm_full(p)), (it >> 1) & 1u, abort_flag, P.status))) break;
+            if (hdr[p * 4] < 0) break;
+            const uint32_t *bmp = bm + p * 4 * W;
+            bool first = true;
+            for (int w = 0; w < W && ok; ++w) {
+                const uint32_t mw = bmp[(2 * u) * W + w] | bmp[(2 * u + 1) * W + w];
+                uint32_t bits = bmp[w] | bmp[W + w] | bmp[2 * W + w] | bmp[3 * W + w];
+                while (bits && ok) {
+                    const int b = __ffs(bits) - 1;
+                    bits &= bits - 1;
+                    const int j = w * 32 + b;
+                    ring.next(NS);  // K fill of tile j: the S issuer waits for it and releases it
+                    const uint32_t vst = ring.st, vph = ring.ph;
+                    ring.next(NS);
+                    const uint32_t vfill = fills + 1;  // index of this V fill
+                    fills += 2;
+                    // the S issuer has seen the stage's previous fill (index
+                    // vfill - NS) land, so the parity wait below means this fill
+                    if (vfill >= (uint32_t)NS &&
+                        !(ok = __all_sync(0xffffffffu, wait_count(sProg, vfill - (uint32_t)NS + 1u, abort_flag,
+                                                                  P.status))))
+                        break;
+                    if (!(ok = __all_sync(0xffffffffu, wait_bar_spin(BAR(BI.kv_full(vst)), vph, abort_flag, P.status))))
+                        break;
+                    const int nj = tile_size(P.block_sizes, j, P.sub);
+                    const bool tail = (nj & 15) != 0;
+                    const uint32_t vzp = (vz_par >> vst) & 1u;
+                    if (tail) {
+                        vz_par ^= 1u << vst;
+                        if (fixer) {
+                            uint4 *vs = reinterpret_cast<uint4 *>(gbase + L.ring + vst * C::kStageBytes);
+                            const int n16 = (16 - (nj & 15)) * 8;
+#pragma unroll
+                            for (int c = 0; c < C::kChunks; ++c)
+                                for (int i = lane; i < n16; i += 32)
+                                    vs[(c * C::kKVChunk + nj * 128) / 16 + i] = make_uint4(0u, 0u, 0u, 0u);
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                            mbar_arrive(BAR(BI.vz(vst)));
+                        } else if (!(ok = wait_warp(BAR(BI.vz(vst)), vzp, abort_flag, P.status))) {
+                            break;
+                        }
+                    }
+                    if ((mw >> b) & 1u) {
+                        if (!(ok = __all_sync(0xffffffffu,
+                                              wait_bar_spin(BAR(BI.p_full(u)), pcnt & 1u, abort_flag, P.status))))
+                            break;
+                        ++pcnt;
+                        if (lane == 0) {
+                            tc_fence_after();
+                            const uint64_t bd = dv + vst * kStage16;
+                            const int kb = (nj + 15) >> 4;  // 16-key blocks holding valid keys
+                            mma_ts(tO, tP, bd, C::kIdescPV, first ? 0u : 1u);
+#pragma unroll
+                            for (int kk = 1; kk < T / 16; ++kk)
+                                if (kk < kb) mma_ts(tO, tP + kk * 8, bd + kk * 128, C::kIdescPV, 1u);
+                            mma_commit(BAR(BI.o_done(u)));
+                            mma_commit(BAR(BI.kv_empty(vst)));
+                        }
+                        first = false;
+                    } else if (lane == 0) {
+                        mbar_arrive(BAR(BI.kv_empty(vst)));  // not selected by this unit
+                    }
+                    __syncwarp();
+                }
+            }
+            if (!ok) break;
+            __syncwarp();
+            if (fixer || lane == 0) mbar_arrive(BAR(BI.bm_empty(p)));
+        }
+        // All MMAs of this issuer complete before TMEM is released.
+        if (lane == 0) {
+            mma_commit(BAR(BI.done(1 + u)));
+            drain_wait(BAR(BI.done(1 + u)), 0u);
         }
         __syncwarp();
       }
@@ -714,15 +938,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == kMmaWarp0) tmem_dealloc(tmem, C::kTmemCols);
+    if (warp == kSWarp) tmem_dealloc(tmem, C::kTmemCols);
 }
 
 template <int T, int D>
-cudaError_t launch_t(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v, AttnParams p, int grid,
-                     cudaStream_t stream) {
+cudaError_t launch_t(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v, AttnParams p, bool paired,
+                     int grid, cudaStream_t stream) {
     p.stages = stages_for<T, D>(p.bm_words);
     const SmemPlan L = smem_plan<T, D>(p.bm_words, p.stages);
-    attn_fwd_kernel<T, D><<<grid, kAttnThreads, L.total, stream>>>(q, k, v, p);
+    if (paired)
+        attn_fwd_kernel<T, D, true><<<grid, kAttnThreads, L.total, stream>>>(q, k, v, p);
+    else
+        attn_fwd_kernel<T, D, false><<<grid, kAttnThreads, L.total, stream>>>(q, k, v, p);
     return cudaGetLastError();
 }
 
@@ -734,7 +961,10 @@ AttnLaunchInfo info_t(int bm_words) {
 
 template <int T, int D>
 cudaError_t prepare_t() {
-    return cudaFuncSetAttribute(attn_fwd_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    const cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<T, D, true>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemLimit);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(attn_fwd_kernel<T, D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 (int)kSmemLimit);
 }
 
@@ -754,12 +984,12 @@ cudaError_t attn_prepare(int tile, int head_dim, int) {
     return prepare_t<64, 64>();
 }
 
-cudaError_t launch_attn(int tile, int head_dim, const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
-                        AttnParams p, int grid, cudaStream_t stream) {
-    if (tile == 128 && head_dim == 128) return launch_t<128, 128>(q, k, v, p, grid, stream);
-    if (tile == 128 && head_dim == 64) return launch_t<128, 64>(q, k, v, p, grid, stream);
-    if (tile == 64 && head_dim == 128) return launch_t<64, 128>(q, k, v, p, grid, stream);
-    return launch_t<64, 64>(q, k, v, p, grid, stream);
+cudaError_t launch_attn(int tile, int head_dim, bool paired, const CUtensorMap &q, const CUtensorMap &k,
+                        const CUtensorMap &v, AttnParams p, int grid, cudaStream_t stream) {
+    if (tile == 128 && head_dim == 128) return launch_t<128, 128>(q, k, v, p, paired, grid, stream);
+    if (tile == 128 && head_dim == 64) return launch_t<128, 64>(q, k, v, p, paired, grid, stream);
+    if (tile == 64 && head_dim == 128) return launch_t<64, 128>(q, k, v, p, paired, grid, stream);
+    return launch_t<64, 64>(q, k, v, p, paired, grid, stream);
 }
 
 }  // namespace vsa

@@ -85,7 +85,18 @@ typedef struct {
     int64_t work_items;   /* 256-query-row work items scheduled */
     int32_t sort_bins;    /* bins of the on-device work ordering */
     int32_t smem_bytes;   /* dynamic shared memory per CTA */
+    int32_t layout;       /* VSA_LAYOUT_*: how the attention kernel's MMA issue is split
+                             over its threads (results are the same either way) */
+    int32_t reserved;
 } vsa_route;
+
+/* Attention kernel MMA-issue layouts (vsa_route.layout).  PAIRED: one thread
+   per 128-row query unit issues both of its products (dense selections).
+   SPLIT: one thread issues every S = Q K^T, one thread per unit its P V
+   (sparse selections).  Chosen from vsa_dims: PAIRED when 4 * max_kv >=
+   3 * num_tiles or tile == 256. */
+#define VSA_LAYOUT_SPLIT 0
+#define VSA_LAYOUT_PAIRED 1
 
 #define VSA_KERNEL_NONE 0
 #define VSA_KERNEL_ATTN_TCGEN05 1

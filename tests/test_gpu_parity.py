@@ -6,6 +6,7 @@ on the GPU, and compares with ``oracle`` on the same inputs (see
 that any row the kernel fails to write shows up (the NaN-filled allocator of
 the sm_121a test list on the FastVideo kernel page).
 """
+import dataclasses
 import math
 
 import numpy as np
@@ -217,6 +218,26 @@ def test_deterministic(vsa, oracle_mod):
     b, lb = _run(vsa, q, k, v, w)
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
     assert torch.equal(la.view(torch.int32), lb.view(torch.int32))
+
+
+def test_issue_layouts_agree_bitwise(vsa, oracle_mod):
+    """The split and paired MMA-issue layouts run the same products in the same
+    order per accumulator, so they give bit-identical results.  The layout
+    follows the row length of q2k_idx: the same selections, with rows padded
+    to every key tile, switch a sparse case from split to paired."""
+    for T, D, NT in ((128, 128, 9), (64, 64, 11)):
+        w = _random_case(500 + T + NT, 2, 3, NT, T, D, max_kv=max(1, NT // 3))
+        (q, k, v), refs = _to_tile_major(w, vsa, oracle_mod)
+        a, la = _run(vsa, q, k, v, w)
+        assert vsa.vsa_last_route()["layout"] == vsa.VSA_LAYOUT_SPLIT
+        wide = torch.full((w.B, w.H, w.NT, w.NT), -1, dtype=torch.int32)
+        wide[..., : w.max_kv] = w.q2k_idx
+        w_wide = dataclasses.replace(w, q2k_idx=wide)
+        b, lb = _run(vsa, q, k, v, w_wide)
+        assert vsa.vsa_last_route()["layout"] == vsa.VSA_LAYOUT_PAIRED
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16)), f"T{T}: layouts differ"
+        assert torch.equal(la.view(torch.int32), lb.view(torch.int32))
+        _check(w, a, la, refs, oracle_mod, list(range(w.B * w.H * w.NT)), f"layouts T{T}")
 
 
 def test_bad_indices_are_flagged_not_faulted(vsa):
