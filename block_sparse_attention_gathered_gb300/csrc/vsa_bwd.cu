@@ -36,10 +36,12 @@
 //                  write P^T and dS^T as bf16 back over the columns they read;
 //                  dV += P^T dO_t and dK += dS^T Q_t accumulate in TMEM with
 //                  the A operand taken from the slot.  One thread issues the
-//                  accumulations, another the copies and S/dP, which go into
-//                  a slot as soon as the previous pair's accumulations have
-//                  read it: the next pair's products overlap this pair's
-//                  elementwise step.
+//                  accumulations, a second the copies and S, a third dP (one
+//                  thread issues tcgen05.mma at about 88 cycles an
+//                  instruction, so the N = 64 products need two issuers); S
+//                  and dP go into a slot as soon as the previous pair's
+//                  accumulations have read it: the next pair's products
+//                  overlap this pair's elementwise step.
 //   bwd_kernel<D, false>  one CTA per (batch, head, query tile t): Q_t and dO_t
 //                  stay; for every selected key tile, S and dP again, dS back
 //                  into TMEM, dQ += dS K_j.  Recomputing S and dP keeps dQ
@@ -67,8 +69,9 @@ constexpr int kEwSplit = 2;                 // elementwise threads per row
 constexpr int kEwThreads = kEwSplit * kBT;  // elementwise warps first
 constexpr int kEwCols = 64 / kEwSplit;      // columns per thread in each 64-column half
 constexpr int kCtlWarp = kEwThreads / 32;   // lane 0 issues the accumulation MMAs
-constexpr int kSdpWarp = kCtlWarp + 1;      // lane 0 issues the TMA copies and the S/dP MMAs
-constexpr int kThreads = kEwThreads + 64;
+constexpr int kSdpWarp = kCtlWarp + 1;      // lane 0 issues the TMA copies and the S MMAs
+constexpr int kDpWarp = kCtlWarp + 2;       // lane 0 issues the dP MMAs
+constexpr int kThreads = kEwThreads + 96;
 constexpr uint32_t kChunkBytes = kBT * 128;  // one 64-column (128-byte) chunk of a 128-row tile
 
 template <int D>
@@ -270,17 +273,22 @@ __global__ void __launch_bounds__(1024)
     // fill in ascending X: one list per round; a key tile appears at most once
     // per list, so its cursor advances in X order
     int32_t *lst = list + bh * (int64_t)NTk * maxlen;
-    int nxt = __ldg(pcb);
+    // the rounds are sequential, so each thread loads its first entry of the
+    // next round (and the round's count) while this round runs
+    int c = __ldg(pcb);
+    int32_t e0 = (tid < c) ? __ldg(plb + tid) : 0;
     for (int X = 0; X < NTk; ++X) {
-        const int c = nxt;
-        if (X + 1 < NTk) nxt = __ldg(pcb + X + 1);
+        const int c_next = (X + 1 < NTk) ? __ldg(pcb + X + 1) : 0;
+        const int32_t e0_next = (tid < c_next) ? __ldg(plb + (int64_t)(X + 1) * maxlen + tid) : 0;
         if (c > 0) {
             const Rows rx = ktile_rows(bs, G, X);
             for (int i = tid; i < c; i += blockDim.x) {
-                const int32_t e = __ldg(plb + (int64_t)X * maxlen + i);
+                const int32_t e = (i == tid) ? e0 : __ldg(plb + (int64_t)X * maxlen + i);
                 lst[atomicAdd(&cur[entry_y(e)], 1)] = pack_entry(X, rx, swap_mask(e & 15));
             }
         }
+        c = c_next;
+        e0 = e0_next;
         __syncthreads();
     }
 }
@@ -448,7 +456,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int b = 0; b < kNumBars; ++b)
-            mbar_init(BAR(b), (b == kBarEw0 || b == kBarEw1) ? kEwThreads : (b == kBarDrain ? 2 : 1));
+            // a slot's S and dP are committed by two threads; three issuers drain
+            mbar_init(BAR(b), (b == kBarEw0 || b == kBarEw1) ? kEwThreads
+                              : (b == kBarDrain ? 3 : ((b == kBarS0 || b == kBarS1) ? 2 : 1)));
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -491,12 +501,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 ++issued[b];
             };
-            // S and dP of the half hv of pair i into slot hv
+            // S of the half hv of pair i into slot hv (dP: warp kDpWarp).  One
+            // thread issues tcgen05.mma at about 88 cycles an instruction, about
+            // three times the 128 x 64 product's own time, so S and dP, which
+            // go to different columns of the slot, are issued by two threads.
             auto issue_sdp = [&](int i, int hv) {
                 const int b = i & 1;
-                // KV: S^T = K_j Q_t^T, dP^T = V_j dO_t^T; else S = Q_t K_j^T, dP = dO_t V_j^T
+                // KV: S^T = K_j Q_t^T; else S = Q_t K_j^T
                 mma_half<D>(slot(hv), base + L::kRes0, base + L::buf(b, 0) + hv * kHalfBytes);
-                mma_half<D>(slot(hv) + 64, base + L::kRes1, base + L::buf(b, 1) + hv * kHalfBytes);
                 mma_commit(BAR(kBarS0 + hv));
             };
             if (n > 0) {
@@ -543,6 +555,41 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (issued[b] > seen[b]) drain_wait(BAR(kBarBuf0 + b), (issued[b] - 1) & 1u);
             }
             // every MMA of both issuers completes before TMEM is released
+            mma_commit(BAR(kBarDrain));
+            drain_wait(BAR(kBarDrain), 0u);
+        }
+        __syncwarp();
+    } else if (warp == kDpWarp) {
+        // ------------------------------------------------------------ dP
+        // dP of the half hv of pair i into the second 64 columns of slot hv,
+        // at the same points as S (the slot free, the pair's tiles landed).
+        if (lane == 0) {
+            bool ok = true;
+            auto issue_dp = [&](int i, int hv) {
+                const int b = i & 1;
+                // KV: dP^T = V_j dO_t^T; else dP = dO_t V_j^T
+                mma_half<D>(slot(hv) + 64, base + L::kRes1, base + L::buf(b, 1) + hv * kHalfBytes);
+                mma_commit(BAR(kBarS0 + hv));
+            };
+            if (n > 0) {
+                ok = wait_bar(BAR(kBarRes), 0u, abort_flag, A.status) &&
+                     wait_bar(BAR(kBarBuf0), 0u, abort_flag, A.status);
+                if (ok) {
+                    tc_fence_after();
+                    issue_dp(0, 0);
+                    issue_dp(0, 1);
+                }
+            }
+            for (int i = 0; i + 1 < n && ok; ++i) {
+                for (int hv = 0; hv < 2 && ok; ++hv) {
+                    if (!(ok = wait_bar(BAR(kBarFree0 + hv), i & 1u, abort_flag, A.status))) break;
+                    if (hv == 0 &&
+                        !(ok = wait_bar(BAR(kBarBuf0 + ((i + 1) & 1)), ((i + 1) >> 1) & 1u, abort_flag, A.status)))
+                        break;
+                    tc_fence_after();
+                    issue_dp(i + 1, hv);
+                }
+            }
             mma_commit(BAR(kBarDrain));
             drain_wait(BAR(kBarDrain), 0u);
         }
