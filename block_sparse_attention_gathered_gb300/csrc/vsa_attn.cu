@@ -92,11 +92,15 @@ struct Cfg {
     static constexpr uint32_t kQBytes = kUnitRows * D * 2;    // one unit's Q
     static constexpr uint32_t kKVChunk = T * 128;             // bytes of one K/V column chunk
     static constexpr uint32_t kStageBytes = T * D * 2;        // one K or V tile
-    // TMEM columns: O of each unit (fp32), one S buffer the units take turns
-    // on (fp32), and P of each unit (bf16 pairs).
-    static constexpr uint32_t kTmemO0 = 0, kTmemO1 = D, kTmemS = 2 * D, kTmemP0 = 2 * D + T,
-                              kTmemP1 = 2 * D + T + T / 2;
-    static constexpr uint32_t kTmemCols = (2 * D + 2 * T <= 256) ? 256 : 512;
+    // TMEM columns: O of each unit (fp32), S (fp32) and P of each unit (bf16
+    // pairs).  With 128-token tiles the units take turns on one S buffer (a
+    // second does not fit next to two O and two P); with 64-token tiles each
+    // unit has its own, so one unit's S never waits for the other's to be
+    // copied out.
+    static constexpr int kSBufs = (T == 64) ? 2 : 1;
+    static constexpr uint32_t kTmemO0 = 0, kTmemO1 = D, kTmemS0 = 2 * D, kTmemS1 = 2 * D + (kSBufs - 1) * T,
+                              kTmemP0 = 2 * D + kSBufs * T, kTmemP1 = 2 * D + kSBufs * T + T / 2;
+    static constexpr uint32_t kTmemCols = (2 * D + (kSBufs + 1) * T <= 256) ? 256 : 512;
     static constexpr uint32_t kIdescQK = idesc_bf16(128, T, false);
     static constexpr uint32_t kIdescPV = idesc_bf16(128, D, true);
 };
@@ -134,7 +138,7 @@ __host__ __device__ inline SmemPlan smem_plan(int bm_words, int NS) {
     s.tslot = s.bars + 8u * (uint32_t)Bars{NS}.count();
     s.flag = s.tslot + 4;
     s.sfree = s.flag + 4;
-    s.sprog = s.sfree + 4;
+    s.sprog = s.sfree + 8;  // one S-release counter per S buffer
     s.total = ((s.sprog + 4 + 15) & ~15u) + 1024;  // + slack to align the base to 1024
     return s;
 }
@@ -211,8 +215,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const int W = P.bm_words;
     const SmemPlan L = smem_plan<T, D>(W, NS);
     const uint32_t sQ = base + L.q;
-    // Count of S tiles the softmax warps have copied out of the shared S buffer
-    // (each of the eight warps of a unit adds 1 per S).
+    // Count of S tiles the softmax warps have copied out of an S buffer (each
+    // of the eight warps of a unit adds 1 per S): one shared count, or one per
+    // unit when each unit has its own buffer (sFree + 4u).
     const uint32_t sFree = base + L.sfree;
     // Count of ring fills the S issuer has seen land.  The S issuer waits for
     // every fill in order; the P V issuers wait for V fills only, and a parity
@@ -250,7 +255,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
         for (int i = 0; i < kIssuers; ++i) mbar_init(BAR(BI.done(i)), 1);
         *abort_flag = 0;
-        *reinterpret_cast<volatile uint32_t *>(gbase + L.sfree) = 0u;
+        reinterpret_cast<volatile uint32_t *>(gbase + L.sfree)[0] = 0u;
+        reinterpret_cast<volatile uint32_t *>(gbase + L.sfree)[1] = 0u;
         *reinterpret_cast<volatile uint32_t *>(gbase + L.sprog) = 0u;
         fence_mbar_init();
         fence_proxy_async_smem();
@@ -468,12 +474,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             Ring ring;
             uint32_t pcnt = 0;    // P V issued (= p_full phases consumed)
             uint32_t gcnt = 0;    // S tiles of both units before this entry (union order, unit 0 first)
+            uint32_t s_own = 0;   // S tiles of this unit issued so far
             uint32_t vz_par = 0;  // per stage: parity of its next tail-zeroing phase
             const uint64_t dq = sdesc_sw128(sQ + u * C::kQBytes, 16, 1024);  // Q_u, K-major
             const uint64_t dk = sdesc_sw128(sRing, 16, 1024);                // stage 0 as K-major B
             const uint64_t dv = sdesc_sw128(sRing, C::kKVChunk, 1024);       // stage 0 as MN-major B
             constexpr uint32_t kStage16 = C::kStageBytes >> 4;
-            const uint32_t tS = tmem + C::kTmemS;
+            const uint32_t tS = tmem + (u ? C::kTmemS1 : C::kTmemS0);
             const uint32_t tP = tmem + (u ? C::kTmemP1 : C::kTmemP0);
             const uint32_t tO = tmem + (u ? C::kTmemO1 : C::kTmemO0);
             bool ok = true;
@@ -537,8 +544,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                             // S first: it needs only K and the softmax having loaded
                             // the previous S; then the pending P V.
                             if (!(ok = wait_bar_spin(BAR(BI.kv_full(kst)), kph, abort_flag, P.status))) break;
-                            // every earlier S tile has left the shared S buffer
-                            if (!(ok = wait_count(sFree, (uint32_t)kUnitWarps * g, abort_flag, P.status))) break;
+                            // every earlier S tile has left the S buffer (shared: both
+                            // units' S in union order; per unit: this unit's)
+                            if (C::kSBufs == 2) {
+                                if (!(ok = wait_count(sFree + 4u * u, (uint32_t)kUnitWarps * s_own, abort_flag,
+                                                      P.status)))
+                                    break;
+                            } else if (!(ok = wait_count(sFree, (uint32_t)kUnitWarps * g, abort_flag, P.status))) {
+                                break;
+                            }
+                            ++s_own;
                             tc_fence_after();
 #pragma unroll
                             for (int kk = 0; kk < D / 16; ++kk)
@@ -589,7 +604,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             for (int u = 0; u < 2; ++u) dq[u] = sdesc_sw128(sQ + u * C::kQBytes, 16, 1024);  // Q_u, K-major
             const uint64_t dk = sdesc_sw128(sRing, 16, 1024);                              // stage 0 as K-major B
             constexpr uint32_t kStage16 = C::kStageBytes >> 4;
-            const uint32_t tS = tmem + C::kTmemS;
+            uint32_t s_unit[2] = {0u, 0u};  // S tiles issued so far per unit (per-unit buffers)
             bool ok = true;
             for (uint32_t it = 0; ok; ++it) {
                 const int p = it & 1;
@@ -622,12 +637,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
                         for (int u = 0; u < 2; ++u) {
                             if (!ok || !((((u ? m1w : m0w) >> b) & 1u))) continue;
-                            // every earlier S tile has left the shared S buffer
-                            if (!(ok = wait_count(sFree, (uint32_t)kUnitWarps * g, abort_flag, P.status))) break;
+                            // every earlier S tile has left the S buffer (shared: both
+                            // units' S in union order; per unit: this unit's)
+                            if (C::kSBufs == 2) {
+                                if (!(ok = wait_count(sFree + 4u * u, (uint32_t)kUnitWarps * s_unit[u], abort_flag,
+                                                      P.status)))
+                                    break;
+                            } else if (!(ok = wait_count(sFree, (uint32_t)kUnitWarps * g, abort_flag, P.status))) {
+                                break;
+                            }
+                            ++s_unit[u];
                             tc_fence_after();
 #pragma unroll
                             for (int kk = 0; kk < D / 16; ++kk)
-                                mma_ss(tS, dq[u] + (kk >> 2) * (C::kQChunk >> 4) + (kk & 3) * 2,
+                                mma_ss(tmem + (u ? C::kTmemS1 : C::kTmemS0), dq[u] + (kk >> 2) * (C::kQChunk >> 4) + (kk & 3) * 2,
                                        dk + kst * kStage16 + (kk >> 2) * (C::kKVChunk >> 4) + (kk & 3) * 2,
                                        C::kIdescQK, kk > 0 ? 1u : 0u);
                             mma_commit(BAR(BI.s_full(u)));
@@ -777,7 +800,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const int row = rb0 + (lane & 15);               // query row within the unit
         const int tsub = (T == 64) ? (q4 >> 1) : 0;      // which 64-row tile of the unit (T == 64)
         const uint32_t tl = (uint32_t)rb0 << 16;
-        const uint32_t tS = tmem + tl + C::kTmemS;
+        const uint32_t tS = tmem + tl + (u ? C::kTmemS1 : C::kTmemS0);
+        const uint32_t sFreeU = sFree + (C::kSBufs == 2 ? 4u * u : 0u);  // the count this unit adds to
         const uint32_t tP = tmem + tl + (u ? C::kTmemP1 : C::kTmemP0);
         const uint32_t tO = tmem + tl + (u ? C::kTmemO1 : C::kTmemO0);
         const float c = P.scale_log2;
@@ -817,7 +841,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     // S is in registers: the shared S buffer may take the next S.
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) red_add_release(sFree, 1u);
+                    if (lane == 0) red_add_release(sFreeU, 1u);
                     float m_new = m;
                     bool fresh = false, resc = false;
                     if (member_row) {
