@@ -43,10 +43,10 @@ FALLBACK_HBM_GBS = 6800.0
 # the SHA-256 of the attention kernel source the capture was taken with; a
 # changed kernel reports null until it is captured again.
 ATTN_TRAFFIC = {
-    # profiles/attn_fwd_t128d128_dense_b1h6_s31200.md: 348.0 MB read + 37.1 MB written
-    ("dense_b1h6d128_s31200_t128x244_lse", "2f17a808ab988937"): 385.01e6,
-    # profiles/attn_fwd_t128d128_uniform_b1h12_k32.md: 176.3 MB read + 33.5 MB written
-    ("uniform_b1h12d128_t128x128_k32", "2f17a808ab988937"): 209.78e6,
+    # profiles/attn_fwd_t128d128_dense_b1h6_s31200.md: 258.6 MB read + 35.0 MB written
+    ("dense_b1h6d128_s31200_t128x244_lse", "32cebcfd69615685"): 293.60e6,
+    # profiles/attn_fwd_t128d128_uniform_b1h12_k32.md: 179.2 MB read + 34.8 MB written
+    ("uniform_b1h12d128_t128x128_k32", "32cebcfd69615685"): 213.97e6,
 }
 
 
