@@ -40,13 +40,14 @@ FALLBACK_BF16_TFLOPS = 1900.0
 FALLBACK_HBM_GBS = 6800.0
 
 # DRAM bytes (read + write) per attention launch from an ncu capture, keyed by
-# the SHA-256 of the attention kernel source the capture was taken with; a
-# changed kernel reports null until it is captured again.
+# the SHA-256 of the attention kernel source the capture was taken with (or of
+# a source that differs from it in comments only); a changed kernel reports
+# null until it is captured again.
 ATTN_TRAFFIC = {
     # profiles/attn_fwd_t128d128_dense_b1h6_s31200.md: 258.6 MB read + 35.0 MB written
-    ("dense_b1h6d128_s31200_t128x244_lse", "32cebcfd69615685"): 293.60e6,
+    ("dense_b1h6d128_s31200_t128x244_lse", "777e096d6954504f"): 293.60e6,
     # profiles/attn_fwd_t128d128_uniform_b1h12_k32.md: 179.2 MB read + 34.8 MB written
-    ("uniform_b1h12d128_t128x128_k32", "32cebcfd69615685"): 213.97e6,
+    ("uniform_b1h12d128_t128x128_k32", "777e096d6954504f"): 213.97e6,
 }
 
 

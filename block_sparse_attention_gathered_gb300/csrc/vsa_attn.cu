@@ -278,14 +278,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const int NT = P.NT;
     const int64_t Sp = P.Sp;
 
-    // Registers: launched at 168 per thread (384 threads); the control
-    // warpgroup (MMA issuers, producer, fix-up) keeps RegSplit::kControl and
-    // the two softmax warpgroups take RegSplit::kSoftmax.  Each re-split sits inside its own
-    // role branch so no code of one role runs under the other's limit.
+    // Registers: launched at 96 per thread (640 threads); the control
+    // warpgroup (MMA issuers, producer, tail V zeroing) drops to
+    // RegSplit::kControl and the four softmax warpgroups rise to
+    // RegSplit::kSoftmax.  Each re-split sits inside its own role branch so no
+    // code of one role runs under the other's limit.
     if (warp >= kSoftmaxWarps) {
       regs_dec<RegSplit<T>::kControl>();
       // Role layout of the MMA issue (a template parameter; the host picks
-      // it from the selection width):
+      // it from the tile size, head dim and selection width):
       //   paired (dense selections: most key tiles serve both units): lane 0
       //     of warp 16 + u issues every MMA of unit u, S_u of the next key
       //     tile before O_u += P_u V of the current one; warp 19 zeroes tail
@@ -418,7 +419,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         __syncwarp();
       } else if (paired && warp == kPvWarp1) {  // (paired is a compile-time constant)
         // ============================================ paired layout
-        // ------------------------------------------------------------ tail V fix-up
+        // ------------------------------------------------------------ tail V zeroing (paired layout)
         // For a tail key tile (valid count not a multiple of 16) P V reads the
         // last 16-key block, whose padding rows may hold NaN/Inf: zero them
         // (rows of 128 bytes; the swizzle permutes 16-byte chunks within a row
