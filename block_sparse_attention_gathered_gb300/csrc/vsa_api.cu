@@ -344,16 +344,15 @@ vsa_status vsa_block_sparse_fwd(const void *q, const void *k, const void *v, con
     const float scale = dims->scale > 0.f ? dims->scale : 1.0f / std::sqrt((float)D);
     p.scale_log2 = scale * 1.4426950408889634f;
     // MMA-issue layout: paired for 128-token kernel tiles with D = 128 when
-    // the rows of q2k_idx can hold at least three quarters of the key tiles
-    // (dense selections: most key tiles then serve both query units of a work
-    // item) or with 256-token tiles (both units are halves of one query tile
-    // and share its selection); split otherwise.  With 64-token tiles or
-    // D = 64 a product is N = 64 wide, and issue by one thread per unit costs
-    // more than the shared-buffer hand-off gains (split measured faster at
-    // every density there).  The host cannot see the selections without a
-    // sync, so the row length stands in for the density.  Results do not
-    // depend on the layout.
-    const bool paired = Tk == 128 && D == 128 && (sub == 2 || 4ll * dims->max_kv >= 3ll * NT);
+    // the rows of q2k_idx can hold every key tile (a dense selection: every
+    // key tile then serves both query units of a work item) or with 256-token
+    // tiles (both units are halves of one query tile and share its
+    // selection); split otherwise.  Split measured faster as soon as a few
+    // key tiles serve only one unit (95 % selections included), and at every
+    // density with 64-token tiles or D = 64, where a product is N = 64 wide.
+    // The host cannot see the selections without a sync, so the row length
+    // stands in for the density.  Results do not depend on the layout.
+    const bool paired = Tk == 128 && D == 128 && (sub == 2 || dims->max_kv >= NT);
     if (launch_attn(Tk, D, paired, tm_q, tm_k, tm_v, p, grid, s) != cudaSuccess) return VSA_ERR_CUDA;
 
     const AttnLaunchInfo info = attn_launch_info(Tk, D, p.bm_words);

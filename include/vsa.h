@@ -93,8 +93,8 @@ typedef struct {
 /* Attention kernel MMA-issue layouts (vsa_route.layout).  PAIRED: one thread
    per 128-row query unit issues both of its products (dense selections).
    SPLIT: one thread issues every S = Q K^T, one thread per unit its P V
-   (sparse selections).  Chosen from vsa_dims: PAIRED when head_dim == 128,
-   tile is 128 or 256, and 4 * max_kv >= 3 * num_tiles or tile == 256. */
+   (sparse selections).  Chosen from vsa_dims: PAIRED when head_dim == 128
+   and either tile == 256, or tile == 128 and max_kv >= num_tiles. */
 #define VSA_LAYOUT_SPLIT 0
 #define VSA_LAYOUT_PAIRED 1
 
