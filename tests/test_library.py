@@ -202,3 +202,31 @@ def test_wait_probe_argument_errors(vsa):
     assert vsa.library().vsa_wait_probe(0, 0, None) == vsa.VSA_ERR_ARG
     assert vsa.library().vsa_wait_probe(0, 2000001, None) == vsa.VSA_ERR_ARG
     assert vsa.library().vsa_wait_probe(0, 1000, None) in (vsa.VSA_ERR_CUDA, vsa.VSA_ERR_ARCH)
+
+
+def test_binding_structs_match_the_header(vsa, tmp_path):
+    """The ctypes mirrors of vsa_dims and vsa_route have the C structs' size
+    and field offsets (a C program built against include/vsa.h reports them),
+    so a field added on one side only is caught without a GPU."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    structs = {"vsa_dims": vsa.VsaDims, "vsa_route": vsa.VsaRoute}
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "vsa.h"', 'int main(void) {']
+    for cname, py in structs.items():
+        lines.append(f'  printf("{cname} size %zu\\n", sizeof({cname}));')
+        for fname, _ in py._fields_:
+            lines.append(f'  printf("{cname} {fname} %zu\\n", offsetof({cname}, {fname}));')
+    lines += ['  return 0;', '}']
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-std=c99", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split("\n")
+    got = {tuple(l.split()[:2]): int(l.split()[2]) for l in out if l}
+    for cname, py in structs.items():
+        assert got[(cname, "size")] == ctypes.sizeof(py), cname
+        for fname, _ in py._fields_:
+            assert got[(cname, fname)] == getattr(py, fname).offset, (cname, fname)
