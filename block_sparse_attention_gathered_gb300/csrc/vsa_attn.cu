@@ -498,6 +498,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 tc_fence_after();
                 bool pending = false, first = true;
                 uint32_t pend_v = 0, pend_ph = 0;
+                uint32_t pend_lo = 0, pend_hi = 0;  // output lanes the pending P V leaves out (T == 64)
                 int pend_kb = 0;
                 bool pend_tail = false;
                 uint32_t seen = 0;
@@ -511,10 +512,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     ++pcnt;
                     tc_fence_after();
                     const uint64_t b = dv + pend_v * kStage16;
-                    mma_ts(tO, tP, b, C::kIdescPV, first ? 0u : 1u);
+                    if constexpr (T == 64) {
 #pragma unroll
-                    for (int kk = 1; kk < T / 16; ++kk)
-                        if (kk < pend_kb) mma_ts(tO, tP + kk * 8, b + kk * 128, C::kIdescPV, 1u);
+                        for (int kk = 0; kk < T / 16; ++kk)
+                            if (kk < pend_kb)
+                                mma_ts_lanes(tO, tP + kk * 8, b + kk * 128, C::kIdescPV, 1u, pend_lo, pend_hi);
+                    } else {
+                        mma_ts(tO, tP, b, C::kIdescPV, first ? 0u : 1u);
+#pragma unroll
+                        for (int kk = 1; kk < T / 16; ++kk)
+                            if (kk < pend_kb) mma_ts(tO, tP + kk * 8, b + kk * 128, C::kIdescPV, 1u);
+                    }
                     mma_commit(BAR(BI.o_done(u)));
                     mma_commit(BAR(BI.kv_empty(pend_v)));
                     first = false;
@@ -570,6 +578,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                             pend_ph = tail ? vzp : vph;
                             pend_kb = (nj + 15) >> 4;
                             pend_tail = tail;
+                            pend_lo = ((pa[w] >> b) & 1u) ? 0u : ~0u;
+                            pend_hi = ((pb[w] >> b) & 1u) ? 0u : ~0u;
                         } else {
                             // not selected by this unit: issue the pending P V (it
                             // frees a V stage), then release both stages of the entry
@@ -758,10 +768,21 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                             tc_fence_after();
                             const uint64_t bd = dv + vst * kStage16;
                             const int kb = (nj + 15) >> 4;  // 16-key blocks holding valid keys
-                            mma_ts(tO, tP, bd, C::kIdescPV, first ? 0u : 1u);
+                            if constexpr (T == 64) {
+                                // two 64-row tiles share the accumulator: rows of a tile
+                                // that does not select j are left out of the product
+                                const uint32_t off_lo = ((bmp[(2 * u) * W + w] >> b) & 1u) ? 0u : ~0u;
+                                const uint32_t off_hi = ((bmp[(2 * u + 1) * W + w] >> b) & 1u) ? 0u : ~0u;
 #pragma unroll
-                            for (int kk = 1; kk < T / 16; ++kk)
-                                if (kk < kb) mma_ts(tO, tP + kk * 8, bd + kk * 128, C::kIdescPV, 1u);
+                                for (int kk = 0; kk < T / 16; ++kk)
+                                    if (kk < kb)
+                                        mma_ts_lanes(tO, tP + kk * 8, bd + kk * 128, C::kIdescPV, 1u, off_lo, off_hi);
+                            } else {
+                                mma_ts(tO, tP, bd, C::kIdescPV, first ? 0u : 1u);
+#pragma unroll
+                                for (int kk = 1; kk < T / 16; ++kk)
+                                    if (kk < kb) mma_ts(tO, tP + kk * 8, bd + kk * 128, C::kIdescPV, 1u);
+                            }
                             mma_commit(BAR(BI.o_done(u)));
                             mma_commit(BAR(BI.kv_empty(vst)));
                         }
@@ -823,6 +844,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             bool ok = true;
             const uint32_t *pa = bmp + (2 * u) * W, *pb = bmp + (2 * u + 1) * W;
             const uint32_t *pm = tsub ? pb : pa;
+            if constexpr (T == 64) {
+                // Every P V accumulates (the rows of a tile that does not select
+                // a key tile are masked out of its product, so no single MMA
+                // may start O afresh): O starts at zero.  The stores complete
+                // before this unit's first P is released (tmem_wait_st), and the
+                // last item's P V finished before its epilogue read O.
+                const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int ch = 0; ch < DH / 8; ++ch) tmem_st2x_8f<DH>(tO + ch * 8, z);
+            }
             for (int w = 0; w < W && ok; ++w) {
                 uint32_t bits = pa[w] | pb[w];
                 const uint32_t mine = pm[w];

@@ -400,15 +400,24 @@ __device__ __forceinline__ void ew_cols(const float (&sv)[kEwCols], const float 
 // acc(128 x D) += A(128 x 128, bf16 pairs in TMEM) x tile(128 x D, MN-major in
 // shared memory: the tile's rows are summed).  ta is the half's TMEM slot,
 // which holds the bf16 pairs of its 64 columns.
-template <int D>
+// BM (64-token tiles): the accumulator's two 64-row halves belong to two
+// caller tiles, and lanes of a half whose tile does not meet this summed half
+// (mask bit 2a + half clear for accumulator half a) are left out of the
+// product altogether; the accumulators then start at zero and every MMA
+// accumulates.
+template <int D, bool BM>
 __device__ __forceinline__ void mma_acc_half(uint32_t tacc, uint32_t ta, uint32_t tile_saddr, int half,
-                                             bool accumulate) {
+                                             bool accumulate, int mk) {
     const uint64_t b = sdesc_sw128(tile_saddr, kChunkBytes, 1024);
+    const uint32_t off_lo = ((mk >> half) & 1) ? 0u : ~0u, off_hi = ((mk >> (2 + half)) & 1) ? 0u : ~0u;
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
         const int kk = half * 4 + q;
-        mma_ts(tacc, ta + packed_col(q), b + kk * (2048 >> 4), BwdCfg<D>::kIdescAcc,
-               (accumulate || kk > 0) ? 1u : 0u);
+        if constexpr (BM)
+            mma_ts_lanes(tacc, ta + packed_col(q), b + kk * (2048 >> 4), BwdCfg<D>::kIdescAcc, 1u, off_lo, off_hi);
+        else
+            mma_ts(tacc, ta + packed_col(q), b + kk * (2048 >> 4), BwdCfg<D>::kIdescAcc,
+                   (accumulate || kk > 0) ? 1u : 0u);
     }
 }
 
@@ -605,11 +614,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int hv = 0; hv < 2 && ok; ++hv) {
                     if (!(ok = wait_bar(BAR(kBarEw0 + hv), i & 1u, abort_flag, A.status))) break;
                     tc_fence_after();
+                    const int mk = BM ? (entry(i) & 15) : 15;
                     if (KV) {
-                        mma_acc_half<D>(tAcc0, slot(hv), base + L::buf(b, 1), hv, i > 0);       // dV += P^T dO_t
-                        mma_acc_half<D>(tAcc1, slot(hv) + 64, base + L::buf(b, 0), hv, i > 0);  // dK += dS^T Q_t
+                        mma_acc_half<D, BM>(tAcc0, slot(hv), base + L::buf(b, 1), hv, i > 0, mk);       // dV += P^T dO_t
+                        mma_acc_half<D, BM>(tAcc1, slot(hv) + 64, base + L::buf(b, 0), hv, i > 0, mk);  // dK += dS^T Q_t
                     } else {
-                        mma_acc_half<D>(tAcc0, slot(hv), base + L::buf(b, 0), hv, i > 0);       // dQ += dS K_j
+                        mma_acc_half<D, BM>(tAcc0, slot(hv), base + L::buf(b, 0), hv, i > 0, mk);       // dQ += dS K_j
                     }
                     mma_commit(BAR(kBarFree0 + hv));
                 }
@@ -633,6 +643,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float ndl_r = KV ? 0.f : __ldg(A.ndelta + xvec_r);
         const int ra = r >> 6;  // this row's 64-row half of the resident tile (warp-uniform)
         bool ok = true;
+        if (BM && n > 0) {
+            // the accumulators start at zero (every masked accumulation adds);
+            // these stores complete before the first arrival on the slot
+            // barrier below (tmem_wait_st there)
+            const uint32_t z[16] = {};
+            const int ncols = KV ? 2 * D : D;  // dV and dK, or dQ
+            for (int cb = h * (ncols / kEwSplit); cb < (h + 1) * (ncols / kEwSplit); cb += 16)
+                tmem_st16(tAcc0 + tl + cb, z);
+        }
         for (int i = 0; i < n; ++i) {
             const int b = i & 1;
             const int32_t e_i = entry(i);

@@ -166,6 +166,24 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
         : "memory");
 }
 
+// mma_ts that leaves some TMEM lanes of D untouched (the instruction's
+// disable-output-lane operand: bit i of the 128-bit mask stops lane i from
+// being written).  off_lo covers lanes 0-63, off_hi lanes 64-127, each as a
+// 32-bit word repeated over its two 32-lane groups: ~0u keeps those lanes as
+// they are, 0 lets the product land.  With two 64-row query tiles in one
+// 128-lane accumulator this keeps a key tile that only one of them selects
+// out of the other's rows entirely, where a zero weight would still turn a
+// non-finite value into NaN (0 * Inf).
+__device__ __forceinline__ void mma_ts_lanes(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                             uint32_t accumulate, uint32_t off_lo, uint32_t off_hi) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, {%5, %5, %6, %6}, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(off_lo), "r"(off_hi)
+        : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 operation issued so far by this
 // thread has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {

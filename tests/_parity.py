@@ -95,3 +95,38 @@ def sample_units(B, H, NT, n, seed, must=()):
     while len(picked) < min(n, total):
         picked.add(int(rng.integers(total)))
     return sorted(picked)
+
+
+def assert_parity_elementwise(gpu: np.ndarray, ref: np.ndarray, block_sizes, units, NT, T, gpu_lse=None,
+                              ref_lse=None, label=""):
+    """Element-by-element comparison for inputs that carry NaN or +-Inf in
+    valid rows: every element the oracle (rounded to FP32) gives as NaN, +Inf
+    or -Inf must be exactly that on the GPU, and the finite elements meet the
+    same bar as ``assert_parity`` (max abs and relative RMS over them).  A
+    non-finite value in a valid V row reaches only some columns of the rows
+    that select it, so rows are not required to be all-NaN here."""
+    bs = np.asarray(block_sizes)
+    ref32 = ref.astype(np.float32)
+    n = gpu.shape[0]
+    valid = np.zeros((n, T), dtype=bool)
+    for i, (_, t) in enumerate(unit_rows(units, NT, T)):
+        valid[i, :int(bs[t])] = True
+    assert (gpu[~valid].view(np.uint32) == 0).all(), f"{label}: padding rows not +0"
+    g, r = gpu[valid], ref32[valid]
+    for name, f in (("NaN", np.isnan), ("+Inf", np.isposinf), ("-Inf", np.isneginf)):
+        bad = f(g) != f(r)
+        assert not bad.any(), f"{label}: {int(bad.sum())} elements differ in being {name}"
+    fin = np.isfinite(r)
+    err = np.abs(g[fin].astype(np.float64) - r[fin])
+    mx = float(err.max()) if err.size else 0.0
+    rel = float(np.linalg.norm(err) / max(np.linalg.norm(r[fin].astype(np.float64)), 1e-30))
+    assert mx <= MAX_ABS and rel <= REL_RMS, f"{label}: max abs {mx:.3e}, rel rms {rel:.3e}"
+    if gpu_lse is not None:
+        gl, rl = gpu_lse[valid], ref_lse.astype(np.float32)[valid]
+        for name, f in (("NaN", np.isnan), ("+Inf", np.isposinf), ("-Inf", np.isneginf)):
+            assert (f(gl) == f(rl)).all(), f"{label}: lse differs in being {name}"
+        lf = np.isfinite(rl)
+        diff = np.abs(gl[lf].astype(np.float64) - rl[lf])
+        assert (diff <= LSE_ABS + LSE_REL * np.abs(rl[lf].astype(np.float64))).all(), f"{label}: lse"
+    print(f"[parity] {label}: {int((~fin).sum())} non-finite elements matched, "
+          f"finite max abs {mx:.3e}, rel rms {rel:.3e}")

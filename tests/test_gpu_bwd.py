@@ -146,3 +146,51 @@ def test_bwd_odd_64_tiles_leave_next_head_alone(vsa):
                                             cd[:, sl].contiguous(), bsd, T)
         for full_g, one in zip((dq, dk, dv), g1):
             assert torch.equal(full_g[:, sl].view(torch.int16), one.view(torch.int16)), f"head {h}"
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_bwd_t64_pair_isolation(vsa, oracle_mod, D):
+    """64-token tiles share 128-row kernel tiles in pairs.  NaN in a VALID row
+    of Q, K or dO reaches exactly the gradients the definition sends it to:
+    query tile t selects key tiles t and t + 3 (of 6), so no key tile serves
+    both tiles of a pair, and the partner's gradients (where a zero weight
+    times NaN would otherwise be NaN) must stay finite and match the oracle.
+    Every element's NaN-ness must match the oracle's."""
+    B, H, NT, T = 1, 2, 6, 64
+    g = torch.Generator().manual_seed(4100 + D)
+    bs = torch.full((NT,), T, dtype=torch.int32)
+    idx = torch.empty((B, H, NT, 2), dtype=torch.int32)
+    for t in range(NT):
+        idx[:, :, t, 0] = t
+        idx[:, :, t, 1] = (t + NT // 2) % NT
+    counts = torch.full((B, H, NT), 2, dtype=torch.int32)
+    q, k, v, do = (torch.randn((B, H, NT * T, D), generator=g).to(torch.bfloat16) for _ in range(4))
+    nan = float("nan")
+    q[0, 0, 0 * 64 + 5, 3] = nan     # head 0: a query row of tile 0 (its dK reaches key tiles 1 and 2)
+    k[0, 1, 2 * 64 + 7, 9] = nan     # head 1: a key row of tile 2 (its dQ reaches query tile 3)
+    do[0, 1, 4 * 64 + 3, 1] = nan    # head 1: a dout row of tile 4 (its dV reaches key tiles 0 and 5)
+    dev = "cuda"
+    qd, kd, vd, dod = (x.to(dev) for x in (q, k, v, do))
+    idd, cd, bsd = idx.to(dev), counts.to(dev), bs.to(dev)
+    out, lse = vsa.block_sparse_attention(qd, kd, vd, idd, cd, bsd, T, want_lse=True)
+    dq, dk, dv = vsa.block_sparse_attention_bwd(qd, kd, vd, out, dod, lse, idd, cd, bsd, T)
+    torch.cuda.synchronize()
+    assert vsa.vsa_check_device_status() == 0
+    refs = oracle_mod.block_sparse_attention_bwd(q, k, v, do, idx, counts, bs, T, 1.0 / math.sqrt(D))
+    for name, got, ref in zip(("dq", "dk", "dv"), (dq, dk, dv), refs):
+        gv = got.float().cpu().numpy().astype(np.float64)
+        rn = np.isnan(ref)
+        assert rn.any() and not rn.all(), name
+        np.testing.assert_array_equal(np.isnan(gv), rn, err_msg=f"D{D} {name}: NaN elements differ")
+        assert np.isfinite(gv[~rn]).all(), f"D{D} {name}: Inf where the oracle is finite"
+        err = gv[~rn] - ref[~rn]
+        rel = float(np.linalg.norm(err) / max(np.linalg.norm(ref[~rn]), 1e-30))
+        mx, scale = float(np.abs(err).max()), float(np.abs(ref[~rn]).max())
+        print(f"[bwd] pairs D{D} {name}: {int(rn.sum())} NaN matched, rel rms {rel:.3e}, max abs {mx:.3e}")
+        assert rel <= REL_RMS and mx <= MAX_REL * scale, f"D{D} {name}: rel rms {rel:.3e}, max abs {mx:.3e}"
+    # the partners named above are finite: dK of key tiles 1, 2 (head 0),
+    # dQ of query tile 3 and dV of key tile 0 (head 1; key tile 5's dV is NaN
+    # by the definition, since query tiles 2 and 5 meet the NaN key)
+    for h, tens, tiles in ((0, dk, (1, 2)), (1, dq, (3,)), (1, dv, (0,))):
+        for t in tiles:
+            assert torch.isfinite(tens[0, h, t * 64:(t + 1) * 64].float()).all(), (h, t)
