@@ -93,32 +93,33 @@ def test_ragged_nan_padding_full(vsa, oracle_mod):
         assert torch.isneginf(lse[b, h, t * 64:(t + 1) * 64]).all()
 
 
-def test_uniform_sampled(vsa, oracle_mod):
+def test_uniform_full(vsa, oracle_mod):
+    """Full size, every one of the 1536 query tiles against the oracle."""
     w = W.make_workload(2)
     (q, k, v), refs = _to_tile_major(w, vsa, oracle_mod)
     out, lse = _run(vsa, q, k, v, w)
-    units = PT.sample_units(w.B, w.H, w.NT, 24, seed=2, must=(0, w.B * w.H * w.NT - 1))
-    _check(w, out, lse, refs, oracle_mod, units, "uniform")
+    _check(w, out, lse, refs, oracle_mod, list(range(w.B * w.H * w.NT)), "uniform")
     assert torch.isfinite(out.float()).all()
 
 
-def test_video_topk_sampled(vsa, oracle_mod):
+def test_video_topk_full(vsa, oracle_mod):
+    """Full size, every one of the 4032 query tiles (ragged cubes) against the oracle."""
     w = W.make_workload(4)
     (q, k, v), refs = _to_tile_major(w, vsa, oracle_mod)
     out, lse = _run(vsa, q, k, v, w)
-    partial = [t for t in range(w.NT) if int(w.block_sizes[t]) < 128]
-    must = [h * w.NT + t for h, t in ((0, partial[0]), (5, partial[-1]), (11, w.NT - 1))]
-    units = PT.sample_units(w.B, w.H, w.NT, 24, seed=4, must=must)
-    _check(w, out, lse, refs, oracle_mod, units, "video")
+    _check(w, out, lse, refs, oracle_mod, list(range(w.B * w.H * w.NT)), "video")
 
 
 def test_dense_limit_sampled(vsa, oracle_mod):
-    """Full size, in the bench's launch configuration (layout + attention, LSE on)."""
+    """Full size, in the bench's launch configuration (layout + attention, LSE
+    on): 160 of the 1464 query tiles (11 %) against the oracle, the tail tile
+    of every head among them, and properties over the whole output."""
     w = W.make_workload(5)
     (q, k, v), refs = _to_tile_major(w, vsa, oracle_mod)
     out, lse = _run(vsa, q, k, v, w)
     last = w.NT - 1
-    units = PT.sample_units(w.B, w.H, w.NT, 16, seed=5, must=(last, w.H * w.NT - 1, 0))
+    must = [h * w.NT + last for h in range(w.H)] + [0]
+    units = PT.sample_units(w.B, w.H, w.NT, 160, seed=5, must=must)
     _check(w, out, lse, refs, oracle_mod, units, "dense")
     # properties over the whole output: valid rows finite, padding rows +0
     assert torch.isfinite(out[:, :, :31200].float()).all()
@@ -209,6 +210,67 @@ def test_nan_in_valid_key_gives_nan_rows(vsa, oracle_mod):
     assert any(sel)
     for t in range(5):
         assert bool(torch.isnan(out[0, 1, t * 64:(t + 1) * 64].float()).all()) == sel[t]
+
+
+def _pair_case(seed, D, NT=6, ragged=False):
+    """64-token tiles whose pairs (2i, 2i+1) select disjoint key tiles: query
+    tile t selects key tiles t and (t + NT/2) mod NT, so every key tile serves
+    exactly one tile of one pair and two pairs in all."""
+    T, B, H = 64, 1, 2
+    g = torch.Generator().manual_seed(seed)
+    bs = torch.full((NT,), T, dtype=torch.int32)
+    if ragged:
+        bs = torch.randint(24, T + 1, (NT,), generator=g).int()
+    idx = torch.empty((B, H, NT, 2), dtype=torch.int32)
+    for t in range(NT):
+        idx[:, :, t, 0] = t
+        idx[:, :, t, 1] = (t + NT // 2) % NT
+    num = torch.full((B, H, NT), 2, dtype=torch.int32)
+    q, k, v = (torch.randn((B, H, NT * T, D), generator=g).to(torch.bfloat16) for _ in range(3))
+    if ragged:
+        q, k, v = (W.pad_tile_major(x, bs, T, "naninf") for x in (q, k, v))
+    return W.Workload("pairs", B, H, D, T, NT, bs, idx, num, 1.0 / math.sqrt(D), True, q=q, k=k, v=v)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("where", ["v", "k"])
+@pytest.mark.parametrize("ragged", [False, True])
+def test_t64_pair_isolation(vsa, oracle_mod, D, where, ragged):
+    """Two 64-token query tiles share one 128-lane accumulator.  A NaN, +Inf or
+    -Inf in a VALID row of a key tile that only one tile of the pair selects
+    must reach only that tile's rows, as in the definition (each query tile
+    attends to its own list); the partner tile's rows stay finite and match
+    the oracle, and every non-finite element matches the oracle's exactly."""
+    w = _pair_case(900 + D + (1 if ragged else 0), D, ragged=ragged)
+    x = (w.v if where == "v" else w.k).clone()
+    # key tiles 0 and 3 are selected by query tiles 0 and 3 only, whose pair
+    # partners (1 and 2) select neither; head 0 gets infinities only (a NaN in
+    # K makes whole rows NaN and would hide them), head 1 NaN and +Inf
+    inf, nan = float("inf"), float("nan")
+    plant = {0: ((0, 9, 3, inf), (3, 20, D - 3, -inf), (0, 21, 8, -inf)),
+             1: ((0, 5, 7, nan), (3, 2, 11, inf), (3, 17, 0, nan))}
+    for h, cells in plant.items():
+        for j, r, c, val in cells:
+            assert r < int(w.block_sizes[j])
+            x[0, h, j * 64 + r, c] = val
+    if where == "v":
+        w.v = x
+    else:
+        w.k = x
+    (q, k, v), refs = _to_tile_major(w, vsa, oracle_mod)
+    out, lse = _run(vsa, q, k, v, w)
+    units = list(range(w.B * w.H * w.NT))
+    ref, ref_lse = oracle_mod.block_sparse_attention(refs[0], refs[1], refs[2], w.q2k_idx, w.q2k_num,
+                                                     w.block_sizes, w.T, w.scale, units=units)
+    g = PT.gather_gpu_units(out, units, w.NT, w.T)
+    gl = PT.gather_gpu_lse(lse, units, w.NT, w.T)
+    PT.assert_parity_elementwise(g, ref, w.block_sizes.numpy(), units, w.NT, w.T, gl, ref_lse,
+                                 label=f"pairs {where} D{D}{' ragged' if ragged else ''}")
+    # the pair partners of the tiles that meet the planted values stay finite
+    for h in range(2):
+        for t in (1, 2, 4, 5):
+            assert torch.isfinite(out[0, h, t * 64:t * 64 + int(w.block_sizes[t])].float()).all(), (h, t)
+    assert not np.isfinite(g).all()
 
 
 def test_deterministic(vsa, oracle_mod):
