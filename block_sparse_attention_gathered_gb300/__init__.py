@@ -73,6 +73,7 @@ def _load() -> ctypes.CDLL:
         "vsa_check_device_status": ([P], i32),
         "vsa_wait_probe": ([i32, ctypes.c_uint32, P], i32),
         "vsa_last_route": ([ctypes.POINTER(VsaRoute)], i32),
+        "vsa_last_step_counts": ([ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int64)], i32),
         "vsa_status_string": ([i32], ctypes.c_char_p),
         "vsa_version": ([], i32),
     }
@@ -86,7 +87,8 @@ _lib = _load()
 EXPORTED = ("vsa_block_sparse_workspace_size", "vsa_block_sparse_fwd", "vsa_block_sparse_fwd_noalloc",
             "vsa_block_sparse_bwd_workspace_size", "vsa_block_sparse_bwd", "vsa_tile_layout", "vsa_untile",
             "vsa_coarse_select_workspace_size", "vsa_coarse_select", "vsa_validate_indices",
-            "vsa_check_device_status", "vsa_wait_probe", "vsa_last_route", "vsa_status_string", "vsa_version")
+            "vsa_check_device_status", "vsa_wait_probe", "vsa_last_route", "vsa_last_step_counts",
+            "vsa_status_string", "vsa_version")
 
 
 def library() -> ctypes.CDLL:
@@ -215,6 +217,16 @@ def vsa_last_route() -> dict:
     if st != VSA_OK:
         raise VsaError(st, "vsa_last_route")
     return r.as_dict()
+
+
+def vsa_last_step_counts() -> tuple:
+    """(tail_steps, full_steps) of the last forward call on the current device
+    (waits for the device)."""
+    tail, full = ctypes.c_int64(0), ctypes.c_int64(0)
+    st = _lib.vsa_last_step_counts(ctypes.byref(tail), ctypes.byref(full))
+    if st != VSA_OK:
+        raise VsaError(st, "vsa_last_step_counts")
+    return int(tail.value), int(full.value)
 
 
 # ------------------------------------------------------------------ helpers

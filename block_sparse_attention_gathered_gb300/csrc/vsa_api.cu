@@ -21,14 +21,22 @@ namespace vsa {
 namespace {
 
 __device__ int32_t g_device_status;  // bits kFlag*; read and cleared by vsa_check_device_status
+// (tail, full) key-tile steps of the last forward call: zeroed by the ordering
+// kernel, counted by the attention kernel, read by vsa_last_step_counts
+__device__ unsigned long long g_step_counts[2];
 
 constexpr int kMaxDevices = 64;
 
 struct DeviceCache {
     std::atomic<int> state{0};  // 0 unknown, 1 supported sm_103, -1 unsupported
+    // the context the entries below were taken in: after cudaDeviceReset the
+    // device gets a new context, a new address for the status word and no
+    // function attributes, so the entry is rebuilt
+    std::atomic<unsigned long long> ctx_id{0};
     std::atomic<int> sm_count{0};
     std::atomic<unsigned> attn_prepared{0};  // bit per (tile, head_dim) variant
     std::atomic<int32_t *> status_ptr{nullptr};
+    std::atomic<unsigned long long *> steps_ptr{nullptr};
 };
 DeviceCache g_dev[kMaxDevices];
 
@@ -55,6 +63,36 @@ EncodeTiledFn encode_fn() {
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long *);
+std::once_flag g_ctx_once;
+CtxGetCurrentFn g_ctx_current = nullptr;
+CtxGetIdFn g_ctx_id = nullptr;
+
+}  // namespace
+
+unsigned long long current_context_id() {
+    std::call_once(g_ctx_once, [] {
+        void *a = nullptr, *b = nullptr;
+        cudaDriverEntryPointQueryResult qa, qb;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &a, 12000, cudaEnableDefault, &qa) == cudaSuccess &&
+            qa == cudaDriverEntryPointSuccess &&
+            cudaGetDriverEntryPointByVersion("cuCtxGetId", &b, 12000, cudaEnableDefault, &qb) == cudaSuccess &&
+            qb == cudaDriverEntryPointSuccess) {
+            g_ctx_current = reinterpret_cast<CtxGetCurrentFn>(a);
+            g_ctx_id = reinterpret_cast<CtxGetIdFn>(b);
+        }
+        cudaGetLastError();
+    });
+    if (!g_ctx_current || !g_ctx_id) return 0;
+    CUcontext c = nullptr;
+    unsigned long long id = 0;
+    if (g_ctx_current(&c) != CUDA_SUCCESS || c == nullptr || g_ctx_id(c, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
+
+namespace {
+
 // Current device, checked to be an sm_103 part; fills its cache entry.
 vsa_status current_device(int *dev_out) {
     int dev = 0;
@@ -65,6 +103,11 @@ vsa_status current_device(int *dev_out) {
     if (dev < 0 || dev >= kMaxDevices) return VSA_ERR_ARCH;
     DeviceCache &c = g_dev[dev];
     int st = c.state.load(std::memory_order_acquire);
+    if (st == 1 && c.ctx_id.load(std::memory_order_acquire) != current_context_id()) {
+        // a new context since the entry was made (cudaDeviceReset): take it afresh
+        c.attn_prepared.store(0u, std::memory_order_release);
+        st = 0;
+    }
     if (st == 0) {
         int major = 0, minor = 0, sms = 0;
         if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
@@ -80,8 +123,15 @@ vsa_status current_device(int *dev_out) {
                 cudaGetLastError();
                 return VSA_ERR_CUDA;
             }
+            unsigned long long *steps = nullptr;
+            if (cudaGetSymbolAddress(reinterpret_cast<void **>(&steps), g_step_counts) != cudaSuccess) {
+                cudaGetLastError();
+                return VSA_ERR_CUDA;
+            }
             c.status_ptr.store(p, std::memory_order_release);
+            c.steps_ptr.store(steps, std::memory_order_release);
             c.sm_count.store(sms, std::memory_order_release);
+            c.ctx_id.store(current_context_id(), std::memory_order_release);  // the symbol lookup made it current
         }
         c.state.store(st, std::memory_order_release);
     }
@@ -141,7 +191,8 @@ constexpr int kSchedThreads = 1024;
 
 __global__ void __launch_bounds__(kSchedThreads)
     schedule_kernel(const int32_t *__restrict__ q2k_num, int NT, int T, int max_kv, int G, int n_items, int bins,
-                    int split, int32_t *__restrict__ order, int32_t *__restrict__ counter) {
+                    int split, int32_t *__restrict__ order, int32_t *__restrict__ counter,
+                    unsigned long long *__restrict__ steps) {
     extern __shared__ int32_t sh[];
     int32_t *hist = sh;          // [bins], indexed by descending rank
     int32_t *cursor = sh + bins;  // [bins]
@@ -210,7 +261,11 @@ __global__ void __launch_bounds__(kSchedThreads)
             order[q + 1] = (i << 2) | 2;
         }
     }
-    if (tid == 0) *counter = 0;
+    if (tid == 0) {
+        *counter = 0;
+        steps[0] = 0ull;
+        steps[1] = 0ull;
+    }
 }
 
 // ------------------------------------------------------------------ validate
@@ -322,7 +377,8 @@ vsa_status vsa_block_sparse_fwd(const void *q, const void *k, const void *v, con
     const int rem = n_items > grid ? n_items % grid : 0;
     const int split = (rem > 0 && 2 * rem <= grid && rem <= kMaxSplit) ? rem : 0;
     schedule_kernel<<<1, kSchedThreads, 2 * bins * sizeof(int32_t), s>>>(q2k_num, NT, T, dims->max_kv, G, n_items,
-                                                                        bins, split, order, counter);
+                                                                        bins, split, order, counter,
+                                                                        dc.steps_ptr.load(std::memory_order_acquire));
     if (cudaGetLastError() != cudaSuccess) return VSA_ERR_CUDA;
 
     AttnParams p;
@@ -334,6 +390,7 @@ vsa_status vsa_block_sparse_fwd(const void *q, const void *k, const void *v, con
     p.order = order;
     p.work_counter = counter;
     p.status = dc.status_ptr.load(std::memory_order_acquire);
+    p.steps = dc.steps_ptr.load(std::memory_order_acquire);
     p.NT = NT * sub;
     p.sub = sub;
     p.max_kv = dims->max_kv;
@@ -687,6 +744,21 @@ vsa_status vsa_check_device_status(vsa_stream_t stream) {
 vsa_status vsa_last_route(vsa_route *route) {
     if (!route) return VSA_ERR_ARG;
     *route = t_route;
+    return VSA_OK;
+}
+
+vsa_status vsa_last_step_counts(int64_t *tail_steps, int64_t *full_steps) {
+    if (!tail_steps || !full_steps) return VSA_ERR_ARG;
+    int dev = 0;
+    vsa_status st = current_device(&dev);
+    if (st != VSA_OK) return st;
+    unsigned long long c[2] = {0ull, 0ull};
+    if (cudaDeviceSynchronize() != cudaSuccess || cudaMemcpyFromSymbol(c, g_step_counts, sizeof c) != cudaSuccess) {
+        cudaGetLastError();
+        return VSA_ERR_CUDA;
+    }
+    *tail_steps = (int64_t)c[0];
+    *full_steps = (int64_t)c[1];
     return VSA_OK;
 }
 

@@ -43,6 +43,12 @@
 //     one control warp zeroes the few padding rows inside the last block in
 //     shared memory first, so NaN/Inf padding in V never meets a zero weight
 //     (0 * NaN = NaN).
+//   * With 64-token tiles a unit is two query tiles in one 128-lane
+//     accumulator; a P V with a key tile only one of them selects disables
+//     the other's 64 output lanes, so each tile's O holds its own key tiles
+//     only (O is zeroed at the start of an item and every P V accumulates).
+//   * The producer counts the (query tile, key tile) steps it hands out,
+//     tail and full, into a device word the host reads for route checks.
 //   * 20 warps: four softmax warpgroups, then a control warpgroup (three
 //     MMA-issuing warps, one of which zeroes tail V rows, and the TMA
 //     producer) that hands registers to the softmax warpgroups with
@@ -319,6 +325,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             const int item = entry < 0 ? -1 : entry >> 2, mode = entry < 0 ? 0 : entry & 3;
             uint32_t *bmp = bm + p * 4 * W;
             int bad = 0;
+            uint32_t n_tail = 0, n_full = 0;  // this lane's (query tile, key tile) steps
             if (item >= 0) {
                 for (int i = lane; i < 4 * W; i += 32) bmp[i] = 0u;
                 __syncwarp();
@@ -346,10 +353,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         }
                         for (int h2 = 0; h2 < sub; ++h2) {
                             const int jj = j * sub + h2;
-                            if (tile_size(P.block_sizes, jj, sub) <= 0) continue;
+                            const int nj = tile_size(P.block_sizes, jj, sub);
+                            if (nj <= 0) continue;
                             const uint32_t bit = 1u << (jj & 31);
                             const uint32_t old = atomicOr(&bmp[s * W + (jj >> 5)], bit);
-                            if (old & bit) bad = 1;  // repeated index
+                            if (old & bit) {
+                                bad = 1;  // repeated index
+                            } else if (nj < T) {
+                                ++n_tail;  // the softmax masks this step's columns past nj
+                            } else {
+                                ++n_full;
+                            }
                         }
                     }
                 }
@@ -361,6 +375,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 hdr[p * 4] = -1;
             }
             if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(P.status, kFlagIndex);
+            n_tail = __reduce_add_sync(0xffffffffu, n_tail);
+            n_full = __reduce_add_sync(0xffffffffu, n_full);
+            if (lane == 0 && (n_tail | n_full)) {
+                atomicAdd(P.steps, (unsigned long long)n_tail);
+                atomicAdd(P.steps + 1, (unsigned long long)n_full);
+            }
             __syncwarp();
             mbar_arrive(BAR(BI.bm_full(p)));
             if (item < 0) break;

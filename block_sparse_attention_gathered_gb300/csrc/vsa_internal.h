@@ -26,6 +26,7 @@ struct AttnParams {
     const int32_t *order;        // [n_items] work order (longest first)
     int32_t *work_counter;       // next slot of `order` to hand out
     int32_t *status;             // device status word
+    unsigned long long *steps;   // (tail, full) key-tile steps, added to by the producer warps
     int32_t NT;                  // kernel tiles (128-token halves when sub == 2)
     int32_t sub;                 // kernel tiles per caller tile: 1, or 2 for 256-token tiles
     int32_t max_kv;
@@ -137,6 +138,12 @@ int select_rows(int NT, int D);
 size_t select_smem_bytes(int NT, int D, int rows);
 cudaError_t select_prepare();
 cudaError_t launch_select(const SelectParams &p, cudaStream_t stream);
+
+// 64-bit ID of the calling thread's current CUDA context (unique for the
+// process's life, so a context made after cudaDeviceReset gets a new one), or
+// 0 when there is none yet or the driver cannot say.  Per-device caches of
+// device addresses and function attributes are keyed on it.
+unsigned long long current_context_id();
 
 // Bounded-wait probe (vsa_check.cu).
 cudaError_t launch_wait_probe(int32_t arrive, uint64_t limit_ns, int32_t *status, cudaStream_t stream);

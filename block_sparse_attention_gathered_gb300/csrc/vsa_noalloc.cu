@@ -16,22 +16,33 @@
 // even though the array keeps the last call's contents.  All calls on a
 // device share the one array: calls that can overlap on the GPU (different
 // streams without ordering between them) race and give wrong results.
-#include <atomic>
+#include <mutex>
 
 #include <cuda_runtime.h>
 
 #include "vsa.h"
+#include "vsa_internal.h"
 
 namespace {
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[VSA_NOALLOC_SCRATCH_BYTES];
 
 constexpr int kMaxDevices = 64;
-std::atomic<void *> g_scratch_addr[kMaxDevices];
+
+// Per device: the scratch array's device address and the context it was
+// looked up in.  The address belongs to that context: after cudaDeviceReset
+// the module is loaded again in a new context and the array moves, so a
+// changed context ID means a fresh lookup.
+struct ScratchEntry {
+    std::mutex lock;
+    unsigned long long ctx = 0;
+    void *addr = nullptr;
+};
+ScratchEntry g_scratch[kMaxDevices];
 
 // Device address of the scratch array on the current device, looked up once
-// per device (the name is only a host-side handle and must not be passed to a
-// kernel directly).
+// per device and context (the array's name is only a host-side handle and must
+// not be passed to a kernel directly).
 vsa_status scratch_address(void **out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) {
@@ -39,8 +50,9 @@ vsa_status scratch_address(void **out) {
         return VSA_ERR_CUDA;
     }
     if (dev < 0 || dev >= kMaxDevices) return VSA_ERR_ARCH;
-    void *p = g_scratch_addr[dev].load(std::memory_order_acquire);
-    if (!p) {
+    ScratchEntry &e = g_scratch[dev];
+    std::lock_guard<std::mutex> g(e.lock);
+    if (e.addr == nullptr || e.ctx != vsa::current_context_id()) {
         int major = 0, minor = 0;
         if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
@@ -48,13 +60,16 @@ vsa_status scratch_address(void **out) {
             return VSA_ERR_CUDA;
         }
         if (major != 10 || minor != 3) return VSA_ERR_ARCH;
+        void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
             cudaGetLastError();
+            e.addr = nullptr;
             return VSA_ERR_CUDA;
         }
-        g_scratch_addr[dev].store(p, std::memory_order_release);
+        e.addr = p;
+        e.ctx = vsa::current_context_id();  // the lookup made the device's context current
     }
-    *out = p;
+    *out = e.addr;
     return VSA_OK;
 }
 

@@ -133,9 +133,9 @@ size_t vsa_block_sparse_workspace_size(const vsa_dims *dims);
  * Out-of-range or repeated indices and out-of-range counts never fault: they
  * are skipped / clamped and flagged as VSA_ERR_INDEX in the device status
  * word.  Use vsa_validate_indices() to check a selection up front.
- * With tile == 64, two tiles share one 128-row MMA; a non-finite value in a
- * VALID V row can then also reach the rows of the paired tile (padding rows
- * are always safe).
+ * With tile == 64, two tiles share one 128-row MMA; a product with a key tile
+ * that only one of them selects leaves the other's rows out entirely, so NaN
+ * or Inf in a valid row reaches only the tiles that select it.
  */
 vsa_status vsa_block_sparse_fwd(const void *q, const void *k, const void *v, const int32_t *q2k_idx,
                                 const int32_t *q2k_num, const int32_t *block_sizes, void *out,
@@ -154,11 +154,17 @@ vsa_status vsa_block_sparse_fwd(const void *q, const void *k, const void *v, con
  * available to the caller -- host callbacks, plug-ins whose device memory is
  * owned by a host framework, or code that must keep a fixed footprint.
  *
- *   - Problems needing more scratch than the array holds (more than
- *     (VSA_NOALLOC_SCRATCH_BYTES - 256) / 4 work items of 256 query rows)
- *     return VSA_ERR_LIMITS before anything is launched.
+ *   - Problems needing more scratch than the array holds return
+ *     VSA_ERR_LIMITS before anything is launched.  The scratch of a problem is
+ *     vsa_block_sparse_workspace_size(): a 256-byte header plus 4 bytes per
+ *     work item (256 query rows of one (batch, head)) and 4 bytes for each of
+ *     up to 256 split entries, so at most
+ *     (VSA_NOALLOC_SCRATCH_BYTES - 256) / 4 - 256 = 261,824 work items fit.
  *   - The first call on a device looks up the array's device address; make
- *     that first call before any stream capture on the device.
+ *     that first call before any stream capture on the device.  The address
+ *     belongs to the device's current context: after cudaDeviceReset (a new
+ *     context) the next call looks it up again, so that call too must come
+ *     before any capture.
  *   - Calls allocate nothing (no cudaMalloc / cudaFree).  Every call on a
  *     device shares the one array: calls that may run concurrently on the GPU
  *     race on it and must be ordered by the caller (one stream, or events).
@@ -209,9 +215,9 @@ vsa_status vsa_tile_layout(const void *q_tok, const void *k_tok, const void *v_t
  *                       (0 for invalid dims)
  * The kernels work on 128-row tiles: a 256-token tile as two halves, two
  * 64-token tiles together with a mask of which 64 x 64 blocks are selected.
- * As in the forward with tile == 64, a non-finite value in a VALID row of
- * one 64-token tile can then reach the gradients of the paired tile through
- * a zero weight (padding rows are zeroed first and never do).
+ * Accumulations over a 64 x 64 block the selection leaves out do not touch
+ * the rows of that block at all, so, as in the forward, NaN or Inf in a valid
+ * row reaches only the gradients the definition sends it to.
  * Deterministic: dQ is recomputed per query tile instead of accumulated with
  * atomics, and dK/dV sum their query tiles in ascending order.
  */
@@ -311,6 +317,24 @@ vsa_status vsa_wait_probe(int32_t arrive, uint32_t limit_us, vsa_stream_t stream
 
 /* Route of the last successful launch on the calling host thread. */
 vsa_status vsa_last_route(vsa_route *route);
+
+/*
+ * Key-tile steps of the last vsa_block_sparse_fwd (or _noalloc) call on the
+ * current device, for route assertions in tests (the sm_121a hardening commit:
+ * tests assert which route ran; the Attn-QAT SM100 commit: full key tiles run
+ * unmasked, the tail tile in a separate masked step).  A step is one query
+ * tile of the kernel (64 or 128 tokens; a 128-token half of a 256-token tile)
+ * against one selected key tile (likewise) with at least one valid key.
+ *   tail_steps  steps whose key tile holds fewer valid keys than the tile:
+ *               the softmax masks the columns past the valid count and P V
+ *               reads only the 16-key blocks holding valid keys
+ *   full_steps  steps with a full key tile: no mask at all
+ * The counts are made on the device (zeroed by the call's ordering kernel,
+ * added to by the attention kernel), so this call waits for the device to
+ * finish (cudaDeviceSynchronize): not for use inside stream capture.  Calls
+ * that overlap on the GPU add to the same counts.
+ */
+vsa_status vsa_last_step_counts(int64_t *tail_steps, int64_t *full_steps);
 
 /* Static description of a status code. */
 const char *vsa_status_string(vsa_status status);

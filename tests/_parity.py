@@ -130,3 +130,32 @@ def assert_parity_elementwise(gpu: np.ndarray, ref: np.ndarray, block_sizes, uni
         assert (diff <= LSE_ABS + LSE_REL * np.abs(rl[lf].astype(np.float64))).all(), f"{label}: lse"
     print(f"[parity] {label}: {int((~fin).sum())} non-finite elements matched, "
           f"finite max abs {mx:.3e}, rel rms {rel:.3e}")
+
+
+def expected_step_counts(q2k_idx, q2k_num, block_sizes, T):
+    """(tail, full) key-tile steps the attention kernel reports for a valid
+    selection, counted on the host: one step per (query kernel tile, selected
+    key kernel tile with a valid key); tail when the key tile is partly filled.
+    Kernel tiles are the caller's tiles, or the 128-token halves of 256-token
+    tiles (both halves of a query tile run, each against every key half)."""
+    idx = np.asarray(q2k_idx).reshape(-1, np.asarray(q2k_idx).shape[-1]) if np.asarray(q2k_idx).size else None
+    num = np.asarray(q2k_num).reshape(-1)
+    bs = np.asarray(block_sizes).astype(np.int64)
+    if T == 256:
+        halves = np.stack([np.clip(bs, 0, 128), np.clip(bs - 128, 0, 128)], axis=1)  # [NT, 2]
+        per_key_tail = ((halves > 0) & (halves < 128)).sum(1)
+        per_key_full = (halves == 128).sum(1)
+        q_mult = 2
+    else:
+        per_key_tail = ((bs > 0) & (bs < T)).astype(np.int64)
+        per_key_full = (bs == T).astype(np.int64)
+        q_mult = 1
+    tail = full = 0
+    for row in range(num.shape[0]):
+        n = int(num[row])
+        if n == 0:
+            continue
+        sel = idx[row, :n]
+        tail += int(per_key_tail[sel].sum())
+        full += int(per_key_full[sel].sum())
+    return q_mult * tail, q_mult * full

@@ -59,6 +59,14 @@ def _run(vsa, q, k, v, w, scale=None):
     return res
 
 
+def _check_steps(vsa, w):
+    """The route's step counts: full key tiles unmasked, partly filled ones masked."""
+    got = vsa.vsa_last_step_counts()
+    want = PT.expected_step_counts(w.q2k_idx, w.q2k_num, w.block_sizes, w.T)
+    assert got == want, f"(tail, full) steps {got}, expected {want}"
+    return got
+
+
 def _check(w, gpu_out, gpu_lse, refs, oracle_mod, units, label):
     ref, ref_lse = oracle_mod.block_sparse_attention(refs[0], refs[1], refs[2], w.q2k_idx, w.q2k_num,
                                                      w.block_sizes, w.T, w.scale, units=units)
@@ -73,6 +81,7 @@ def test_tiny_full(vsa, oracle_mod):
     out, lse = _run(vsa, q, k, v, w)
     units = list(range(w.B * w.H * w.NT))
     _check(w, out, lse, refs, oracle_mod, units, "tiny")
+    assert _check_steps(vsa, w) == (0, 2 * 4 * 2)
     r = vsa.vsa_last_route()
     assert r["kernel"] == vsa.VSA_KERNEL_ATTN_TCGEN05 and (r["tile"], r["head_dim"]) == (64, 64)
     assert r["work_items"] == 2 and r["grid"] == 2
@@ -84,6 +93,7 @@ def test_ragged_nan_padding_full(vsa, oracle_mod):
     out, lse = _run(vsa, q, k, v, w)
     units = list(range(w.B * w.H * w.NT))
     _check(w, out, lse, refs, oracle_mod, units, "ragged")
+    _check_steps(vsa, w)
     # empty selections give exactly +0 and -inf
     empty = (w.q2k_num == 0).nonzero().tolist()
     assert empty
@@ -108,6 +118,8 @@ def test_video_topk_full(vsa, oracle_mod):
     (q, k, v), refs = _to_tile_major(w, vsa, oracle_mod)
     out, lse = _run(vsa, q, k, v, w)
     _check(w, out, lse, refs, oracle_mod, list(range(w.B * w.H * w.NT)), "video")
+    tail, full = _check_steps(vsa, w)
+    assert tail > 0 and full > 0
 
 
 def test_dense_limit_sampled(vsa, oracle_mod):
@@ -125,6 +137,8 @@ def test_dense_limit_sampled(vsa, oracle_mod):
     assert torch.isfinite(out[:, :, :31200].float()).all()
     assert (out[:, :, 31200:].view(torch.int16) == 0).all()
     assert torch.isneginf(lse[:, :, 31200:]).all() and torch.isfinite(lse[:, :, :31200]).all()
+    # one masked step per query tile (the 96-token tail key tile), 243 full ones
+    assert _check_steps(vsa, w) == (6 * 244, 6 * 244 * 243)
     r = vsa.vsa_last_route()
     assert r["kernel"] == vsa.VSA_KERNEL_ATTN_TCGEN05 and (r["tile"], r["head_dim"]) == (128, 128)
     assert r["work_items"] == 6 * 122
@@ -154,6 +168,7 @@ def test_variants_ragged(vsa, oracle_mod, T, D, NT):
     (q, k, v), refs = _to_tile_major(w, vsa, oracle_mod)
     out, lse = _run(vsa, q, k, v, w)
     _check(w, out, lse, refs, oracle_mod, list(range(w.B * w.H * w.NT)), f"T{T}D{D}NT{NT}")
+    _check_steps(vsa, w)
 
 
 def test_many_waves(vsa, oracle_mod):
@@ -178,6 +193,7 @@ def test_split_last_wave(vsa, oracle_mod, T):
     out, lse = _run(vsa, q, k, v, w)
     assert vsa.vsa_last_route()["work_items"] == n_items
     _check(w, out, lse, refs, oracle_mod, list(range(w.B * w.H * w.NT)), f"split T{T}")
+    _check_steps(vsa, w)   # split items count their unit once, on the CTA that runs it
     # bit-identical across runs, although which items are split may differ
     # (items of equal length take their places in any order)
     again, _ = _run(vsa, q, k, v, w)

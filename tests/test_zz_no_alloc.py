@@ -48,6 +48,21 @@ def test_oversized_problem_is_refused_before_launch(vsa):
     assert st == vsa.VSA_ERR_ARG
 
 
+def test_noalloc_limit_at_boundary(vsa):
+    """The scratch of a problem is a 256-byte header plus 4 bytes per work item
+    and per possible split entry (256 of them): exactly 1 MiB holds 261,824
+    work items; one more is refused before anything reaches the device."""
+    fit = vsa.make_dims(1, 64, 8182, 128, 64, 1)      # 64 heads x 4091 items = 261,824
+    over = vsa.make_dims(1, 75, 6982, 128, 64, 1)     # 75 heads x 3491 items = 261,825
+    assert vsa.vsa_block_sparse_workspace_size(fit) == vsa.VSA_NOALLOC_SCRATCH_BYTES
+    assert vsa.vsa_block_sparse_workspace_size(over) == vsa.VSA_NOALLOC_SCRATCH_BYTES + 4
+    assert (vsa.VSA_NOALLOC_SCRATCH_BYTES - 256) // 4 - 256 == 261824
+    fake = ctypes.c_void_p(0x100000)
+    st = vsa.library().vsa_block_sparse_fwd_noalloc(fake, fake, fake, fake, fake, fake, fake, None,
+                                                    ctypes.byref(over), None)
+    assert st == vsa.VSA_ERR_LIMITS
+
+
 def _compare(got, ref, label):
     g, r = got.float(), ref.float()
     gn, rn = torch.isnan(g), torch.isnan(r)
@@ -93,11 +108,18 @@ def test_no_alloc_matches_workspace_entry(vsa, cfg):
     torch.cuda.synchronize()
     assert vsa.vsa_check_device_status() == vsa.VSA_OK
 
+    outs = [torch.full_like(q, float("nan")) for _ in range(2)]
+    lses = [torch.full((B, H, Sp), float("nan"), dtype=torch.float32, device=dev) for _ in range(2)]
     for call in range(2):
-        out = torch.full_like(q, float("nan"))
-        lse = torch.full((B, H, Sp), float("nan"), dtype=torch.float32, device=dev)
+        out, lse = outs[call], lses[call]
+        torch.cuda.synchronize()
+        free_before = torch.cuda.mem_get_info()[0]
         vsa.vsa_block_sparse_fwd_noalloc(q, k, v, idx, num, bs, out, lse, dims)
         torch.cuda.synchronize()
+        # the second call (the first may load the library's device code) must
+        # leave the device's free memory exactly as it was
+        if call == 1:
+            assert torch.cuda.mem_get_info()[0] == free_before, f"{name}: device memory changed"
         assert vsa.vsa_check_device_status() == vsa.VSA_OK
         _compare(out, ref_out, f"{name} call {call} out")
         assert torch.equal(torch.isneginf(lse), torch.isneginf(ref_lse))
