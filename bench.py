@@ -11,6 +11,12 @@ Prints ONE JSON line (rank 0).  ``value`` is effective TFLOPS on selected tiles
 (4*D*sum n_t*n_j over the selected tile pairs, valid tokens only) over the
 device-timed step; ``e2e`` repeats the measurement through the C ABI from
 pinned host buffers with the host<->device copies inside the timed region.
+After the headline step (and outside it) the default run also times the
+backward pass of the same workload (``bwd``) and, each on its own, the other
+workloads (``workloads``: the tiny, uniform, ragged 64-token and video top-k
+cases, and the dense case re-tiled with 64-token tiles at head_dim 128 and 64
+and with 256-token tiles), each with its attention roofline and, for
+token-major inputs, its layout roofline.
 With ``--impl reference`` the CPU oracle is timed instead, on a bounded sample
 of the same workload.
 """
@@ -39,16 +45,26 @@ UNIT = "TFLOP/s"
 FALLBACK_BF16_TFLOPS = 1900.0
 FALLBACK_HBM_GBS = 6800.0
 
-# DRAM bytes (read + write) per attention launch from an ncu capture, keyed by
-# the SHA-256 of the attention kernel source the capture was taken with (or of
-# a source that differs from it in comments only); a changed kernel reports
-# null until it is captured again.
+# DRAM bytes (read + write) per attention launch from one ncu capture of
+# dram__bytes_read.sum + dram__bytes_write.sum, keyed by workload and by the
+# SHA-256 (first 16 hex digits) of the attention kernel source the capture was
+# taken with; a changed kernel reports null until it is captured again.
 ATTN_TRAFFIC = {
-    # profiles/attn_fwd_t128d128_dense_b1h6_s31200.md: 258.6 MB read + 35.0 MB written
-    ("dense_b1h6d128_s31200_t128x244_lse", "777e096d6954504f"): 293.60e6,
-    # profiles/attn_fwd_t128d128_uniform_b1h12_k32.md: 179.2 MB read + 34.8 MB written
-    ("uniform_b1h12d128_t128x128_k32", "777e096d6954504f"): 213.97e6,
+    ("dense_b1h6d128_s31200_t128x244_lse", "777e096d6954504f"): 293.60e6,  # 258.6 MB read + 35.0 MB written
+    ("uniform_b1h12d128_t128x128_k32", "777e096d6954504f"): 213.97e6,      # 179.2 MB read + 34.8 MB written
 }
+
+# Workloads timed after the headline step in the default run (attention, and
+# the tile layout where the inputs are token-major): (label, cfg, tile, head_dim).
+EXTRA_WORKLOADS = (
+    ("tiny", 1, None, None),
+    ("uniform", 2, None, None),
+    ("ragged_t64", 3, None, None),
+    ("video_topk", 4, None, None),
+    ("dense_t64_d128", 5, 64, None),
+    ("dense_t64_d64", 5, 64, 64),
+    ("dense_t256", 5, 256, None),
+)
 
 
 def _rank_env():
@@ -181,7 +197,7 @@ def run_reference(args, cfg):
     rank, world, _ = _rank_env()
     if rank != 0:
         return
-    w = W.make_workload(cfg, tile=args.tile)
+    w = W.make_workload(cfg, tile=args.tile, head_dim=args.head_dim)
     import oracle
     oracle.build()
     nthreads = oracle.default_threads()
@@ -203,11 +219,20 @@ def run_reference(args, cfg):
         "impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "H": w.H, "S": w.S or w.Sp, "head_dim": w.D, "tile": w.T,
-                   "num_tiles": w.NT, "density": round(density(w), 4), "lse": w.want_lse},
+        "config": config_dict(w),
         "cpu_baseline": {"value": val, "unit": UNIT, "cores": nthreads, "kind": "oracle", "sample": sample},
         "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
+
+
+def config_dict(w, eff=None) -> dict:
+    """The ``config`` object of a bench line: the same keys for both arms."""
+    if eff is None:
+        eff = W.effective_flops(w)
+    return {"workload": w.name, "B": w.B, "H": w.H, "S": w.S or w.Sp, "head_dim": w.D, "tile": w.T,
+            "num_tiles": w.NT, "density": round(density(w), 4), "lse": w.want_lse, "effective_flops": eff,
+            "padded_flops": W.padded_flops(w), "l2": "flushed (256 MB write) between steps",
+            "step": ("tile layout (q,k,v) + " if w.token_major else "") + "work ordering + tcgen05 attention"}
 
 
 def density(w) -> float:
@@ -252,6 +277,67 @@ def aggregate(eff_flops_per_rank: float, world: int, ms_max: float) -> float:
     return world * eff_flops_per_rank / (ms_max / 1e3) / 1e12
 
 
+def time_workload(vsa, w, dev, steps: int, warmup: int, flush) -> dict:
+    """Times one workload on its own: the tile layout (token-major inputs only)
+    and the forward call (work ordering + attention), each with CUDA events on
+    the launching stream, L2 flushed before every step.  Returns its roofline
+    entry for the bench line."""
+    B, H, D, T, NT, S, Sp = w.B, w.H, w.D, w.T, w.NT, w.S, w.Sp
+    stream = torch.cuda.current_stream()
+    idx, num, bs = w.q2k_idx.to(dev), w.q2k_num.to(dev), w.block_sizes.to(dev)
+    if w.token_major:
+        src = [x.to(dev) for x in (w.q_tok, w.k_tok, w.v_tok)]
+        r2t = w.row_to_token.to(dev)
+        tiles = [torch.empty((B, H, Sp, D), dtype=torch.bfloat16, device=dev) for _ in range(3)]
+    else:
+        tiles = [x.to(dev) for x in (w.q, w.k, w.v)]
+    out = torch.empty((B, H, Sp, D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, H, Sp), dtype=torch.float32, device=dev) if w.want_lse else None
+    dims = vsa.make_dims(B, H, NT, T, D, idx.shape[-1], w.scale)
+    ws = torch.empty(vsa.vsa_block_sparse_workspace_size(dims), dtype=torch.uint8, device=dev)
+
+    def one():
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        e[0].record(stream)
+        if w.token_major:
+            vsa.vsa_tile_layout(src[0], src[1], src[2], tiles[0], tiles[1], tiles[2], r2t, B, S, H, D, NT, T,
+                                stream)
+        e[1].record(stream)
+        vsa.vsa_block_sparse_fwd(tiles[0], tiles[1], tiles[2], idx, num, bs, out, lse, dims, ws, stream)
+        e[2].record(stream)
+        return e
+
+    for _ in range(max(warmup, 3)):
+        one()
+    torch.cuda.synchronize()
+    marks = []
+    for _ in range(steps):
+        flush.zero_()
+        marks.append(one())
+    torch.cuda.synchronize()
+    if vsa.vsa_check_device_status() != 0:
+        raise RuntimeError(f"device status error on {w.name}")
+    route = vsa.vsa_last_route()
+    tail, full = vsa.vsa_last_step_counts()
+    peak, hbm, _ = _peaks()
+    eff = W.effective_flops(w)
+    attn = sum(m[1].elapsed_time(m[2]) for m in marks) / steps
+    ach = eff / (attn / 1e3) / 1e12
+    entry = {"workload": w.name, "attn_ms": attn, "effective_flops": eff, "padded_flops": W.padded_flops(w),
+             "achieved": ach, "unit": UNIT, "frac": ach / peak, "density": round(density(w), 4),
+             "layout": "paired" if route["layout"] == vsa.VSA_LAYOUT_PAIRED else "split",
+             "kernel": f"attn_fwd_kernel<{min(T, 128)},{D}>", "grid": route["grid"],
+             "work_items": route["work_items"], "stages": route["stages"],
+             "steps_tail_full": [tail, full], "timed_calls": steps}
+    if w.token_major:
+        lay = sum(m[0].elapsed_time(m[1]) for m in marks) / steps
+        gbs = layout_bytes(w) / (lay / 1e3) / 1e9
+        entry["layout_ms"] = lay
+        entry["layout_roofline"] = {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
+                                    "frac": gbs / hbm, "bytes": layout_bytes(w)}
+    return entry
+
+
 def run_ours(args, cfg):
     import block_sparse_attention_gathered_gb300 as vsa
 
@@ -261,16 +347,21 @@ def run_ours(args, cfg):
         torch.cuda.set_device(local)
         dist.init_process_group("nccl")
     dev = torch.device("cuda", torch.cuda.current_device())
-    w = W.make_workload(cfg, tile=args.tile)
-    assert w.token_major
+    w = W.make_workload(cfg, tile=args.tile, head_dim=args.head_dim)
+    token = w.token_major
     eff = W.effective_flops(w)
     B, H, D, T, NT, S = w.B, w.H, w.D, w.T, w.NT, w.S
     Sp = w.Sp
 
-    q_tok, k_tok, v_tok = (x.to(dev) for x in (w.q_tok, w.k_tok, w.v_tok))
-    r2t = w.row_to_token.to(dev)
+    if token:
+        q_tok, k_tok, v_tok = (x.to(dev) for x in (w.q_tok, w.k_tok, w.v_tok))
+        r2t = w.row_to_token.to(dev)
+        tiles = [torch.empty((B, H, Sp, D), dtype=torch.bfloat16, device=dev) for _ in range(3)]
+    else:
+        # tile-major inputs (the ragged workload's NaN/Inf padding must reach
+        # the kernel as it is): no layout step
+        tiles = [x.to(dev) for x in (w.q, w.k, w.v)]
     idx, num, bs = w.q2k_idx.to(dev), w.q2k_num.to(dev), w.block_sizes.to(dev)
-    tiles = [torch.empty((B, H, Sp, D), dtype=torch.bfloat16, device=dev) for _ in range(3)]
     out = torch.empty((B, H, Sp, D), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((B, H, Sp), dtype=torch.float32, device=dev) if w.want_lse else None
     select = bool(args.select)
@@ -296,14 +387,18 @@ def run_ours(args, cfg):
     def ev():
         return torch.cuda.Event(enable_timing=True)
 
-    def step(qt, kt, vt):
-        """One pass of the hot path; returns events after the layout, after the
-        selection (the same event when there is none) and after the attention
-        call (recorded on the launching stream)."""
-        l0, l1, a1 = ev(), ev(), ev()
+    def step():
+        """One pass of the hot path; returns events before the step, after the
+        layout, after the selection (the same event when there is none), after
+        the attention call and after the un-tiling (recorded on the launching
+        stream)."""
+        l0, a1 = ev(), ev()
         l0.record(stream)
-        vsa.vsa_tile_layout(qt, kt, vt, tiles[0], tiles[1], tiles[2], r2t, B, S, H, D, NT, T, stream)
-        l1.record(stream)
+        l1 = l0
+        if token:
+            vsa.vsa_tile_layout(q_tok, k_tok, v_tok, tiles[0], tiles[1], tiles[2], r2t, B, S, H, D, NT, T, stream)
+            l1 = ev()
+            l1.record(stream)
         s1 = l1
         if select:
             vsa.vsa_coarse_select(tiles[0], tiles[1], bs, topk, idx, num, sel_dims, sel_ws, stream)
@@ -325,7 +420,7 @@ def run_ours(args, cfg):
         torch.cuda.synchronize()
 
     for _ in range(max(args.warmup, 3)):
-        step(q_tok, k_tok, v_tok)
+        step()
     barrier()
     if vsa.vsa_check_device_status() != 0:
         raise RuntimeError("device status error during warm-up")
@@ -338,20 +433,22 @@ def run_ours(args, cfg):
         barrier()
         for _ in range(args.steps):
             flush.zero_()  # L2 flush, outside the timed events
-            marks.append(step(q_tok, k_tok, v_tok))
+            marks.append(step())
         barrier()
     step_ms = [m[0].elapsed_time(m[4]) for m in marks]
     untile_ms = [m[3].elapsed_time(m[4]) for m in marks] if untile else None
-    layout_ms = [m[0].elapsed_time(m[1]) for m in marks]
+    layout_ms = [m[0].elapsed_time(m[1]) for m in marks] if token else None
     select_ms = [m[1].elapsed_time(m[2]) for m in marks] if select else None
     attn_ms = [m[2].elapsed_time(m[3]) for m in marks]
     ms = max_over_ranks(sum(step_ms) / len(step_ms), dev)
     if vsa.vsa_check_device_status() != 0:
         raise RuntimeError("device status error in the timed region")
+    route = vsa.vsa_last_route()
+    steps_tail_full = list(vsa.vsa_last_step_counts())
 
-    # ---------------------------------------------------------------- backward (optional)
+    # ---------------------------------------------------------------- backward (outside the step)
     bwd_line = None
-    if args.bwd:
+    if args.bwd and w.want_lse:
         dout = torch.randn((B, H, Sp, D), generator=torch.Generator().manual_seed(W.SEED_BASE + 200)).to(
             torch.bfloat16).to(dev)
         grads = [torch.empty_like(out) for _ in range(3)]
@@ -362,7 +459,7 @@ def run_ours(args, cfg):
             vsa.vsa_block_sparse_bwd(tiles[0], tiles[1], tiles[2], out, dout, lse, idx, num, bs, grads[0],
                                      grads[1], grads[2], bdims, bws, stream)
 
-        step(q_tok, k_tok, v_tok)
+        step()
         for _ in range(max(args.warmup, 3)):
             bwd_step()
         barrier()
@@ -381,14 +478,19 @@ def run_ours(args, cfg):
         b_flops = 2.5 * eff  # dV, dP, dS-weighted dQ and dK, plus S: 5 products of the forward's 2
         bwd_line = {"ms": b_ms, "effective_flops": b_flops, "achieved": b_flops / (b_ms / 1e3) / 1e12,
                     "unit": "TFLOP/s", "frac": b_flops / (b_ms / 1e3) / 1e12 / _peaks()[0],
-                    "launches": len(b_marks), "kernels": "delta, k2q transpose, dK/dV, dQ (tcgen05)"}
+                    "timed_calls": len(b_marks), "kernels": "delta, pairs, k2q transpose, dK/dV, dQ (tcgen05)"}
 
     # ---------------------------------------------------------------- end to end from host buffers
-    hq, hk, hv = (x.pin_memory() for x in (w.q_tok, w.k_tok, w.v_tok))
-    hidx, hnum, hbs, hr2t = (x.pin_memory() for x in (w.q2k_idx, w.q2k_num, w.block_sizes, w.row_to_token))
+    if token:
+        hq, hk, hv = (x.pin_memory() for x in (w.q_tok, w.k_tok, w.v_tok))
+        h_in = ((q_tok, hq), (k_tok, hk), (v_tok, hv), (bs, w.block_sizes.pin_memory()),
+                (r2t, w.row_to_token.pin_memory()))
+    else:
+        h_in = tuple((d_, h_.pin_memory()) for d_, h_ in zip(tiles, (w.q, w.k, w.v))) + \
+            ((bs, w.block_sizes.pin_memory()),)
     # with the GPU selection the selection arrays are outputs, not inputs
-    h_in = ((q_tok, hq), (k_tok, hk), (v_tok, hv), (bs, hbs), (r2t, hr2t)) + \
-        (() if select else ((idx, hidx), (num, hnum)))
+    if not select:
+        h_in = h_in + ((idx, w.q2k_idx.pin_memory()), (num, w.q2k_num.pin_memory()))
     hout = torch.empty((B, H, Sp, D), dtype=torch.bfloat16).pin_memory()
     if untile:  # the gate is an input too, and the token-major output is read back
         hgate = gate.cpu().pin_memory()
@@ -401,7 +503,7 @@ def run_ours(args, cfg):
     def e2e_step():
         for d_, h_ in h_in:
             d_.copy_(h_, non_blocking=True)
-        step(q_tok, k_tok, v_tok)
+        step()
         hout.copy_(out_tok if untile else out, non_blocking=True)
         if hlse is not None:
             hlse.copy_(lse, non_blocking=True)
@@ -420,38 +522,47 @@ def run_ours(args, cfg):
     barrier()
     e2e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in e_ms) / len(e_ms), dev)
 
-    route = vsa.vsa_last_route()
+    # ---------------------------------------------------------------- other workloads (outside the step)
+    extra = {}
+    if args.extra and rank == 0:
+        for label, c, tile, hd in EXTRA_WORKLOADS:
+            if (c, tile or 128, hd or 128) == (cfg, args.tile or 128, args.head_dim or 128):
+                continue  # the headline workload itself
+            extra[label] = time_workload(vsa, W.make_workload(c, tile=tile, head_dim=hd), dev, args.extra_steps,
+                                         3, flush)
+
     peak, hbm, src = _peaks()
     attn_avg = sum(attn_ms) / len(attn_ms)
-    lay_avg = sum(layout_ms) / len(layout_ms)
     achieved = eff / (attn_avg / 1e3) / 1e12
-    lay_gbs = layout_bytes(w) / (lay_avg / 1e3) / 1e9
     traffic = ATTN_TRAFFIC.get((w.name, _attn_source_hash()))
     if rank == 0:
+        config = config_dict(w, eff)
         line = {
             "metric": METRIC, "value": aggregate(eff, world, ms), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": w.name, "B": B, "H": H, "S": S, "head_dim": D, "tile": T, "num_tiles": NT,
-                       "density": round(density(w), 4), "lse": w.want_lse, "effective_flops": eff,
-                       "padded_flops": W.padded_flops(w), "l2": "flushed (256 MB write) between steps",
-                       "step": "tile layout (q,k,v) + work ordering + tcgen05 attention"},
-            "attn_ms": attn_avg, "layout_ms": lay_avg,
+            "config": config,
+            "attn_ms": attn_avg,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                          "frac": achieved / peak, "traffic": traffic,
                          "peak_source": f"{src} bf16 burst (cuBLAS)",
                          "kernel": f"attn_fwd_kernel<{min(T, 128)},{D},"
                                    f"{'paired' if route.get('layout') == vsa.VSA_LAYOUT_PAIRED else 'split'}>"},
-            "layout_roofline": {"bound": "hbm", "achieved": lay_gbs, "peak": hbm, "unit": "GB/s",
-                                "frac": lay_gbs / hbm, "bytes": layout_bytes(w),
-                                "peak_source": f"{src} HBM copy", "kernel": "layout_kernel"},
             "e2e": {"value": aggregate(eff, world, e2e_ms), "unit": UNIT, "ms_per_step": e2e_ms,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            # per step: tile layout, [tile pooling, selection,] work-ordering sort, attention, [un-tiling]
-            "gpu_launches": (3 + (2 if select else 0) + (1 if untile else 0)) * args.steps,
+            # per step: [tile layout,] [tile pooling, selection,] work-ordering sort, attention, [un-tiling]
+            "gpu_launches": ((1 if token else 0) + 2 + (2 if select else 0) + (1 if untile else 0)) * args.steps,
             "clocks": clk.summary(),
             "route": route,
+            "steps_tail_full": steps_tail_full,
         }
+        if token:
+            lay_avg = sum(layout_ms) / len(layout_ms)
+            lay_gbs = layout_bytes(w) / (lay_avg / 1e3) / 1e9
+            line["layout_ms"] = lay_avg
+            line["layout_roofline"] = {"bound": "hbm", "achieved": lay_gbs, "peak": hbm, "unit": "GB/s",
+                                       "frac": lay_gbs / hbm, "bytes": layout_bytes(w),
+                                       "peak_source": f"{src} HBM copy", "kernel": "layout_kernel"}
         if select:
             sel_avg = sum(select_ms) / len(select_ms)
             pool_bytes = pooled_bytes(w)
@@ -472,6 +583,8 @@ def run_ours(args, cfg):
             line["config"]["step"] += " + un-tiling with gate"
         if bwd_line is not None:
             line["bwd"] = bwd_line
+        if extra:
+            line["workloads"] = extra
         if not args.no_cpu_baseline and world == 1:
             line["cpu_baseline"] = cpu_oracle_run(w, args.cpu_seconds)
         print(json.dumps(line), flush=True)
@@ -486,20 +599,25 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--config", type=int, default=5, choices=[2, 4, 5])
+    ap.add_argument("--config", type=int, default=5, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--tile", type=int, default=None, choices=[128, 256],
+    ap.add_argument("--tile", type=int, default=None, choices=[64, 128, 256],
                     help="dense-limit workload only: tile size (default 128)")
-    ap.add_argument("--bwd", action="store_true",
-                    help="also time the backward pass (reported under \"bwd\", outside the step)")
+    ap.add_argument("--head-dim", type=int, default=None, choices=[64, 128],
+                    help="dense-limit workload only: head_dim (default 128)")
+    ap.add_argument("--no-bwd", dest="bwd", action="store_false",
+                    help="skip the backward timing (reported under \"bwd\", outside the step)")
+    ap.add_argument("--no-extra", dest="extra", action="store_false",
+                    help="skip timing the other workloads (reported under \"workloads\")")
+    ap.add_argument("--extra-steps", type=int, default=20)
     ap.add_argument("--untile", action="store_true",
                     help="end the step with the un-tiling of the output times a gate")
     ap.add_argument("--select", action="store_true",
                     help="video-grid workload only: select the key tiles on the GPU inside the step")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     args = ap.parse_args()
-    if args.tile not in (None, 128) and args.config != 5:
-        ap.error("--tile 256 needs the dense-limit workload (--config 5)")
+    if (args.tile not in (None, 128) or args.head_dim not in (None, 128)) and args.config != 5:
+        ap.error("--tile and --head-dim re-shape the dense-limit workload (--config 5) only")
     if args.select and args.config != 4:
         ap.error("--select needs the video-grid workload (--config 4)")
     if args.impl == "reference":

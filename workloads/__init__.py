@@ -297,25 +297,27 @@ def _video_topk(seed: int) -> Workload:
                     notes={"topk": topk})
 
 
-def _dense(seed: int, S: int = 31200, H: int = 6, T: int = 128) -> Workload:
+def _dense(seed: int, S: int = 31200, H: int = 6, T: int = 128, D: int = 128) -> Workload:
     g = _gen(seed)
-    B, D = 1, 128
+    B = 1
     r2t, bs = linear_row_map(S, T)
     NT = int(bs.numel())
     q, k, v = (_bf16_normal(g, (B, S, H, D)) for _ in range(3))
     counts = torch.full((B, H, NT), NT, dtype=torch.int32)
     idx = torch.arange(NT, dtype=torch.int32).view(1, 1, 1, NT).expand(B, H, NT, NT).contiguous()
-    name = WORKLOAD_NAMES[5] if T == 128 else f"dense_b1h6d128_s31200_t{T}x{NT}_lse"
+    name = WORKLOAD_NAMES[5] if (T, D) == (128, 128) else f"dense_b1h6d{D}_s31200_t{T}x{NT}_lse"
     return Workload(name, B, H, D, T, NT, bs, idx, counts, 1.0 / math.sqrt(D),
                     True, S=S, q_tok=q, k_tok=k, v_tok=v, row_to_token=r2t)
 
 
-def make_workload(cfg: int, seed: Optional[int] = None, tile: Optional[int] = None) -> Workload:
+def make_workload(cfg: int, seed: Optional[int] = None, tile: Optional[int] = None,
+                  head_dim: Optional[int] = None) -> Workload:
     """Build workload ``cfg`` (1..5) with seed ``SEED_BASE + cfg`` by default.
-    ``tile`` re-tiles the dense-limit workload (5) with 256-token tiles."""
+    ``tile`` (64 or 256) and ``head_dim`` (64) re-shape the dense-limit
+    workload (5): the same 6 heads x 31200 tokens, every key tile selected."""
     seed = SEED_BASE + cfg if seed is None else seed
-    if tile is not None and tile != 128:
+    if (tile is not None and tile != 128) or (head_dim is not None and head_dim != 128):
         if cfg != 5:
-            raise ValueError("only the dense-limit workload takes another tile size")
-        return _dense(seed, T=tile)
+            raise ValueError("only the dense-limit workload takes another tile size or head_dim")
+        return _dense(seed, T=tile or 128, D=head_dim or 128)
     return {1: _tiny, 2: _uniform, 3: _ragged, 4: _video_topk, 5: _dense}[cfg](seed)
