@@ -27,7 +27,7 @@ VSA_ERR_CUDA, VSA_ERR_TIMEOUT, VSA_ERR_INDEX, VSA_ERR_WORKSPACE = -5, -6, -7, -8
 VSA_KERNEL_NONE, VSA_KERNEL_ATTN_TCGEN05, VSA_KERNEL_LAYOUT, VSA_KERNEL_VALIDATE = 0, 1, 2, 3
 VSA_KERNEL_SELECT, VSA_KERNEL_UNTILE, VSA_KERNEL_BWD = 4, 5, 6
 VSA_LAYOUT_SPLIT, VSA_LAYOUT_PAIRED = 0, 1  # vsa_route.layout: MMA-issue layout of the attention kernel
-VSA_MAX_BATCH_HEADS, VSA_MAX_TILES = 65535, 8192
+VSA_MAX_BATCH_HEADS, VSA_MAX_TILES, VSA_MAX_TILES_BWD, VSA_SMEM_BITMAP_TILES = 65535, (1 << 22) - 1, 8192, 8192
 
 
 class VsaDims(ctypes.Structure):

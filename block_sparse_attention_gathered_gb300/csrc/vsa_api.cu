@@ -9,6 +9,7 @@
 // were not built for is refused with an error instead of returning
 // uninitialised output; the SM count and the shared-memory opt-in are cached
 // per device in atomics.
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstring>
@@ -140,6 +141,8 @@ vsa_status current_device(int *dev_out) {
     return VSA_OK;
 }
 
+int64_t kernel_tiles(const vsa_dims *d) { return (int64_t)d->num_tiles * (d->tile == 256 ? 2 : 1); }
+
 vsa_status check_dims(const vsa_dims *d) {
     if (!d) return VSA_ERR_ARG;
     if (d->B <= 0 || d->H <= 0 || d->num_tiles <= 0 || d->max_kv < 0) return VSA_ERR_ARG;
@@ -148,7 +151,7 @@ vsa_status check_dims(const vsa_dims *d) {
     if (!std::isfinite(d->scale)) return VSA_ERR_ARG;
     if ((int64_t)d->B * d->H > VSA_MAX_BATCH_HEADS) return VSA_ERR_LIMITS;
     // 256-token tiles run as two 128-token halves each
-    if ((int64_t)d->num_tiles * (d->tile == 256 ? 2 : 1) > VSA_MAX_TILES) return VSA_ERR_LIMITS;
+    if (kernel_tiles(d) > VSA_MAX_TILES) return VSA_ERR_LIMITS;
     const int64_t rows = (int64_t)d->B * d->H * d->num_tiles * d->tile;
     if (rows + kItemRows >= (int64_t(1) << VSA_MAX_ROWS_LOG2)) return VSA_ERR_LIMITS;
     if ((int64_t)d->B * d->H * d->num_tiles * (int64_t)d->max_kv >= (int64_t(1) << 31)) return VSA_ERR_LIMITS;
@@ -164,9 +167,32 @@ constexpr size_t kWsHeader = 256;  // work counter, padded
 // per split item.
 constexpr int kMaxSplit = 256;
 
-size_t workspace_bytes_for(const vsa_dims *d) {
+// Dims the backward and the coarse selection accept: check_dims plus their
+// tighter tile limit.
+vsa_status check_dims_small(const vsa_dims *d) {
+    const vsa_status st = check_dims(d);
+    if (st != VSA_OK) return st;
+    return kernel_tiles(d) > VSA_MAX_TILES_BWD ? VSA_ERR_LIMITS : VSA_OK;
+}
+
+// Workspace of the forward: a 256 B header (work counter), the order list,
+// and, beyond kSmemBitmapTiles kernel tiles, the selection bitmaps of every
+// CTA (two buffers of four bitmaps of ceil(kernel tiles / 32) words each),
+// 256-byte aligned.
+int bitmap_words(const vsa_dims *d) { return (int)((kernel_tiles(d) + 31) / 32); }
+bool bitmaps_in_workspace(const vsa_dims *d) { return kernel_tiles(d) > kSmemBitmapTiles; }
+size_t order_bytes_for(const vsa_dims *d) {
     const int64_t n_items = (int64_t)d->B * d->H * items_per_seq(d);
     return kWsHeader + (size_t)(n_items + kMaxSplit) * sizeof(int32_t);
+}
+size_t bitmap_offset_for(const vsa_dims *d) { return (order_bytes_for(d) + 255) & ~(size_t)255; }
+size_t bitmap_bytes_per_cta(const vsa_dims *d) { return (size_t)2 * 4 * bitmap_words(d) * sizeof(uint32_t); }
+
+size_t workspace_bytes_for(const vsa_dims *d) {
+    if (!bitmaps_in_workspace(d)) return order_bytes_for(d);
+    const int64_t n_items = (int64_t)d->B * d->H * items_per_seq(d);
+    const int64_t ctas = n_items < kMaxGridCtas ? n_items : kMaxGridCtas;
+    return bitmap_offset_for(d) + (size_t)ctas * bitmap_bytes_per_cta(d);
 }
 
 vsa_status encode_rows_map(CUtensorMap *m, const void *ptr, int64_t rows, int D, int box_rows) {
@@ -372,7 +398,8 @@ vsa_status vsa_block_sparse_fwd(const void *q, const void *k, const void *v, con
 
     // One persistent CTA per SM.  When the last wave would fill at most half
     // of them, its items are split into one-unit items.
-    const int sms = dc.sm_count.load(std::memory_order_acquire);
+    // (kMaxGridCtas bounds the grid for the workspace's per-CTA bitmap regions)
+    const int sms = std::min(dc.sm_count.load(std::memory_order_acquire), kMaxGridCtas);
     const int grid = n_items < sms ? n_items : sms;
     const int rem = n_items > grid ? n_items % grid : 0;
     const int split = (rem > 0 && 2 * rem <= grid && rem <= kMaxSplit) ? rem : 0;
@@ -391,6 +418,9 @@ vsa_status vsa_block_sparse_fwd(const void *q, const void *k, const void *v, con
     p.work_counter = counter;
     p.status = dc.status_ptr.load(std::memory_order_acquire);
     p.steps = dc.steps_ptr.load(std::memory_order_acquire);
+    p.bm_global = bitmaps_in_workspace(dims)
+                      ? reinterpret_cast<uint32_t *>(reinterpret_cast<char *>(workspace) + bitmap_offset_for(dims))
+                      : nullptr;
     p.NT = NT * sub;
     p.sub = sub;
     p.max_kv = dims->max_kv;
@@ -412,7 +442,7 @@ vsa_status vsa_block_sparse_fwd(const void *q, const void *k, const void *v, con
     const bool paired = Tk == 128 && D == 128 && (sub == 2 || dims->max_kv >= NT);
     if (launch_attn(Tk, D, paired, tm_q, tm_k, tm_v, p, grid, s) != cudaSuccess) return VSA_ERR_CUDA;
 
-    const AttnLaunchInfo info = attn_launch_info(Tk, D, p.bm_words);
+    const AttnLaunchInfo info = attn_launch_info(Tk, D, p.bm_global ? 0 : p.bm_words);
     t_route.kernel = VSA_KERNEL_ATTN_TCGEN05;
     t_route.tile = T;
     t_route.head_dim = D;
@@ -501,7 +531,7 @@ static BwdWs bwd_ws(const vsa_dims *d) {
 }
 
 size_t vsa_block_sparse_bwd_workspace_size(const vsa_dims *dims) {
-    if (check_dims(dims) != VSA_OK) return 0;
+    if (check_dims_small(dims) != VSA_OK) return 0;
     return bwd_ws(dims).total;
 }
 
@@ -509,7 +539,7 @@ vsa_status vsa_block_sparse_bwd(const void *q, const void *k, const void *v, con
                                 const float *lse, const int32_t *q2k_idx, const int32_t *q2k_num,
                                 const int32_t *block_sizes, void *dq, void *dk, void *dv, const vsa_dims *dims,
                                 void *workspace, size_t workspace_bytes, vsa_stream_t stream) {
-    vsa_status st = check_dims(dims);
+    vsa_status st = check_dims_small(dims);
     if (st != VSA_OK) return st;
     if (!q || !k || !v || !out || !dout || !lse || !q2k_num || !block_sizes || !dq || !dk || !dv ||
         (!q2k_idx && dims->max_kv > 0))
@@ -649,17 +679,17 @@ vsa_status vsa_validate_indices(const int32_t *q2k_idx, const int32_t *q2k_num, 
 }
 
 size_t vsa_coarse_select_workspace_size(const vsa_dims *dims) {
-    if (check_dims(dims) != VSA_OK) return 0;
+    if (check_dims_small(dims) != VSA_OK) return 0;
     return 2 * (size_t)dims->B * dims->H * dims->num_tiles * dims->head_dim * sizeof(float);
 }
 
 vsa_status vsa_coarse_select(const void *q, const void *k, const int32_t *block_sizes, int32_t topk,
                              int32_t *q2k_idx, int32_t *q2k_num, const vsa_dims *dims, void *workspace,
                              size_t workspace_bytes, vsa_stream_t stream) {
-    vsa_status st = check_dims(dims);
+    vsa_status st = check_dims_small(dims);
     if (st != VSA_OK) return st;
     if (!q || !k || !block_sizes || !q2k_num || topk < 0 || (!q2k_idx && topk > 0)) return VSA_ERR_ARG;
-    if (topk > VSA_MAX_TILES) return VSA_ERR_LIMITS;
+    if (topk > VSA_MAX_TILES_BWD) return VSA_ERR_LIMITS;
     if (!aligned(q, 16) || !aligned(k, 16) || !aligned(block_sizes, 4) || !aligned(q2k_num, 4) ||
         (q2k_idx && !aligned(q2k_idx, 4)))
         return VSA_ERR_ALIGN;

@@ -219,7 +219,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t *gbase = smem_raw + (base - raw);
     const int W = P.bm_words;
-    const SmemPlan L = smem_plan<T, D>(W, NS);
+    // the selection bitmaps: in shared memory, or (beyond kSmemBitmapTiles
+    // kernel tiles) in this CTA's region of the workspace
+    const SmemPlan L = smem_plan<T, D>(P.bm_global ? 0 : W, NS);
     const uint32_t sQ = base + L.q;
     // Count of S tiles the softmax warps have copied out of an S buffer (each
     // of the eight warps of a unit adds 1 per S): one shared count, or one per
@@ -231,7 +233,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     // fill has landed, which this count tells them.
     const uint32_t sProg = base + L.sprog;
     const uint32_t sRing = base + L.ring;
-    uint32_t *bm = reinterpret_cast<uint32_t *>(gbase + L.bm);           // [2][4][W]
+    uint32_t *bm = P.bm_global ? P.bm_global + (size_t)blockIdx.x * 2 * 4 * W
+                               : reinterpret_cast<uint32_t *>(gbase + L.bm);  // [2][4][W]
     volatile int32_t *hdr = reinterpret_cast<int32_t *>(gbase + L.hdr);  // [2][4]
     const uint32_t bars = base + L.bars;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(gbase + L.tslot);
@@ -1020,8 +1023,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 template <int T, int D>
 cudaError_t launch_t(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v, AttnParams p, bool paired,
                      int grid, cudaStream_t stream) {
-    p.stages = stages_for<T, D>(p.bm_words);
-    const SmemPlan L = smem_plan<T, D>(p.bm_words, p.stages);
+    const int smem_words = p.bm_global ? 0 : p.bm_words;  // bitmap words held in shared memory
+    p.stages = stages_for<T, D>(smem_words);
+    const SmemPlan L = smem_plan<T, D>(smem_words, p.stages);
     if (paired)
         attn_fwd_kernel<T, D, true><<<grid, kAttnThreads, L.total, stream>>>(q, k, v, p);
     else

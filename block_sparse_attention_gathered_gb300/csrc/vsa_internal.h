@@ -15,7 +15,8 @@ enum : int32_t { kFlagIndex = 1, kFlagTimeout = 2 };
 constexpr int kUnitRows = 128;
 constexpr int kItemRows = 256;
 constexpr int kAttnThreads = 640;  // 16 softmax warps, 2 MMA issuers, 1 producer, 1 fix-up warp
-constexpr int kMaxTiles = 8192;     // VSA_MAX_TILES
+constexpr int kSmemBitmapTiles = 8192;  // VSA_SMEM_BITMAP_TILES
+constexpr int kMaxGridCtas = 1024;      // bound on the attention grid (one CTA per SM), for workspace sizing
 
 struct AttnParams {
     const int32_t *q2k_idx;      // [B*H*NT, max_kv]
@@ -27,6 +28,8 @@ struct AttnParams {
     int32_t *work_counter;       // next slot of `order` to hand out
     int32_t *status;             // device status word
     unsigned long long *steps;   // (tail, full) key-tile steps, added to by the producer warps
+    uint32_t *bm_global;         // per-CTA selection bitmaps in the workspace (more than
+                                 // kSmemBitmapTiles kernel tiles), or nullptr: in shared memory
     int32_t NT;                  // kernel tiles (128-token halves when sub == 2)
     int32_t sub;                 // kernel tiles per caller tile: 1, or 2 for 256-token tiles
     int32_t max_kv;
@@ -45,7 +48,8 @@ struct AttnLaunchInfo {
 
 // Ring depth and dynamic shared memory of the attention kernel variant: the
 // deepest K/V ring that fits the 227 KB per-CTA limit next to the Q tiles and
-// the selection bitmaps.
+// the selection bitmaps (bm_words: bitmap words kept in shared memory, 0 when
+// they live in the workspace).
 AttnLaunchInfo attn_launch_info(int tile, int head_dim, int bm_words);
 
 // Enables the variant's shared-memory size on the current device (once).

@@ -56,12 +56,19 @@ typedef enum {
     VSA_ERR_WORKSPACE = -8  /* workspace missing or smaller than required */
 } vsa_status;
 
-/* Launch limits.  The first two follow the page's MaxBatchHeads / MaxRows;
- * the tile limit is this kernel's own (the per-CTA selection bitmap lives in
- * shared memory), tighter than the page's 2^22. */
+/* Launch limits, checked before any launch: the sm_121a hardening commit's
+ * MaxBatchHeads, MaxRows and MaxTiles (within_launch_limits).  The tile limit
+ * counts kernel tiles: a 256-token tile is two of them. */
 #define VSA_MAX_BATCH_HEADS 65535
-#define VSA_MAX_ROWS_LOG2 31        /* B*H*num_tiles*tile < 2^31 */
-#define VSA_MAX_TILES 8192          /* num_tiles <= 8192 (4096 with 256-token tiles) */
+#define VSA_MAX_ROWS_LOG2 31              /* B*H*num_tiles*tile < 2^31 */
+#define VSA_MAX_TILES ((1 << 22) - 1)     /* forward: kernel tiles < 2^22 */
+/* The forward keeps each work item's selection bitmaps in shared memory up
+ * to this many kernel tiles, and in a per-CTA region of the workspace beyond
+ * (vsa_block_sparse_workspace_size counts it). */
+#define VSA_SMEM_BITMAP_TILES 8192
+/* The backward and the coarse selection: num_tiles <= 8192 (4096 with
+ * 256-token tiles); their partner lists pack a tile index in 13 bits. */
+#define VSA_MAX_TILES_BWD 8192
 
 typedef struct {
     int32_t B;          /* batch */
@@ -280,7 +287,7 @@ vsa_status vsa_validate_indices(const int32_t *q2k_idx, const int32_t *q2k_num,
  *   block_sizes  int32 [NT], each in [0, tile]; a size outside that range
  *                is never read past the tile, makes the tile unselectable and
  *                flags VSA_ERR_INDEX in the device status word
- *   topk         kept tiles per query tile, 0 <= topk <= VSA_MAX_TILES
+ *   topk         kept tiles per query tile, 0 <= topk <= VSA_MAX_TILES_BWD
  *   q2k_idx      int32 [B, H, NT, topk] out: kept tiles in ascending order,
  *                -1 after the last one (may be NULL when topk == 0)
  *   q2k_num      int32 [B, H, NT] out: number kept

@@ -200,6 +200,26 @@ def test_split_last_wave(vsa, oracle_mod, T):
     assert torch.equal(out.view(torch.int16), again.view(torch.int16))
 
 
+@pytest.mark.parametrize("T", [64, 128])
+def test_tiles_beyond_shared_memory_bitmaps(vsa, oracle_mod, T):
+    """8200 tiles, just above the 8192 whose selection bitmaps fit in shared
+    memory: the kernel keeps them in the workspace instead (the hardening
+    commit's limit is 2^22 tiles).  Selections reach tiles on both sides of
+    8192; 640 query tiles are compared with the oracle, among them every
+    query tile that selects a tile past 8191 in one head."""
+    NT = 8200
+    w = _random_case(4242 + T, 1, 2, NT, T, 64, max_kv=4, empty_frac=0.05)
+    (q, k, v), refs = _to_tile_major(w, vsa, oracle_mod)
+    out, lse = _run(vsa, q, k, v, w)
+    high = [t for t in range(NT)
+            if (w.q2k_idx[0, 0, t, :int(w.q2k_num[0, 0, t])] >= 8192).any()][:300]
+    assert high
+    units = PT.sample_units(w.B, w.H, w.NT, 640, seed=T, must=high + [NT - 1, 2 * NT - 1, 8191, 8192 + NT])
+    _check(w, out, lse, refs, oracle_mod, units, f"8200 tiles T{T}")
+    _check_steps(vsa, w)
+    assert vsa.vsa_last_route()["work_items"] == 2 * (NT * T // 256)
+
+
 def test_all_empty_and_zero_max_kv(vsa):
     dev = "cuda"
     B, H, NT, T, D = 1, 2, 4, 128, 128

@@ -81,19 +81,47 @@ def test_launch_limits(vsa):
     # batch * heads <= 65535
     assert _fwd(vsa, vsa.make_dims(256, 256, 4, 64, 64, 2)) == vsa.VSA_ERR_LIMITS
     assert vsa.vsa_block_sparse_workspace_size(vsa.make_dims(256, 256, 4, 64, 64, 2)) == 0
-    # tiles <= 8192 (selection bitmap held in shared memory)
-    assert _fwd(vsa, vsa.make_dims(1, 1, 8193, 64, 64, 2)) == vsa.VSA_ERR_LIMITS
+    # kernel tiles < 2^22 (the hardening commit's MaxTiles)
+    assert vsa.VSA_MAX_TILES == (1 << 22) - 1
+    assert vsa.vsa_block_sparse_workspace_size(vsa.make_dims(1, 1, (1 << 22) - 1, 64, 64, 2)) > 0
+    assert vsa.vsa_block_sparse_workspace_size(vsa.make_dims(1, 1, 1 << 22, 64, 64, 2)) == 0
+    assert _fwd(vsa, vsa.make_dims(1, 1, 1 << 22, 64, 64, 2)) == vsa.VSA_ERR_LIMITS
     # rows < 2^31
     assert _fwd(vsa, vsa.make_dims(16, 4096, 8192, 128, 64, 2)) == vsa.VSA_ERR_LIMITS
     assert _fwd(vsa, vsa.make_dims(65535, 1, 257, 128, 128, 1)) == vsa.VSA_ERR_LIMITS
 
 
 def test_tile_256_limits(vsa):
-    # 256-token tiles run as two 128-token halves: at most 4096 of them
-    assert vsa.vsa_block_sparse_workspace_size(vsa.make_dims(1, 2, 4096, 256, 128, 2)) > 0
-    assert vsa.vsa_block_sparse_workspace_size(vsa.make_dims(1, 2, 4097, 256, 128, 2)) == 0
-    assert _fwd(vsa, vsa.make_dims(1, 2, 4097, 256, 128, 2)) == vsa.VSA_ERR_LIMITS
+    # 256-token tiles run as two 128-token halves, and the limit counts halves
+    half = (1 << 21) - 1   # 2 * half = 2^22 - 2 kernel tiles
+    assert vsa.vsa_block_sparse_workspace_size(vsa.make_dims(1, 2, half, 256, 128, 2)) > 0
+    assert vsa.vsa_block_sparse_workspace_size(vsa.make_dims(1, 2, half + 1, 256, 128, 2)) == 0
+    assert _fwd(vsa, vsa.make_dims(1, 2, half + 1, 256, 128, 2)) == vsa.VSA_ERR_LIMITS
     assert _fwd(vsa, vsa.make_dims(1, 2, 4, 512, 128, 2)) == vsa.VSA_ERR_ARG
+    # the backward and the coarse selection keep 8192 kernel tiles
+    assert vsa.vsa_block_sparse_bwd_workspace_size(vsa.make_dims(1, 2, 4096, 256, 128, 2)) > 0
+    assert vsa.vsa_block_sparse_bwd_workspace_size(vsa.make_dims(1, 2, 4097, 256, 128, 2)) == 0
+    assert vsa.vsa_block_sparse_bwd_workspace_size(vsa.make_dims(1, 1, 8192, 64, 64, 2)) > 0
+    assert vsa.vsa_block_sparse_bwd_workspace_size(vsa.make_dims(1, 1, 8193, 64, 64, 2)) == 0
+    assert vsa.vsa_coarse_select_workspace_size(vsa.make_dims(1, 1, 8193, 64, 64, 2)) == 0
+
+
+def test_bitmap_workspace_beyond_shared_memory(vsa):
+    # up to 8192 kernel tiles the selection bitmaps live in shared memory and
+    # the workspace is the header plus the order list; beyond, each CTA (at
+    # most 1024, at most one per work item) gets 2 x 4 bitmaps in the workspace
+    small = vsa.make_dims(1, 1, 8192, 64, 64, 2)
+    items = 8192 * 64 // 256
+    assert vsa.vsa_block_sparse_workspace_size(small) == 256 + 4 * (items + 256)
+    big = vsa.make_dims(1, 1, 8200, 64, 64, 2)
+    items = 8200 * 64 // 256
+    order = 256 + 4 * (items + 256)
+    words = (8200 + 31) // 32
+    assert vsa.vsa_block_sparse_workspace_size(big) == ((order + 255) // 256) * 256 + 1024 * 2 * 4 * words * 4
+    few = vsa.make_dims(1, 1, 8200, 256, 64, 2)  # 16400 kernel tiles, 8200 work items
+    words = (16400 + 31) // 32
+    order = 256 + 4 * (8200 + 256)
+    assert vsa.vsa_block_sparse_workspace_size(few) == ((order + 255) // 256) * 256 + 1024 * 2 * 4 * words * 4
     # one 256-row work item per 256-token tile
     assert vsa.vsa_block_sparse_workspace_size(vsa.make_dims(2, 3, 10, 256, 64, 4)) == 256 + 4 * (6 * 10 + 256)
 
