@@ -439,7 +439,7 @@ vsa_status vsa_block_sparse_fwd(const void *q, const void *k, const void *v, con
     // density with 64-token tiles or D = 64, where a product is N = 64 wide.
     // The host cannot see the selections without a sync, so the row length
     // stands in for the density.  Results do not depend on the layout.
-    const bool paired = Tk == 128 && D == 128 && (sub == 2 || dims->max_kv >= NT);
+    const bool paired = !p.bm_global && Tk == 128 && D == 128 && (sub == 2 || dims->max_kv >= NT);
     if (launch_attn(Tk, D, paired, tm_q, tm_k, tm_v, p, grid, s) != cudaSuccess) return VSA_ERR_CUDA;
 
     const AttnLaunchInfo info = attn_launch_info(Tk, D, p.bm_global ? 0 : p.bm_words);

@@ -207,7 +207,7 @@ __device__ __forceinline__ int tile_size(const int32_t *block_sizes, int jj, int
     return n < 0 ? 0 : (n > 128 ? 128 : n);
 }
 
-template <int T, int D, bool kPaired>
+template <int T, int D, bool kPaired, bool kGB>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const AttnParams P) {
@@ -219,9 +219,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t *gbase = smem_raw + (base - raw);
     const int W = P.bm_words;
-    // the selection bitmaps: in shared memory, or (beyond kSmemBitmapTiles
-    // kernel tiles) in this CTA's region of the workspace
-    const SmemPlan L = smem_plan<T, D>(P.bm_global ? 0 : W, NS);
+    // the selection bitmaps: in shared memory, or (kGB: beyond
+    // kSmemBitmapTiles kernel tiles) in this CTA's region of the workspace;
+    // a compile-time choice, so the shared-memory form reads them with
+    // shared-memory loads
+    const SmemPlan L = smem_plan<T, D>(kGB ? 0 : W, NS);
     const uint32_t sQ = base + L.q;
     // Count of S tiles the softmax warps have copied out of an S buffer (each
     // of the eight warps of a unit adds 1 per S): one shared count, or one per
@@ -233,8 +235,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     // fill has landed, which this count tells them.
     const uint32_t sProg = base + L.sprog;
     const uint32_t sRing = base + L.ring;
-    uint32_t *bm = P.bm_global ? P.bm_global + (size_t)blockIdx.x * 2 * 4 * W
-                               : reinterpret_cast<uint32_t *>(gbase + L.bm);  // [2][4][W]
+    uint32_t *bm = kGB ? P.bm_global + (size_t)blockIdx.x * 2 * 4 * W
+                       : reinterpret_cast<uint32_t *>(gbase + L.bm);  // [2][4][W]
     volatile int32_t *hdr = reinterpret_cast<int32_t *>(gbase + L.hdr);  // [2][4]
     const uint32_t bars = base + L.bars;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(gbase + L.tslot);
@@ -601,8 +603,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                             pend_ph = tail ? vzp : vph;
                             pend_kb = (nj + 15) >> 4;
                             pend_tail = tail;
-                            pend_lo = ((pa[w] >> b) & 1u) ? 0u : ~0u;
-                            pend_hi = ((pb[w] >> b) & 1u) ? 0u : ~0u;
+                            if constexpr (T == 64) {
+                                pend_lo = ((pa[w] >> b) & 1u) ? 0u : ~0u;
+                                pend_hi = ((pb[w] >> b) & 1u) ? 0u : ~0u;
+                            }
                         } else {
                             // not selected by this unit: issue the pending P V (it
                             // frees a V stage), then release both stages of the entry
@@ -1026,10 +1030,18 @@ cudaError_t launch_t(const CUtensorMap &q, const CUtensorMap &k, const CUtensorM
     const int smem_words = p.bm_global ? 0 : p.bm_words;  // bitmap words held in shared memory
     p.stages = stages_for<T, D>(smem_words);
     const SmemPlan L = smem_plan<T, D>(smem_words, p.stages);
-    if (paired)
-        attn_fwd_kernel<T, D, true><<<grid, kAttnThreads, L.total, stream>>>(q, k, v, p);
-    else
-        attn_fwd_kernel<T, D, false><<<grid, kAttnThreads, L.total, stream>>>(q, k, v, p);
+    // The paired layout is only chosen for 128-token kernel tiles, and the
+    // workspace bitmaps run in the split layout (both layouts agree bitwise).
+    if (p.bm_global) {
+        attn_fwd_kernel<T, D, false, true><<<grid, kAttnThreads, L.total, stream>>>(q, k, v, p);
+    } else if constexpr (T == 128) {
+        if (paired)
+            attn_fwd_kernel<T, D, true, false><<<grid, kAttnThreads, L.total, stream>>>(q, k, v, p);
+        else
+            attn_fwd_kernel<T, D, false, false><<<grid, kAttnThreads, L.total, stream>>>(q, k, v, p);
+    } else {
+        attn_fwd_kernel<T, D, false, false><<<grid, kAttnThreads, L.total, stream>>>(q, k, v, p);
+    }
     return cudaGetLastError();
 }
 
@@ -1041,10 +1053,16 @@ AttnLaunchInfo info_t(int bm_words) {
 
 template <int T, int D>
 cudaError_t prepare_t() {
-    const cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<T, D, true>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemLimit);
+    cudaError_t e = cudaSuccess;
+    if constexpr (T == 128) {
+        e = cudaFuncSetAttribute(attn_fwd_kernel<T, D, true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kSmemLimit);
+        if (e != cudaSuccess) return e;
+    }
+    e = cudaFuncSetAttribute(attn_fwd_kernel<T, D, false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kSmemLimit);
     if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(attn_fwd_kernel<T, D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    return cudaFuncSetAttribute(attn_fwd_kernel<T, D, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 (int)kSmemLimit);
 }
 

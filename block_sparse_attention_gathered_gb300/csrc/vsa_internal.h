@@ -58,7 +58,8 @@ cudaError_t attn_prepare(int tile, int head_dim, int device);
 // Launches with p.stages taken from attn_launch_info (the caller's value is
 // ignored).  `paired` picks the MMA-issue role layout (both are exact; they
 // differ only in speed): paired for dense selections at T = D = 128, split
-// otherwise.
+// otherwise; with 64-token tiles or bitmaps in the workspace it is ignored
+// (split).
 cudaError_t launch_attn(int tile, int head_dim, bool paired, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
                         const CUtensorMap &tm_v, AttnParams p, int grid, cudaStream_t stream);
 
