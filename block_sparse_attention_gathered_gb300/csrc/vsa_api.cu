@@ -177,7 +177,7 @@ vsa_status check_dims_small(const vsa_dims *d) {
 
 // Workspace of the forward: a 256 B header (work counter), the order list,
 // and, beyond kSmemBitmapTiles kernel tiles, the selection bitmaps of every
-// CTA (two buffers of four bitmaps of ceil(kernel tiles / 32) words each),
+// CTA (two buffers of kItemBitmaps bitmaps of ceil(kernel tiles / 32) words each),
 // 256-byte aligned.
 int bitmap_words(const vsa_dims *d) { return (int)((kernel_tiles(d) + 31) / 32); }
 bool bitmaps_in_workspace(const vsa_dims *d) { return kernel_tiles(d) > kSmemBitmapTiles; }
@@ -186,7 +186,9 @@ size_t order_bytes_for(const vsa_dims *d) {
     return kWsHeader + (size_t)(n_items + kMaxSplit) * sizeof(int32_t);
 }
 size_t bitmap_offset_for(const vsa_dims *d) { return (order_bytes_for(d) + 255) & ~(size_t)255; }
-size_t bitmap_bytes_per_cta(const vsa_dims *d) { return (size_t)2 * 4 * bitmap_words(d) * sizeof(uint32_t); }
+size_t bitmap_bytes_per_cta(const vsa_dims *d) {
+    return (size_t)2 * kItemBitmaps * bitmap_words(d) * sizeof(uint32_t);
+}
 
 size_t workspace_bytes_for(const vsa_dims *d) {
     if (!bitmaps_in_workspace(d)) return order_bytes_for(d);

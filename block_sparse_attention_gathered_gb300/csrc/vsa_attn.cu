@@ -139,7 +139,7 @@ __host__ __device__ inline SmemPlan smem_plan(int bm_words, int NS) {
     s.q = 0;
     s.ring = 2 * C::kQBytes;
     s.bm = s.ring + (uint32_t)NS * C::kStageBytes;
-    s.hdr = s.bm + 2u * 4u * 4u * (uint32_t)bm_words;
+    s.hdr = s.bm + 2u * (uint32_t)kItemBitmaps * 4u * (uint32_t)bm_words;
     s.bars = s.hdr + 32;
     s.tslot = s.bars + 8u * (uint32_t)Bars{NS}.count();
     s.flag = s.tslot + 4;
@@ -235,8 +235,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     // fill has landed, which this count tells them.
     const uint32_t sProg = base + L.sprog;
     const uint32_t sRing = base + L.ring;
-    uint32_t *bm = kGB ? P.bm_global + (size_t)blockIdx.x * 2 * 4 * W
-                       : reinterpret_cast<uint32_t *>(gbase + L.bm);  // [2][4][W]
+    uint32_t *bm = kGB ? P.bm_global + (size_t)blockIdx.x * 2 * kItemBitmaps * W
+                       : reinterpret_cast<uint32_t *>(gbase + L.bm);  // [2][kItemBitmaps][W]
     volatile int32_t *hdr = reinterpret_cast<int32_t *>(gbase + L.hdr);  // [2][4]
     const uint32_t bars = base + L.bars;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(gbase + L.tslot);
@@ -328,11 +328,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             // order entries: work item << 2 | which units run (0 both, 1 or 2 one)
             const int entry = (slot < P.n_items) ? __ldg(P.order + slot) : -1;
             const int item = entry < 0 ? -1 : entry >> 2, mode = entry < 0 ? 0 : entry & 3;
-            uint32_t *bmp = bm + p * 4 * W;
+            uint32_t *bmp = bm + p * kItemBitmaps * W;
             int bad = 0;
             uint32_t n_tail = 0, n_full = 0;  // this lane's (query tile, key tile) steps
             if (item >= 0) {
-                for (int i = lane; i < 4 * W; i += 32) bmp[i] = 0u;
+                for (int i = lane; i < kItemBitmaps * W; i += 32) bmp[i] = 0u;
                 __syncwarp();
                 const int bh = item / P.G, g = item - (item / P.G) * P.G;
                 // selections are per caller tile: with 256-token tiles both units
@@ -366,6 +366,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                                 bad = 1;  // repeated index
                             } else if (nj < T) {
                                 ++n_tail;  // the softmax masks this step's columns past nj
+                                atomicOr(&bmp[4 * W + (jj >> 5)], bit);  // partial tile
                             } else {
                                 ++n_full;
                             }
@@ -454,12 +455,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             const int p = it & 1;
             if (!wait_warp(BAR(BI.bm_full(p)), (it >> 1) & 1u, abort_flag, P.status)) break;
             if (hdr[p * 4] < 0) break;
-            const uint32_t *bmp = bm + p * 4 * W;
+            const uint32_t *bmp = bm + p * kItemBitmaps * W;
             bool ok = true;
             for (int w = 0; w < W && ok; ++w) {
                 uint32_t bits = bmp[w] | bmp[W + w] | bmp[2 * W + w] | bmp[3 * W + w];
+                const uint32_t part_w = bmp[4 * W + w];  // partial tiles
                 while (bits) {
-                    const int j = w * 32 + __ffs(bits) - 1;
+                    const int b = __ffs(bits) - 1;
+                    const int j = w * 32 + b;
                     bits &= bits - 1;
                     const uint32_t kst = ring.st, kph = ring.ph;
                     ring.next(NS);
@@ -470,6 +473,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     // cycle ahead of the fills it waits for.
                     if (!(ok = wait_warp(BAR(BI.kv_full(kst)), kph, abort_flag, P.status))) break;
                     if (!(ok = wait_warp(BAR(BI.kv_full(vst)), vph, abort_flag, P.status))) break;
+                    if (!((part_w >> b) & 1u)) continue;
                     const int nj = tile_size(P.block_sizes, j, P.sub);
                     if ((nj & 15) == 0) continue;
                     uint4 *vs = reinterpret_cast<uint4 *>(gbase + L.ring + vst * C::kStageBytes);
@@ -514,7 +518,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 const int p = it & 1;
                 if (!(ok = wait_bar(BAR(BI.bm_full(p)), (it >> 1) & 1u, abort_flag, P.status))) break;
                 if (hdr[p * 4] < 0) break;
-                const uint32_t *bmp = bm + p * 4 * W;
+                const uint32_t *bmp = bm + p * kItemBitmaps * W;
                 const uint32_t *pa = bmp + (2 * u) * W, *pb = pa + W;
                 // member entries of this unit, so Q can be released right after its last S
                 uint32_t n_mine = 0;
@@ -557,6 +561,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
                 for (int w = 0; w < W && ok; ++w) {
                     const uint32_t mw = pa[w] | pb[w];
+                    const uint32_t part_w = bmp[4 * W + w];  // partial tiles
                     uint32_t bits = bmp[w] | bmp[W + w] | bmp[2 * W + w] | bmp[3 * W + w];
                     while (bits && ok) {
                         const int b = __ffs(bits) - 1;
@@ -566,7 +571,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         ring.next(NS);
                         const uint32_t vst = ring.st, vph = ring.ph;
                         ring.next(NS);
-                        const int nj = tile_size(P.block_sizes, j, P.sub);
+                        const int nj = ((part_w >> b) & 1u) ? tile_size(P.block_sizes, j, P.sub) : T;
                         const bool tail = (nj & 15) != 0;
                         const uint32_t vzp = (vz_par >> vst) & 1u;
                         if (tail) vz_par ^= 1u << vst;
@@ -648,7 +653,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 const int p = it & 1;
                 if (!(ok = wait_bar(BAR(BI.bm_full(p)), (it >> 1) & 1u, abort_flag, P.status))) break;
                 if (hdr[p * 4] < 0) break;
-                const uint32_t *bmp = bm + p * 4 * W;
+                const uint32_t *bmp = bm + p * kItemBitmaps * W;
                 // member entries per unit, so Q_u is released right after its last S
                 uint32_t n_mine[2] = {0u, 0u}, seen[2] = {0u, 0u};
                 for (int w = 0; w < W; ++w) {
@@ -745,10 +750,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             const int p = it & 1;
             if (!(ok = wait_warp(BAR(BI.bm_full(p)), (it >> 1) & 1u, abort_flag, P.status))) break;
             if (hdr[p * 4] < 0) break;
-            const uint32_t *bmp = bm + p * 4 * W;
+            const uint32_t *bmp = bm + p * kItemBitmaps * W;
             bool first = true;
             for (int w = 0; w < W && ok; ++w) {
                 const uint32_t mw = bmp[(2 * u) * W + w] | bmp[(2 * u + 1) * W + w];
+                const uint32_t part_w = bmp[4 * W + w];  // partial tiles
                 uint32_t bits = bmp[w] | bmp[W + w] | bmp[2 * W + w] | bmp[3 * W + w];
                 while (bits && ok) {
                     const int b = __ffs(bits) - 1;
@@ -767,7 +773,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         break;
                     if (!(ok = __all_sync(0xffffffffu, wait_bar_spin(BAR(BI.kv_full(vst)), vph, abort_flag, P.status))))
                         break;
-                    const int nj = tile_size(P.block_sizes, j, P.sub);
+                    const int nj = ((part_w >> b) & 1u) ? tile_size(P.block_sizes, j, P.sub) : T;
                     const bool tail = (nj & 15) != 0;
                     const uint32_t vzp = (vz_par >> vst) & 1u;
                     if (tail) {
@@ -861,7 +867,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             const int item = hdr[p * 4];
             const int mode = hdr[p * 4 + 1];
             if (item < 0) break;
-            const uint32_t *bmp = bm + p * 4 * W;
+            const uint32_t *bmp = bm + p * kItemBitmaps * W;
             const int bh = item / P.G, g = item - (item / P.G) * P.G;
             const int t = (T == 128) ? 2 * g + u : 4 * g + 2 * u + tsub;
             const int r = (T == 128) ? row : (row & 63);
@@ -884,14 +890,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             for (int w = 0; w < W && ok; ++w) {
                 uint32_t bits = pa[w] | pb[w];
                 const uint32_t mine = pm[w];
+                const uint32_t part_w = bmp[4 * W + w];  // partial tiles
                 while (bits) {
                     const int b = __ffs(bits) - 1;
                     bits &= bits - 1;
                     const int j = w * 32 + b;
-                    const int nj = tile_size(P.block_sizes, j, P.sub);  // loaded before the wait for S
+                    // valid keys: read only for partial tiles, before the wait for S
+                    const int nj = ((part_w >> b) & 1u) ? tile_size(P.block_sizes, j, P.sub) : T;
                     if (!(ok = wait_warp(BAR(BI.s_full(u)), cnt & 1u, abort_flag, P.status))) break;
                     tc_fence_after();
-                    const bool member_row = ((mine >> b) & 1u) != 0u;  // warp-uniform
+                    // warp-uniform; with 128-token tiles every entry of the unit is its own
+                    const bool member_row = (T == 128) || ((mine >> b) & 1u) != 0u;
                     float s[TH];
                     if (member_row) {
                         if constexpr (T == 128) tmem_ld2x_64<TH>(tS, s);

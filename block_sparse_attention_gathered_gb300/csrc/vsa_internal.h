@@ -16,6 +16,11 @@ constexpr int kUnitRows = 128;
 constexpr int kItemRows = 256;
 constexpr int kAttnThreads = 640;  // 16 softmax warps, 2 MMA issuers, 1 producer, 1 fix-up warp
 constexpr int kSmemBitmapTiles = 8192;  // VSA_SMEM_BITMAP_TILES
+// Bitmaps per work-item buffer of the attention kernel: the four selection
+// bitmaps (one per query-tile slot) and one of the selected tiles that are
+// partial (fewer valid keys than the tile), so the kernel reads block_sizes
+// only for those.
+constexpr int kItemBitmaps = 5;
 constexpr int kMaxGridCtas = 1024;      // bound on the attention grid (one CTA per SM), for workspace sizing
 
 struct AttnParams {

@@ -109,7 +109,8 @@ def test_tile_256_limits(vsa):
 def test_bitmap_workspace_beyond_shared_memory(vsa):
     # up to 8192 kernel tiles the selection bitmaps live in shared memory and
     # the workspace is the header plus the order list; beyond, each CTA (at
-    # most 1024, at most one per work item) gets 2 x 4 bitmaps in the workspace
+    # most 1024, at most one per work item) gets 2 x 5 bitmaps in the workspace
+    # (two buffers of the four slot bitmaps and the partial-tile bitmap)
     small = vsa.make_dims(1, 1, 8192, 64, 64, 2)
     items = 8192 * 64 // 256
     assert vsa.vsa_block_sparse_workspace_size(small) == 256 + 4 * (items + 256)
@@ -117,11 +118,11 @@ def test_bitmap_workspace_beyond_shared_memory(vsa):
     items = 8200 * 64 // 256
     order = 256 + 4 * (items + 256)
     words = (8200 + 31) // 32
-    assert vsa.vsa_block_sparse_workspace_size(big) == ((order + 255) // 256) * 256 + 1024 * 2 * 4 * words * 4
+    assert vsa.vsa_block_sparse_workspace_size(big) == ((order + 255) // 256) * 256 + 1024 * 2 * 5 * words * 4
     few = vsa.make_dims(1, 1, 8200, 256, 64, 2)  # 16400 kernel tiles, 8200 work items
     words = (16400 + 31) // 32
     order = 256 + 4 * (8200 + 256)
-    assert vsa.vsa_block_sparse_workspace_size(few) == ((order + 255) // 256) * 256 + 1024 * 2 * 4 * words * 4
+    assert vsa.vsa_block_sparse_workspace_size(few) == ((order + 255) // 256) * 256 + 1024 * 2 * 5 * words * 4
     # one 256-row work item per 256-token tile
     assert vsa.vsa_block_sparse_workspace_size(vsa.make_dims(2, 3, 10, 256, 64, 4)) == 256 + 4 * (6 * 10 + 256)
 
