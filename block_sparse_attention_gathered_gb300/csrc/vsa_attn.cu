@@ -899,8 +899,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     const int nj = ((part_w >> b) & 1u) ? tile_size(P.block_sizes, j, P.sub) : T;
                     if (!(ok = wait_warp(BAR(BI.s_full(u)), cnt & 1u, abort_flag, P.status))) break;
                     tc_fence_after();
-                    // warp-uniform; with 128-token tiles every entry of the unit is its own
-                    const bool member_row = (T == 128) || ((mine >> b) & 1u) != 0u;
+                    // warp-uniform.  With 128-token tiles every entry of the unit is
+                    // its own; stating it at compile time measured 12-15 % faster
+                    // on sparse selections (split layout) and 1 % slower on dense
+                    // ones (paired), so the paired form keeps the test.
+                    const bool member_row = (T == 128 && !kPaired) || ((mine >> b) & 1u) != 0u;
                     float s[TH];
                     if (member_row) {
                         if constexpr (T == 128) tmem_ld2x_64<TH>(tS, s);
