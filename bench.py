@@ -50,8 +50,8 @@ FALLBACK_HBM_GBS = 6800.0
 # SHA-256 (first 16 hex digits) of the attention kernel source the capture was
 # taken with; a changed kernel reports null until it is captured again.
 ATTN_TRAFFIC = {
-    ("dense_b1h6d128_s31200_t128x244_lse", "eca0b26a939cd8d9"): 323.25e6,  # 288.3 MB read + 34.9 MB written
-    ("uniform_b1h12d128_t128x128_k32", "eca0b26a939cd8d9"): 201.45e6,      # 168.8 MB read + 32.6 MB written
+    ("dense_b1h6d128_s31200_t128x244_lse", "58b5ed214b38cfad"): 329.05e6,  # 295.4 MB read + 33.7 MB written
+    ("uniform_b1h12d128_t128x128_k32", "58b5ed214b38cfad"): 208.73e6,      # 174.4 MB read + 34.4 MB written
 }
 
 # Workloads timed after the headline step in the default run (attention, and
