@@ -19,9 +19,11 @@
 //   * S_u = Q_u K_j^T (tcgen05, smem x smem -> TMEM) for the key tiles unit u
 //     selects, and O_u += P_u V_j with P read from TMEM, are issued in one of
 //     two layouts (a template parameter; the host picks it from the
-//     selection width).  One thread issues tcgen05.mma at about 88 cycles an
-//     instruction, while two threads issuing at once keep the tensor pipe at
-//     its full rate (64 cycles an M128 N128 K16 MMA):
+//     selection width).  One thread issues back-to-back MMAs at the pipe's
+//     rate (measured: 64 cycles an M128 N128 K16 MMA; an M128 N64 K16 S
+//     product takes 48, the time its 6 KB of shared-memory operands take at
+//     128 bytes a clock); the layouts differ in which waits sit between the
+//     MMAs of one thread:
 //       - paired (dense selections): one thread per unit issues both of its
 //         products, the next S before the current P V, which keeps P V out of
 //         the way of the S hand-off between the units;
@@ -306,11 +308,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       //     next S keeps out of its way.
       //   split (sparse selections, where a key tile mostly serves one unit):
       //     lane 0 of warp 16 issues every S; warp 17 + 2u issues O_u += P_u V
-      //     as soon as P_u is stored; warp 17 zeroes tail V rows.  One thread
-      //     issues tcgen05.mma at about 88 cycles an instruction, while two
-      //     threads issuing at once keep the tensor pipe at its full rate (64
-      //     cycles an M128 N128 K16 MMA), so the S stream and the P V streams
-      //     overlap instead of queueing in one thread.
+      //     as soon as P_u is stored; warp 17 zeroes tail V rows.  The S
+      //     stream and the P V streams wait on different barriers, so with
+      //     separate issuing threads neither waits behind the other.
       constexpr bool paired = kPaired;
       if (warp == kProducerWarp) {
         // ------------------------------------------------------------ producer

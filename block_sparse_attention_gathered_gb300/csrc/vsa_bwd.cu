@@ -36,9 +36,10 @@
 //                  write P^T and dS^T as bf16 back over the columns they read;
 //                  dV += P^T dO_t and dK += dS^T Q_t accumulate in TMEM with
 //                  the A operand taken from the slot.  One thread issues the
-//                  accumulations, a second the copies and S, a third dP (one
-//                  thread issues tcgen05.mma at about 88 cycles an
-//                  instruction, so the N = 64 products need two issuers); S
+//                  accumulations, a second the copies and S, a third dP (the
+//                  N = 64 products each read 6 KB of shared-memory operands,
+//                  48 cycles at 128 bytes a clock, and a thread issuing them
+//                  also waits on its barriers; two issuers overlap that); S
 //                  and dP go into a slot as soon as the previous pair's
 //                  accumulations have read it: the next pair's products
 //                  overlap this pair's elementwise step.
@@ -510,10 +511,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 ++issued[b];
             };
-            // S of the half hv of pair i into slot hv (dP: warp kDpWarp).  One
-            // thread issues tcgen05.mma at about 88 cycles an instruction, about
-            // three times the 128 x 64 product's own time, so S and dP, which
-            // go to different columns of the slot, are issued by two threads.
+            // S of the half hv of pair i into slot hv (dP: warp kDpWarp).  S and
+            // dP go to different columns of the slot and are issued by two
+            // threads, so each thread's barrier waits overlap the other's
+            // products.
             auto issue_sdp = [&](int i, int hv) {
                 const int b = i & 1;
                 // KV: S^T = K_j Q_t^T; else S = Q_t K_j^T
