@@ -895,8 +895,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     const int b = __ffs(bits) - 1;
                     bits &= bits - 1;
                     const int j = w * 32 + b;
-                    // valid keys: read only for partial tiles, before the wait for S
-                    const int nj = ((part_w >> b) & 1u) ? tile_size(P.block_sizes, j, P.sub) : T;
+                    // valid keys, loaded before the wait for S: in the split layout
+                    // only for partial tiles; the paired form loads every tile's
+                    // count (the load hides under the wait, and this form measured
+                    // 2 % faster on dense selections than the bitmap test)
+                    const int nj = (kPaired || ((part_w >> b) & 1u)) ? tile_size(P.block_sizes, j, P.sub) : T;
                     if (!(ok = wait_warp(BAR(BI.s_full(u)), cnt & 1u, abort_flag, P.status))) break;
                     tc_fence_after();
                     // warp-uniform.  With 128-token tiles every entry of the unit is
