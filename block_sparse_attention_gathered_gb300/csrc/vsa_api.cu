@@ -382,12 +382,32 @@ vsa_status vsa_block_sparse_fwd(const void *q, const void *k, const void *v, con
         dc.attn_prepared.fetch_or(variant_bit, std::memory_order_acq_rel);
     }
 
+    // The dense form: when the rows of q2k_idx can hold every key tile (a
+    // dense selection) or with 256-token tiles (both units are halves of one
+    // query tile and share its selection).
+    //  * 128-token kernel tiles, D = 128: the paired MMA-issue layout.  The
+    //    split layout measured faster as soon as a few key tiles serve only
+    //    one unit (95 % selections included), and at every density with
+    //    D = 64, where a P V product is N = 64 wide.
+    //  * 64-token tiles: ring entries of key-tile pairs, so S is N = 128 wide
+    //    (dense T64 D128: 2.86 -> 2.50 ms).  Pairs measured 1.5-1.8 times
+    //    slower on top-k and uniform sparse selections, which rarely take both
+    //    tiles of a pair.
+    // The host cannot see the selections without a sync, so the row length
+    // stands in for the density.  Results do not depend on the form.  It runs
+    // with the selection bitmaps in shared memory only.
+    const bool dense_sel = sub == 2 || dims->max_kv >= NT;
+    const bool paired = !bitmaps_in_workspace(dims) && dense_sel && ((Tk == 128 && D == 128) || Tk == 64);
+    const int key_rows = (Tk == 64 && paired) ? 128 : Tk;
+
     const int64_t Sp = (int64_t)NT * T;
     const int64_t rows = (int64_t)dims->B * dims->H * Sp;
     CUtensorMap tm_q, tm_k, tm_v;
     if ((st = encode_rows_map(&tm_q, q, rows, D, kUnitRows)) != VSA_OK) return st;
-    if ((st = encode_rows_map(&tm_k, k, rows, D, Tk)) != VSA_OK) return st;
-    if ((st = encode_rows_map(&tm_v, v, rows, D, Tk)) != VSA_OK) return st;
+    // K and V go by ring entries of key_rows rows (a tile, or a pair of
+    // 64-token tiles)
+    if ((st = encode_rows_map(&tm_k, k, rows, D, key_rows)) != VSA_OK) return st;
+    if ((st = encode_rows_map(&tm_v, v, rows, D, key_rows)) != VSA_OK) return st;
 
     const int G = (int)items_per_seq(dims);
     const int n_items = (int)((int64_t)dims->B * dims->H * G);
@@ -432,19 +452,9 @@ vsa_status vsa_block_sparse_fwd(const void *q, const void *k, const void *v, con
     p.Sp = Sp;
     const float scale = dims->scale > 0.f ? dims->scale : 1.0f / std::sqrt((float)D);
     p.scale_log2 = scale * 1.4426950408889634f;
-    // MMA-issue layout: paired for 128-token kernel tiles with D = 128 when
-    // the rows of q2k_idx can hold every key tile (a dense selection: every
-    // key tile then serves both query units of a work item) or with 256-token
-    // tiles (both units are halves of one query tile and share its
-    // selection); split otherwise.  Split measured faster as soon as a few
-    // key tiles serve only one unit (95 % selections included), and at every
-    // density with 64-token tiles or D = 64, where a product is N = 64 wide.
-    // The host cannot see the selections without a sync, so the row length
-    // stands in for the density.  Results do not depend on the layout.
-    const bool paired = !p.bm_global && Tk == 128 && D == 128 && (sub == 2 || dims->max_kv >= NT);
     if (launch_attn(Tk, D, paired, tm_q, tm_k, tm_v, p, grid, s) != cudaSuccess) return VSA_ERR_CUDA;
 
-    const AttnLaunchInfo info = attn_launch_info(Tk, D, p.bm_global ? 0 : p.bm_words);
+    const AttnLaunchInfo info = attn_launch_info(Tk, D, p.bm_global ? 0 : p.bm_words, paired);
     t_route.kernel = VSA_KERNEL_ATTN_TCGEN05;
     t_route.tile = T;
     t_route.head_dim = D;

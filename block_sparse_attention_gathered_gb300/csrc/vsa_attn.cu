@@ -91,25 +91,42 @@ template <int T> struct RegSplit {
 constexpr uint32_t kSmemLimit = 232448;  // 227 KB opt-in per CTA
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when the max grows by > 2^8
 
-template <int T, int D>
+// Key rows of one ring entry: a tile, or for the dense form at 64-token tiles
+// a pair of tiles.
+template <int T, bool kDense>
+__host__ __device__ constexpr int key_rows() {
+    return (T == 64 && kDense) ? 128 : T;
+}
+
+template <int T, int D, int KEYROWS>
 struct Cfg {
     static_assert(T == 64 || T == 128, "tile");
+    static_assert(KEYROWS == T || (T == 64 && KEYROWS == 128), "key rows per ring entry");
     static_assert(D == 64 || D == 128, "head_dim");
     static constexpr int kChunks = D / 64;                    // 128-byte column chunks per row
     static constexpr uint32_t kQChunk = kUnitRows * 128;      // bytes of one Q column chunk
     static constexpr uint32_t kQBytes = kUnitRows * D * 2;    // one unit's Q
-    static constexpr uint32_t kKVChunk = T * 128;             // bytes of one K/V column chunk
-    static constexpr uint32_t kStageBytes = T * D * 2;        // one K or V tile
+    // A ring entry holds KT key rows: one tile, or (the dense form at 64-token
+    // tiles) the pair of tiles (2m, 2m+1), which sit back to back in the
+    // tile-major layout.  S of a pair entry is N = 128 wide, which runs at the
+    // tensor pipe's rate; an N = 64 S product is bound by its 6 KB of
+    // shared-memory operands (48 cycles against 32 of math).  Pairs stream a
+    // key tile no query tile selects whenever its partner is selected, so
+    // they are taken only for dense selections.
+    static constexpr int KT = KEYROWS;
+    static constexpr uint32_t kKVChunk = KT * 128;            // bytes of one K/V column chunk
+    static constexpr uint32_t kStageBytes = KT * D * 2;       // one entry's K or V
     // TMEM columns: O of each unit (fp32), S (fp32) and P of each unit (bf16
     // pairs).  With 128-token tiles the units take turns on one S buffer (a
     // second does not fit next to two O and two P); with 64-token tiles each
     // unit has its own, so one unit's S never waits for the other's to be
     // copied out.
-    static constexpr int kSBufs = (T == 64) ? 2 : 1;
-    static constexpr uint32_t kTmemO0 = 0, kTmemO1 = D, kTmemS0 = 2 * D, kTmemS1 = 2 * D + (kSBufs - 1) * T,
-                              kTmemP0 = 2 * D + kSBufs * T, kTmemP1 = 2 * D + kSBufs * T + T / 2;
-    static constexpr uint32_t kTmemCols = (2 * D + (kSBufs + 1) * T <= 256) ? 256 : 512;
-    static constexpr uint32_t kIdescQK = idesc_bf16(128, T, false);
+    static constexpr int kSBufs = (T == 64 && 2 * D + 3 * KT <= 512) ? 2 : 1;
+    static constexpr uint32_t kTmemO0 = 0, kTmemO1 = D, kTmemS0 = 2 * D, kTmemS1 = 2 * D + (kSBufs - 1) * KT,
+                              kTmemP0 = 2 * D + kSBufs * KT, kTmemP1 = 2 * D + kSBufs * KT + KT / 2;
+    static constexpr uint32_t kTmemCols = (2 * D + (kSBufs + 1) * KT <= 256) ? 256 : 512;
+    static_assert(2 * D + (kSBufs + 1) * KT <= 512, "TMEM plan");
+    static constexpr uint32_t kIdescQK = idesc_bf16(128, KT, false);
     static constexpr uint32_t kIdescPV = idesc_bf16(128, D, true);
 };
 
@@ -134,9 +151,9 @@ struct SmemPlan {
     uint32_t q, ring, bm, hdr, bars, tslot, flag, sfree, sprog, total;
 };
 
-template <int T, int D>
+template <int T, int D, int KT>
 __host__ __device__ inline SmemPlan smem_plan(int bm_words, int NS) {
-    using C = Cfg<T, D>;
+    using C = Cfg<T, D, KT>;
     SmemPlan s;
     s.q = 0;
     s.ring = 2 * C::kQBytes;
@@ -151,10 +168,10 @@ __host__ __device__ inline SmemPlan smem_plan(int bm_words, int NS) {
     return s;
 }
 
-template <int T, int D>
+template <int T, int D, int KT>
 inline int stages_for(int bm_words) {
     int ns = kMaxStages;
-    while (ns > 2 && smem_plan<T, D>(bm_words, ns).total > kSmemLimit) --ns;
+    while (ns > 2 && smem_plan<T, D, KT>(bm_words, ns).total > kSmemLimit) --ns;
     return ns;
 }
 
@@ -193,6 +210,15 @@ __device__ __forceinline__ bool wait_count(uint32_t addr, uint32_t target, volat
     }
 }
 
+// Ring entries of a 32-tile bitmap word x (the union of an item's slots): bit
+// b marks an entry whose key rows start at kernel tile 32w + b.  When an entry
+// is a pair of 64-token tiles (2m, 2m+1) it is marked at the even bit.
+template <int T, int KT>
+__device__ __forceinline__ uint32_t entry_bits(uint32_t x) {
+    if (KT == T) return x;
+    return (x | (x >> 1)) & 0x55555555u;
+}
+
 // Tile index held by bitmap slot s (unit = s/2, half = s%2) of item g.
 template <int T>
 __device__ __forceinline__ int tile_of_slot(int g, int s) {
@@ -209,11 +235,15 @@ __device__ __forceinline__ int tile_size(const int32_t *block_sizes, int jj, int
     return n < 0 ? 0 : (n > 128 ? 128 : n);
 }
 
+// kPaired selects the dense form: with 128-token tiles the paired MMA-issue
+// layout, with 64-token tiles ring entries of key-tile pairs (issued in the
+// split layout).
 template <int T, int D, bool kPaired, bool kGB>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const AttnParams P) {
-    using C = Cfg<T, D>;
+    using C = Cfg<T, D, key_rows<T, kPaired>()>;
+    constexpr bool kIssuePaired = kPaired && T == 128;  // the paired MMA-issue layout
     const int NS = P.stages;
     const Bars BI{NS};
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -225,7 +255,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     // kSmemBitmapTiles kernel tiles) in this CTA's region of the workspace;
     // a compile-time choice, so the shared-memory form reads them with
     // shared-memory loads
-    const SmemPlan L = smem_plan<T, D>(kGB ? 0 : W, NS);
+    const SmemPlan L = smem_plan<T, D, C::KT>(kGB ? 0 : W, NS);
     const uint32_t sQ = base + L.q;
     // Count of S tiles the softmax warps have copied out of an S buffer (each
     // of the eight warps of a unit adds 1 per S): one shared count, or one per
@@ -251,7 +281,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < NS; ++s) {
             mbar_init(BAR(BI.kv_full(s)), 1);
-            mbar_init(BAR(BI.kv_empty(s)), kPaired ? kPairedIssuers : kIssuers);  // arrivals per fill
+            mbar_init(BAR(BI.kv_empty(s)), kIssuePaired ? kPairedIssuers : kIssuers);  // arrivals per fill
             mbar_init(BAR(BI.vz(s)), 32);
         }
         #pragma unroll
@@ -311,7 +341,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       //     as soon as P_u is stored; warp 17 zeroes tail V rows.  The S
       //     stream and the P V streams wait on different barriers, so with
       //     separate issuing threads neither waits behind the other.
-      constexpr bool paired = kPaired;
+      constexpr bool paired = kIssuePaired;
       if (warp == kProducerWarp) {
         // ------------------------------------------------------------ producer
         const uint64_t pol_kv = l2_policy_evict_last();
@@ -407,10 +437,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             if (!ok) break;
             ++q_loads;
             for (int w = 0; w < W && ok; ++w) {
-                uint32_t bits = bmp[w] | bmp[W + w] | bmp[2 * W + w] | bmp[3 * W + w];
+                uint32_t bits = entry_bits<T, C::KT>(bmp[w] | bmp[W + w] | bmp[2 * W + w] | bmp[3 * W + w]);
                 while (bits && ok) {
-                    const int j = w * 32 + __ffs(bits) - 1;
+                    const int j = w * 32 + __ffs(bits) - 1;  // first kernel tile of the entry
                     bits &= bits - 1;
+                    // KT rows from tile j on (for a pair of 64-token tiles j and
+                    // j + 1; past the last tile the box reads rows no product uses)
                     const int32_t krow = (int32_t)((int64_t)bh * Sp + (int64_t)j * T);
                     for (int kv = 0; kv < 2; ++kv) {
                         const uint32_t st = ring.st;
@@ -657,8 +689,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 // member entries per unit, so Q_u is released right after its last S
                 uint32_t n_mine[2] = {0u, 0u}, seen[2] = {0u, 0u};
                 for (int w = 0; w < W; ++w) {
-                    n_mine[0] += __popc(bmp[w] | bmp[W + w]);
-                    n_mine[1] += __popc(bmp[2 * W + w] | bmp[3 * W + w]);
+                    n_mine[0] += __popc(entry_bits<T, C::KT>(bmp[w] | bmp[W + w]));
+                    n_mine[1] += __popc(entry_bits<T, C::KT>(bmp[2 * W + w] | bmp[3 * W + w]));
                 }
 #pragma unroll
                 for (int u = 0; u < 2; ++u)
@@ -666,7 +698,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 if (!ok) break;
                 tc_fence_after();
                 for (int w = 0; w < W && ok; ++w) {
-                    const uint32_t m0w = bmp[w] | bmp[W + w], m1w = bmp[2 * W + w] | bmp[3 * W + w];
+                    // entries each unit takes part in
+                    const uint32_t m0w = entry_bits<T, C::KT>(bmp[w] | bmp[W + w]);
+                    const uint32_t m1w = entry_bits<T, C::KT>(bmp[2 * W + w] | bmp[3 * W + w]);
                     uint32_t bits = m0w | m1w;
                     while (bits && ok) {
                         const int b = __ffs(bits) - 1;
@@ -753,14 +787,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             const uint32_t *bmp = bm + p * kItemBitmaps * W;
             bool first = true;
             for (int w = 0; w < W && ok; ++w) {
-                const uint32_t mw = bmp[(2 * u) * W + w] | bmp[(2 * u + 1) * W + w];
-                const uint32_t part_w = bmp[4 * W + w];  // partial tiles
-                uint32_t bits = bmp[w] | bmp[W + w] | bmp[2 * W + w] | bmp[3 * W + w];
+                const uint32_t sa_w = bmp[(2 * u) * W + w], sb_w = bmp[(2 * u + 1) * W + w];  // this unit's tiles
+                const uint32_t all_w = bmp[w] | bmp[W + w] | bmp[2 * W + w] | bmp[3 * W + w];
+                const uint32_t mw = entry_bits<T, C::KT>(sa_w | sb_w);  // entries this unit takes part in
+                const uint32_t part_w = bmp[4 * W + w];          // partial tiles
+                uint32_t bits = entry_bits<T, C::KT>(all_w);
                 while (bits && ok) {
                     const int b = __ffs(bits) - 1;
                     bits &= bits - 1;
                     const int j = w * 32 + b;
-                    ring.next(NS);  // K fill of tile j: the S issuer waits for it and releases it
+                    ring.next(NS);  // K fill of entry j: the S issuer waits for it and releases it
                     const uint32_t vst = ring.st, vph = ring.ph;
                     ring.next(NS);
                     const uint32_t vfill = fills + 1;  // index of this V fill
@@ -773,18 +809,32 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         break;
                     if (!(ok = __all_sync(0xffffffffu, wait_bar_spin(BAR(BI.kv_full(vst)), vph, abort_flag, P.status))))
                         break;
-                    const int nj = ((part_w >> b) & 1u) ? tile_size(P.block_sizes, j, P.sub) : T;
-                    const bool tail = (nj & 15) != 0;
+                    // valid keys of each tile of the entry (64-token tiles: the
+                    // pair j, j + 1, rows 64h on); a tail is a tile some product
+                    // reads whose valid keys end inside a 16-key block
+                    constexpr int kHalves = C::KT / T;
+                    int nj[kHalves];
+                    bool tail = false;
+#pragma unroll
+                    for (int h = 0; h < kHalves; ++h) {
+                        nj[h] = ((part_w >> (b + h)) & 1u) ? tile_size(P.block_sizes, j + h, P.sub) : T;
+                        if (((all_w >> (b + h)) & 1u) && (nj[h] & 15) != 0) tail = true;
+                    }
                     const uint32_t vzp = (vz_par >> vst) & 1u;
                     if (tail) {
                         vz_par ^= 1u << vst;
                         if (fixer) {
                             uint4 *vs = reinterpret_cast<uint4 *>(gbase + L.ring + vst * C::kStageBytes);
-                            const int n16 = (16 - (nj & 15)) * 8;
 #pragma unroll
-                            for (int c = 0; c < C::kChunks; ++c)
-                                for (int i = lane; i < n16; i += 32)
-                                    vs[(c * C::kKVChunk + nj * 128) / 16 + i] = make_uint4(0u, 0u, 0u, 0u);
+                            for (int h = 0; h < kHalves; ++h) {
+                                if (!((all_w >> (b + h)) & 1u) || (nj[h] & 15) == 0) continue;
+                                const int r0 = h * T + nj[h];  // first padding row of the tile
+                                const int n16 = (16 - (nj[h] & 15)) * 8;
+#pragma unroll
+                                for (int c = 0; c < C::kChunks; ++c)
+                                    for (int i = lane; i < n16; i += 32)
+                                        vs[(c * C::kKVChunk + r0 * 128) / 16 + i] = make_uint4(0u, 0u, 0u, 0u);
+                            }
                             fence_proxy_async_smem();
                             __syncwarp();
                             mbar_arrive(BAR(BI.vz(vst)));
@@ -800,17 +850,26 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         if (lane == 0) {
                             tc_fence_after();
                             const uint64_t bd = dv + vst * kStage16;
-                            const int kb = (nj + 15) >> 4;  // 16-key blocks holding valid keys
                             if constexpr (T == 64) {
-                                // two 64-row tiles share the accumulator: rows of a tile
-                                // that does not select j are left out of the product
-                                const uint32_t off_lo = ((bmp[(2 * u) * W + w] >> b) & 1u) ? 0u : ~0u;
-                                const uint32_t off_hi = ((bmp[(2 * u + 1) * W + w] >> b) & 1u) ? 0u : ~0u;
+                                // two 64-row query tiles share the accumulator and two
+                                // 64-key tiles the entry: the 16-key blocks of key tile
+                                // j + h go only to the query tiles that select it (the
+                                // other's 64 output lanes disabled), and only up to its
+                                // valid keys
 #pragma unroll
-                                for (int kk = 0; kk < T / 16; ++kk)
-                                    if (kk < kb)
-                                        mma_ts_lanes(tO, tP + kk * 8, bd + kk * 128, C::kIdescPV, 1u, off_lo, off_hi);
+                                for (int h = 0; h < kHalves; ++h) {
+                                    const uint32_t lo = (sa_w >> (b + h)) & 1u, hi = (sb_w >> (b + h)) & 1u;
+                                    if (!(lo | hi)) continue;
+                                    const uint32_t off_lo = lo ? 0u : ~0u, off_hi = hi ? 0u : ~0u;
+                                    const int kb = (nj[h] + 15) >> 4;  // 16-key blocks holding valid keys
+#pragma unroll
+                                    for (int kk = 0; kk < T / 16; ++kk)
+                                        if (kk < kb)
+                                            mma_ts_lanes(tO, tP + (h * (T / 16) + kk) * 8, bd + (h * (T / 16) + kk) * 128,
+                                                         C::kIdescPV, 1u, off_lo, off_hi);
+                                }
                             } else {
+                                const int kb = (nj[0] + 15) >> 4;  // 16-key blocks holding valid keys
                                 mma_ts(tO, tP, bd, C::kIdescPV, first ? 0u : 1u);
 #pragma unroll
                                 for (int kk = 1; kk < T / 16; ++kk)
@@ -843,9 +902,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         // Eight warps per unit, two threads per query row in the same warp.
         // Warp 8u + 4sb + q4 takes TMEM lanes (rows) 32q4 + 16sb .. +15 with
         // the .16x32bx2 shape: thread t holds row t%16 and the columns of half
-        // t/16 (S: T/2 columns, O: D/2 columns, P: T/4 packed columns).  The
-        // row maximum and the final row sum combine the halves with one shuffle.
-        constexpr int TH = T / 2;   // S columns per thread
+        // t/16 (S: 64 columns, O: D/2 columns, P: 32 packed columns).  With
+        // 64-token tiles a half is exactly one key tile of the entry's pair.
+        // The row maximum and the final row sum combine the halves with one
+        // shuffle.
+        constexpr int TH = C::KT / 2;  // S columns per thread
         constexpr int DH = D / 2;   // O columns per thread
         const int u = warp >> 3;
         const int sb = (warp >> 2) & 1;
@@ -888,28 +949,35 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 for (int ch = 0; ch < DH / 8; ++ch) tmem_st2x_8f<DH>(tO + ch * 8, z);
             }
             for (int w = 0; w < W && ok; ++w) {
-                uint32_t bits = pa[w] | pb[w];
+                uint32_t bits = entry_bits<T, C::KT>(pa[w] | pb[w]);
                 const uint32_t mine = pm[w];
                 const uint32_t part_w = bmp[4 * W + w];  // partial tiles
                 while (bits) {
                     const int b = __ffs(bits) - 1;
                     bits &= bits - 1;
                     const int j = w * 32 + b;
-                    // valid keys, loaded before the wait for S: in the split layout
-                    // only for partial tiles; the paired form loads every tile's
-                    // count (the load hides under the wait, and this form measured
-                    // 2 % faster on dense selections than the bitmap test)
-                    const int nj = (kPaired || ((part_w >> b) & 1u)) ? tile_size(P.block_sizes, j, P.sub) : T;
+                    // This thread's key tile (j, or j + hf of a 64-token pair) and
+                    // its valid keys, loaded before the wait for S: in the split
+                    // layout only for partial tiles; the paired form loads every
+                    // tile's count (the load hides under the wait, and this form
+                    // measured 2 % faster on dense selections than the bitmap test)
+                    const int jt = (C::KT == T) ? j : j + hf;
+                    const int nj =
+                        (kIssuePaired || ((part_w >> (jt & 31)) & 1u)) ? tile_size(P.block_sizes, jt, P.sub) : T;
                     if (!(ok = wait_warp(BAR(BI.s_full(u)), cnt & 1u, abort_flag, P.status))) break;
                     tc_fence_after();
-                    // warp-uniform.  With 128-token tiles every entry of the unit is
+                    // warp-uniform: does this warp's query tile take part in the
+                    // entry?  With 128-token tiles every entry of the unit is
                     // its own; stating it at compile time measured 12-15 % faster
                     // on sparse selections (split layout) and 1 % slower on dense
                     // ones (paired), so the paired form keeps the test.
-                    const bool member_row = (T == 128 && !kPaired) || ((mine >> b) & 1u) != 0u;
+                    const bool member_row =
+                        (T == 128 && !kIssuePaired) || ((entry_bits<T, C::KT>(mine) >> b) & 1u) != 0u;
+                    // per thread with 64-token tiles: does it select this half's tile?
+                    const bool member_t = (C::KT == T) || ((mine >> (jt & 31)) & 1u) != 0u;
                     float s[TH];
                     if (member_row) {
-                        if constexpr (T == 128) tmem_ld2x_64<TH>(tS, s);
+                        if constexpr (TH == 64) tmem_ld2x_64<TH>(tS, s);
                         else tmem_ld2x_32<TH>(tS, s);
                     }
                     // S is in registers: the shared S buffer may take the next S.
@@ -919,10 +987,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     float m_new = m;
                     bool fresh = false, resc = false;
                     if (member_row) {
-                        if (nj < T) {
+                        // columns past the valid keys (and, with 64-token tiles, a
+                        // whole half whose tile this row does not select) are -inf
+                        const int lim = !member_t ? 0 : (C::KT == T ? nj - hf * TH : nj);
+                        if (lim < TH) {
 #pragma unroll
                             for (int i = 0; i < TH; ++i)
-                                if (hf * TH + i >= nj) s[i] = -INFINITY;
+                                if (i >= lim) s[i] = -INFINITY;
                         }
                         float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
 #pragma unroll
@@ -1039,41 +1110,47 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     if (warp == kSWarp) tmem_dealloc(tmem, C::kTmemCols);
 }
 
+// The dense form (kPaired) runs with the selection bitmaps in shared memory
+// only; beyond kSmemBitmapTiles kernel tiles the split, per-tile form runs.
 template <int T, int D>
 cudaError_t launch_t(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v, AttnParams p, bool paired,
                      int grid, cudaStream_t stream) {
     const int smem_words = p.bm_global ? 0 : p.bm_words;  // bitmap words held in shared memory
-    p.stages = stages_for<T, D>(smem_words);
-    const SmemPlan L = smem_plan<T, D>(smem_words, p.stages);
-    // The paired layout is only chosen for 128-token kernel tiles, and the
-    // workspace bitmaps run in the split layout (both layouts agree bitwise).
-    if (p.bm_global) {
-        attn_fwd_kernel<T, D, false, true><<<grid, kAttnThreads, L.total, stream>>>(q, k, v, p);
-    } else if constexpr (T == 128) {
-        if (paired)
-            attn_fwd_kernel<T, D, true, false><<<grid, kAttnThreads, L.total, stream>>>(q, k, v, p);
+    const bool dense = paired && !p.bm_global;
+    if (dense) {
+        constexpr int KT = key_rows<T, true>();
+        p.stages = stages_for<T, D, KT>(smem_words);
+        const SmemPlan L = smem_plan<T, D, KT>(smem_words, p.stages);
+        attn_fwd_kernel<T, D, true, false><<<grid, kAttnThreads, L.total, stream>>>(q, k, v, p);
+    } else {
+        constexpr int KT = key_rows<T, false>();
+        p.stages = stages_for<T, D, KT>(smem_words);
+        const SmemPlan L = smem_plan<T, D, KT>(smem_words, p.stages);
+        if (p.bm_global)
+            attn_fwd_kernel<T, D, false, true><<<grid, kAttnThreads, L.total, stream>>>(q, k, v, p);
         else
             attn_fwd_kernel<T, D, false, false><<<grid, kAttnThreads, L.total, stream>>>(q, k, v, p);
-    } else {
-        attn_fwd_kernel<T, D, false, false><<<grid, kAttnThreads, L.total, stream>>>(q, k, v, p);
     }
     return cudaGetLastError();
 }
 
 template <int T, int D>
-AttnLaunchInfo info_t(int bm_words) {
-    const int ns = stages_for<T, D>(bm_words);
-    return AttnLaunchInfo{ns, (int)smem_plan<T, D>(bm_words, ns).total};
+AttnLaunchInfo info_t(int bm_words, bool dense) {
+    if (dense) {
+        constexpr int KT = key_rows<T, true>();
+        const int ns = stages_for<T, D, KT>(bm_words);
+        return AttnLaunchInfo{ns, (int)smem_plan<T, D, KT>(bm_words, ns).total};
+    }
+    constexpr int KT = key_rows<T, false>();
+    const int ns = stages_for<T, D, KT>(bm_words);
+    return AttnLaunchInfo{ns, (int)smem_plan<T, D, KT>(bm_words, ns).total};
 }
 
 template <int T, int D>
 cudaError_t prepare_t() {
-    cudaError_t e = cudaSuccess;
-    if constexpr (T == 128) {
-        e = cudaFuncSetAttribute(attn_fwd_kernel<T, D, true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)kSmemLimit);
-        if (e != cudaSuccess) return e;
-    }
+    cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<T, D, true, false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemLimit);
+    if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(attn_fwd_kernel<T, D, false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kSmemLimit);
     if (e != cudaSuccess) return e;
@@ -1083,11 +1160,11 @@ cudaError_t prepare_t() {
 
 }  // namespace
 
-AttnLaunchInfo attn_launch_info(int tile, int head_dim, int bm_words) {
-    if (tile == 128 && head_dim == 128) return info_t<128, 128>(bm_words);
-    if (tile == 128 && head_dim == 64) return info_t<128, 64>(bm_words);
-    if (tile == 64 && head_dim == 128) return info_t<64, 128>(bm_words);
-    return info_t<64, 64>(bm_words);
+AttnLaunchInfo attn_launch_info(int tile, int head_dim, int bm_words, bool dense) {
+    if (tile == 128 && head_dim == 128) return info_t<128, 128>(bm_words, dense);
+    if (tile == 128 && head_dim == 64) return info_t<128, 64>(bm_words, dense);
+    if (tile == 64 && head_dim == 128) return info_t<64, 128>(bm_words, dense);
+    return info_t<64, 64>(bm_words, dense);
 }
 
 cudaError_t attn_prepare(int tile, int head_dim, int) {

@@ -54,17 +54,17 @@ struct AttnLaunchInfo {
 // Ring depth and dynamic shared memory of the attention kernel variant: the
 // deepest K/V ring that fits the 227 KB per-CTA limit next to the Q tiles and
 // the selection bitmaps (bm_words: bitmap words kept in shared memory, 0 when
-// they live in the workspace).
-AttnLaunchInfo attn_launch_info(int tile, int head_dim, int bm_words);
+// they live in the workspace; dense: the dense form, see launch_attn).
+AttnLaunchInfo attn_launch_info(int tile, int head_dim, int bm_words, bool dense);
 
 // Enables the variant's shared-memory size on the current device (once).
 cudaError_t attn_prepare(int tile, int head_dim, int device);
 
 // Launches with p.stages taken from attn_launch_info (the caller's value is
-// ignored).  `paired` picks the MMA-issue role layout (both are exact; they
-// differ only in speed): paired for dense selections at T = D = 128, split
-// otherwise; with 64-token tiles or bitmaps in the workspace it is ignored
-// (split).
+// ignored).  `paired` picks the dense form (all forms are exact; they differ
+// only in speed): with 128-token kernel tiles the paired MMA-issue layout,
+// with 64-token tiles ring entries of key-tile pairs, whose K and V maps then
+// have 128-row boxes.  With bitmaps in the workspace it is ignored.
 cudaError_t launch_attn(int tile, int head_dim, bool paired, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
                         const CUtensorMap &tm_v, AttnParams p, int grid, cudaStream_t stream);
 

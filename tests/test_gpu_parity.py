@@ -161,13 +161,22 @@ def _random_case(seed, B, H, NT, T, D, pad="naninf", empty_frac=0.15, full=False
     return W.Workload("random", B, H, D, T, NT, bs, idx, counts, 1.0 / math.sqrt(D), True, q=q, k=k, v=v)
 
 
-@pytest.mark.parametrize("T,D,NT", [(64, 64, 9), (64, 128, 7), (128, 64, 5), (128, 128, 5), (64, 64, 1),
-                                    (128, 128, 3), (256, 64, 5), (256, 128, 3), (256, 128, 1)])
-def test_variants_ragged(vsa, oracle_mod, T, D, NT):
-    w = _random_case(100 + T + D + NT, 2, 3, NT, T, D)
+@pytest.mark.parametrize("T,D,NT,narrow", [(64, 64, 9, False), (64, 128, 7, False), (128, 64, 5, False),
+                                           (128, 128, 5, False), (64, 64, 1, False), (128, 128, 3, False),
+                                           (256, 64, 5, False), (256, 128, 3, False), (256, 128, 1, False),
+                                           (64, 64, 9, True), (64, 128, 8, True), (128, 128, 5, True)])
+def test_variants_ragged(vsa, oracle_mod, T, D, NT, narrow):
+    """Random selections on ragged tiles with NaN/Inf padding, every element
+    against the oracle.  Rows of q2k_idx hold every key tile (the dense form:
+    key-tile pairs at 64-token tiles, the paired MMA issue at 128) unless
+    `narrow` (one slot short: the split, per-tile form)."""
+    w = _random_case(100 + T + D + NT + (7 if narrow else 0), 2, 3, NT, T, D, max_kv=NT - 1 if narrow else None)
     (q, k, v), refs = _to_tile_major(w, vsa, oracle_mod)
     out, lse = _run(vsa, q, k, v, w)
-    _check(w, out, lse, refs, oracle_mod, list(range(w.B * w.H * w.NT)), f"T{T}D{D}NT{NT}")
+    # 256-token tiles always share one selection per unit pair (the dense form at D = 128)
+    dense_form = (T == 256 and D == 128) or (not narrow and (T == 64 or (T == 128 and D == 128)))
+    assert vsa.vsa_last_route()["layout"] == (vsa.VSA_LAYOUT_PAIRED if dense_form else vsa.VSA_LAYOUT_SPLIT)
+    _check(w, out, lse, refs, oracle_mod, list(range(w.B * w.H * w.NT)), f"T{T}D{D}NT{NT}{' narrow' if narrow else ''}")
     _check_steps(vsa, w)
 
 
@@ -271,13 +280,22 @@ def _pair_case(seed, D, NT=6, ragged=False):
 @pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("where", ["v", "k"])
 @pytest.mark.parametrize("ragged", [False, True])
-def test_t64_pair_isolation(vsa, oracle_mod, D, where, ragged):
+@pytest.mark.parametrize("form", ["tile", "pair"])
+def test_t64_pair_isolation(vsa, oracle_mod, D, where, ragged, form):
     """Two 64-token query tiles share one 128-lane accumulator.  A NaN, +Inf or
     -Inf in a VALID row of a key tile that only one tile of the pair selects
     must reach only that tile's rows, as in the definition (each query tile
     attends to its own list); the partner tile's rows stay finite and match
-    the oracle, and every non-finite element matches the oracle's exactly."""
+    the oracle, and every non-finite element matches the oracle's exactly.
+    Both 64-token forms run: one ring entry per key tile, and (rows of
+    q2k_idx padded to every key tile: the dense form) one per pair of key
+    tiles, where the two query tiles of a unit select different tiles of one
+    pair (query tile 0 key tile 0, query tile 1 key tile 1)."""
     w = _pair_case(900 + D + (1 if ragged else 0), D, ragged=ragged)
+    if form == "pair":
+        wide = torch.full((w.B, w.H, w.NT, w.NT), -1, dtype=torch.int32)
+        wide[..., : w.max_kv] = w.q2k_idx
+        w = dataclasses.replace(w, q2k_idx=wide)
     x = (w.v if where == "v" else w.k).clone()
     # key tiles 0 and 3 are selected by query tiles 0 and 3 only, whose pair
     # partners (1 and 2) select neither; head 0 gets infinities only (a NaN in
@@ -295,13 +313,14 @@ def test_t64_pair_isolation(vsa, oracle_mod, D, where, ragged):
         w.k = x
     (q, k, v), refs = _to_tile_major(w, vsa, oracle_mod)
     out, lse = _run(vsa, q, k, v, w)
+    assert vsa.vsa_last_route()["layout"] == (vsa.VSA_LAYOUT_PAIRED if form == "pair" else vsa.VSA_LAYOUT_SPLIT)
     units = list(range(w.B * w.H * w.NT))
     ref, ref_lse = oracle_mod.block_sparse_attention(refs[0], refs[1], refs[2], w.q2k_idx, w.q2k_num,
                                                      w.block_sizes, w.T, w.scale, units=units)
     g = PT.gather_gpu_units(out, units, w.NT, w.T)
     gl = PT.gather_gpu_lse(lse, units, w.NT, w.T)
     PT.assert_parity_elementwise(g, ref, w.block_sizes.numpy(), units, w.NT, w.T, gl, ref_lse,
-                                 label=f"pairs {where} D{D}{' ragged' if ragged else ''}")
+                                 label=f"pairs {where} D{D}{' ragged' if ragged else ''} {form}")
     # the pair partners of the tiles that meet the planted values stay finite
     for h in range(2):
         for t in (1, 2, 4, 5):
