@@ -121,7 +121,8 @@ struct Cfg {
     // second does not fit next to two O and two P); with 64-token tiles each
     // unit has its own, so one unit's S never waits for the other's to be
     // copied out.
-    static constexpr int kSBufs = (T == 64 && 2 * D + 3 * KT <= 512) ? 2 : 1;
+    // one S buffer per unit whenever two O, two S and two P fit in TMEM
+    static constexpr int kSBufs = (2 * D + 3 * KT <= 512) ? 2 : 1;
     static constexpr uint32_t kTmemO0 = 0, kTmemO1 = D, kTmemS0 = 2 * D, kTmemS1 = 2 * D + (kSBufs - 1) * KT,
                               kTmemP0 = 2 * D + kSBufs * KT, kTmemP1 = 2 * D + kSBufs * KT + KT / 2;
     static constexpr uint32_t kTmemCols = (2 * D + (kSBufs + 1) * KT <= 256) ? 256 : 512;

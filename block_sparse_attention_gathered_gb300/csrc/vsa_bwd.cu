@@ -612,10 +612,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             // as the elementwise step has written it
             for (int i = 0; i < n && ok; ++i) {
                 const int b = i & 1;
+                // the pair's block mask, loaded before the waits so its latency
+                // stays off the chain from the elementwise step to these MMAs
+                const int mk = BM ? (entry(i) & 15) : 15;
                 for (int hv = 0; hv < 2 && ok; ++hv) {
                     if (!(ok = wait_bar(BAR(kBarEw0 + hv), i & 1u, abort_flag, A.status))) break;
                     tc_fence_after();
-                    const int mk = BM ? (entry(i) & 15) : 15;
                     if (KV) {
                         mma_acc_half<D, BM>(tAcc0, slot(hv), base + L::buf(b, 1), hv, i > 0, mk);       // dV += P^T dO_t
                         mma_acc_half<D, BM>(tAcc1, slot(hv) + 64, base + L::buf(b, 0), hv, i > 0, mk);  // dK += dS^T Q_t
