@@ -92,16 +92,22 @@ typedef struct {
     int64_t work_items;   /* 256-query-row work items scheduled */
     int32_t sort_bins;    /* bins of the on-device work ordering */
     int32_t smem_bytes;   /* dynamic shared memory per CTA */
-    int32_t layout;       /* VSA_LAYOUT_*: how the attention kernel's MMA issue is split
-                             over its threads (results are the same either way) */
+    int32_t layout;       /* VSA_LAYOUT_*: the attention kernel's form, sparse or dense
+                             (results agree within the stated tolerance) */
     int32_t reserved;
 } vsa_route;
 
-/* Attention kernel MMA-issue layouts (vsa_route.layout).  PAIRED: one thread
-   per 128-row query unit issues both of its products (dense selections).
-   SPLIT: one thread issues every S = Q K^T, one thread per unit its P V
-   (sparse selections).  Chosen from vsa_dims: PAIRED when head_dim == 128
-   and either tile == 256, or tile == 128 and max_kv >= num_tiles. */
+/* Attention kernel forms (vsa_route.layout).  SPLIT, the sparse form: one
+   thread issues every S = Q K^T, one thread per 128-row query unit its P V,
+   and the K/V ring holds one key tile per entry.  PAIRED, the dense form:
+   with 128-token kernel tiles and head_dim 128, one thread per unit issues
+   both of its products (bit-identical to SPLIT); with 64-token tiles, a ring
+   entry holds a pair of key tiles so S is 128 keys wide (within the stated
+   tolerance of SPLIT: the running maximum advances per entry).  Chosen from
+   vsa_dims: PAIRED when the selection bitmaps fit shared memory
+   (VSA_SMEM_BITMAP_TILES) and either tile == 256 with head_dim == 128, or
+   max_kv >= num_tiles with tile == 64, or with tile == 128 and
+   head_dim == 128. */
 #define VSA_LAYOUT_SPLIT 0
 #define VSA_LAYOUT_PAIRED 1
 
