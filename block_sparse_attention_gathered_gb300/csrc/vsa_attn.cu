@@ -18,21 +18,25 @@
 //     ring is as deep as shared memory allows.
 //   * S_u = Q_u K_j^T (tcgen05, smem x smem -> TMEM) for the key tiles unit u
 //     selects, and O_u += P_u V_j with P read from TMEM, are issued in one of
-//     two layouts (a template parameter; the host picks it from the
-//     selection width).  One thread issues back-to-back MMAs at the pipe's
-//     rate (measured: 64 cycles an M128 N128 K16 MMA; an M128 N64 K16 S
-//     product takes 48, the time its 6 KB of shared-memory operands take at
-//     128 bytes a clock); the layouts differ in which waits sit between the
-//     MMAs of one thread:
-//       - paired (dense selections): one thread per unit issues both of its
-//         products, the next S before the current P V, which keeps P V out of
-//         the way of the S hand-off between the units;
-//       - split (sparse selections, where a key tile mostly serves one unit):
-//         one thread issues every S, and one thread per unit its P V as soon
-//         as P is stored, so S and P V issue overlap.
-//   * TMEM holds O of both units, ONE S buffer the units take turns on (a
-//     shared-memory counter tells an issuer when every earlier S has been
-//     copied out), and P of each unit as bf16 pairs.
+//     two forms (a template parameter; the host picks it from the selection
+//     width).  One thread issues back-to-back MMAs at the pipe's rate
+//     (measured: 64 cycles an M128 N128 K16 MMA; an M128 N64 K16 S product
+//     takes 48, the time its 6 KB of shared-memory operands take at 128 bytes
+//     a clock); the issue layouts differ in which waits sit between the MMAs
+//     of one thread:
+//       - dense form (rows that can hold every key tile): with 128-token
+//         tiles one thread per unit issues both of its products, the next S
+//         before the current P V, which keeps P V out of the way of the S
+//         hand-off between the units ("paired" issue); with 64-token tiles a
+//         ring entry holds a pair of key tiles, so S is 128 keys wide;
+//       - sparse form (where a key tile mostly serves one unit): one thread
+//         issues every S, and one thread per unit its P V as soon as P is
+//         stored, so S and P V issue overlap ("split" issue), one key tile per
+//         ring entry.
+//   * TMEM holds O of both units, the S buffer (one per unit where it fits,
+//     else ONE the units take turns on; a shared-memory counter tells an
+//     issuer when every earlier S has been copied out), and P of each unit as
+//     bf16 pairs.
 //   * Eight softmax warps per unit, two threads per query row in the same
 //     warp (the .16x32bx2 TMEM shape: thread t holds row t%16 of the warp's
 //     16 lanes and one half of its columns).  The row maximum and the final
@@ -49,6 +53,8 @@
 //     accumulator; a P V with a key tile only one of them selects disables
 //     the other's 64 output lanes, so each tile's O holds its own key tiles
 //     only (O is zeroed at the start of an item and every P V accumulates).
+//     In the dense form each thread half of a row holds one key tile of the
+//     entry's pair, masked whole when its query tile does not select it.
 //   * The producer counts the (query tile, key tile) steps it hands out,
 //     tail and full, into a device word the host reads for route checks.
 //   * 20 warps: four softmax warpgroups, then a control warpgroup (three

@@ -145,6 +145,27 @@ def test_dense_limit_sampled(vsa, oracle_mod):
     assert r["grid"] == min(6 * 122, torch.cuda.get_device_properties(0).multi_processor_count)
 
 
+@pytest.mark.parametrize("D", [128, 64])
+def test_dense_t64_sampled(vsa, oracle_mod, D):
+    """The dense workload at 64-token tiles, full size, in the bench's launch
+    configuration: the dense form (key-tile pairs).  96 of the 2928 query
+    tiles against the oracle, the 32-token tail tile of every head among
+    them, and properties over the whole output."""
+    w = W.make_workload(5, tile=64, head_dim=D)
+    (q, k, v), refs = _to_tile_major(w, vsa, oracle_mod)
+    out, lse = _run(vsa, q, k, v, w)
+    r = vsa.vsa_last_route()
+    assert (r["tile"], r["head_dim"], r["layout"]) == (64, D, vsa.VSA_LAYOUT_PAIRED)
+    last = w.NT - 1
+    must = [h * w.NT + last for h in range(w.H)] + [0, 1]
+    units = PT.sample_units(w.B, w.H, w.NT, 96, seed=7 + D, must=must)
+    _check(w, out, lse, refs, oracle_mod, units, f"dense T64 D{D}")
+    assert torch.isfinite(out[:, :, :31200].float()).all()
+    assert (out[:, :, 31200:].view(torch.int16) == 0).all()
+    # one masked step per query tile (the 32-token tail key tile), 487 full ones
+    assert _check_steps(vsa, w) == (6 * 488, 6 * 488 * 487)
+
+
 def _random_case(seed, B, H, NT, T, D, pad="naninf", empty_frac=0.15, full=False, max_kv=None):
     g = torch.Generator().manual_seed(seed)
     max_kv = NT if max_kv is None else max_kv
