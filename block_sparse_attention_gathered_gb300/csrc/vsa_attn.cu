@@ -85,7 +85,7 @@ constexpr int kPvWarp0 = 17;
 constexpr int kProducerWarp = 18;
 constexpr int kPvWarp1 = 19;
 constexpr int kIssuers = 3;        // split layout: a ring fill is released by three arrivals
-constexpr int kPairedIssuers = 2;  // paired layout: by two
+constexpr int kPairedIssuers = 2;  // paired layout: by two, and the tail-V zeroing warp
 constexpr int kMaxStages = 8;
 // Register split (control warpgroup, four softmax warpgroups); the sum stays
 // within the 640 x 96 registers the CTA is launched with.
@@ -288,7 +288,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < NS; ++s) {
             mbar_init(BAR(BI.kv_full(s)), 1);
-            mbar_init(BAR(BI.kv_empty(s)), kIssuePaired ? kPairedIssuers : kIssuers);  // arrivals per fill
+            // releases per fill: paired, both issuers and the warp that zeroes
+            // tail V rows; split, three by the issuers
+            mbar_init(BAR(BI.kv_empty(s)), kIssuePaired ? kPairedIssuers + 1 : kIssuers);
             mbar_init(BAR(BI.vz(s)), 32);
         }
         #pragma unroll
@@ -507,23 +509,26 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     ring.next(NS);
                     const uint32_t vst = ring.st, vph = ring.ph;
                     ring.next(NS);
-                    // Wait for every fill in order, like the MMA issuers: a parity
-                    // wait is only meaningful when the waiter is never a whole ring
-                    // cycle ahead of the fills it waits for.
+                    // Wait for every fill in order and give each its third
+                    // release, so no stage is refilled before this warp has seen
+                    // its current fill: every parity wait here refers to the fill
+                    // meant.
                     if (!(ok = wait_warp(BAR(BI.kv_full(kst)), kph, abort_flag, P.status))) break;
+                    if (lane == 0) mbar_arrive(BAR(BI.kv_empty(kst)));
                     if (!(ok = wait_warp(BAR(BI.kv_full(vst)), vph, abort_flag, P.status))) break;
-                    if (!((part_w >> b) & 1u)) continue;
-                    const int nj = tile_size(P.block_sizes, j, P.sub);
-                    if ((nj & 15) == 0) continue;
-                    uint4 *vs = reinterpret_cast<uint4 *>(gbase + L.ring + vst * C::kStageBytes);
-                    const int n16 = (16 - (nj & 15)) * 8;
+                    const int nj = ((part_w >> b) & 1u) ? tile_size(P.block_sizes, j, P.sub) : T;
+                    if ((nj & 15) != 0) {
+                        uint4 *vs = reinterpret_cast<uint4 *>(gbase + L.ring + vst * C::kStageBytes);
+                        const int n16 = (16 - (nj & 15)) * 8;
 #pragma unroll
-                    for (int c = 0; c < C::kChunks; ++c)
-                        for (int i = lane; i < n16; i += 32)
-                            vs[(c * C::kKVChunk + nj * 128) / 16 + i] = make_uint4(0u, 0u, 0u, 0u);
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    mbar_arrive(BAR(BI.vz(vst)));
+                        for (int c = 0; c < C::kChunks; ++c)
+                            for (int i = lane; i < n16; i += 32)
+                                vs[(c * C::kKVChunk + nj * 128) / 16 + i] = make_uint4(0u, 0u, 0u, 0u);
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        mbar_arrive(BAR(BI.vz(vst)));
+                    }
+                    if (lane == 0) mbar_arrive(BAR(BI.kv_empty(vst)));
                 }
             }
             if (!ok) break;
