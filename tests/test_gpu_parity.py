@@ -212,17 +212,26 @@ def test_many_waves(vsa, oracle_mod):
 
 
 @pytest.mark.parametrize("T", [64, 128, 256])
-def test_split_last_wave(vsa, oracle_mod, T):
+@pytest.mark.parametrize("form", ["sparse", "dense"])
+def test_split_last_wave(vsa, oracle_mod, T, form):
     """One work item per SM plus a few: the last wave's items run as one-unit
-    items on two CTAs each, and each CTA writes only its unit's rows."""
+    items on two CTAs each, and each CTA writes only its unit's rows.  Both
+    forms: short rows of q2k_idx (sparse) and rows that hold every key tile
+    at D = 128 (dense: the paired MMA issue at 128- and 256-token tiles,
+    key-tile pairs at 64)."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     n_items = sms + 5
     NT = n_items * 256 // T
-    w = _random_case(300 + T, 1, 1, NT, T, 64, max_kv=3)
+    if form == "sparse":
+        w = _random_case(300 + T, 1, 1, NT, T, 64, max_kv=3)
+    else:
+        w = _random_case(310 + T, 1, 1, NT, T, 128)
     (q, k, v), refs = _to_tile_major(w, vsa, oracle_mod)
     out, lse = _run(vsa, q, k, v, w)
-    assert vsa.vsa_last_route()["work_items"] == n_items
-    _check(w, out, lse, refs, oracle_mod, list(range(w.B * w.H * w.NT)), f"split T{T}")
+    r = vsa.vsa_last_route()
+    assert r["work_items"] == n_items
+    assert r["layout"] == (vsa.VSA_LAYOUT_PAIRED if form == "dense" else vsa.VSA_LAYOUT_SPLIT)
+    _check(w, out, lse, refs, oracle_mod, list(range(w.B * w.H * w.NT)), f"split T{T} {form}")
     _check_steps(vsa, w)   # split items count their unit once, on the CTA that runs it
     # bit-identical across runs, although which items are split may differ
     # (items of equal length take their places in any order)
