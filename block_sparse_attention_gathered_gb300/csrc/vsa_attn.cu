@@ -571,13 +571,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 tc_fence_after();
                 bool pending = false, first = true;
                 uint32_t pend_v = 0, pend_ph = 0;
-                uint32_t pend_lo = 0, pend_hi = 0;  // output lanes the pending P V leaves out (T == 64)
                 int pend_kb = 0;
                 bool pend_tail = false;
                 uint32_t seen = 0;
 
-                // O_u += P_u V of the pending entry (P from shared memory), then
-                // this issuer's release of that V stage.
+                // O_u += P_u V of the pending entry (P from TMEM), then this
+                // issuer's release of that V stage.  (This issue layout runs
+                // with 128-token tiles only.)
                 auto pv = [&]() -> bool {
                     if (!wait_bar(BAR(pend_tail ? BI.vz(pend_v) : BI.kv_full(pend_v)), pend_ph, abort_flag, P.status))
                         return false;
@@ -585,17 +585,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     ++pcnt;
                     tc_fence_after();
                     const uint64_t b = dv + pend_v * kStage16;
-                    if constexpr (T == 64) {
+                    mma_ts(tO, tP, b, C::kIdescPV, first ? 0u : 1u);
 #pragma unroll
-                        for (int kk = 0; kk < T / 16; ++kk)
-                            if (kk < pend_kb)
-                                mma_ts_lanes(tO, tP + kk * 8, b + kk * 128, C::kIdescPV, 1u, pend_lo, pend_hi);
-                    } else {
-                        mma_ts(tO, tP, b, C::kIdescPV, first ? 0u : 1u);
-#pragma unroll
-                        for (int kk = 1; kk < T / 16; ++kk)
-                            if (kk < pend_kb) mma_ts(tO, tP + kk * 8, b + kk * 128, C::kIdescPV, 1u);
-                    }
+                    for (int kk = 1; kk < T / 16; ++kk)
+                        if (kk < pend_kb) mma_ts(tO, tP + kk * 8, b + kk * 128, C::kIdescPV, 1u);
                     mma_commit(BAR(BI.o_done(u)));
                     mma_commit(BAR(BI.kv_empty(pend_v)));
                     first = false;
@@ -652,10 +645,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                             pend_ph = tail ? vzp : vph;
                             pend_kb = (nj + 15) >> 4;
                             pend_tail = tail;
-                            if constexpr (T == 64) {
-                                pend_lo = ((pa[w] >> b) & 1u) ? 0u : ~0u;
-                                pend_hi = ((pb[w] >> b) & 1u) ? 0u : ~0u;
-                            }
                         } else {
                             // not selected by this unit: issue the pending P V (it
                             // frees a V stage), then release both stages of the entry
