@@ -908,6 +908,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         // The row maximum and the final row sum combine the halves with one
         // shuffle.
         constexpr int TH = C::KT / 2;  // S columns per thread
+        // Split form at 128-token tiles: P goes to registers before the wait for
+        // the unit's previous P V, so the exponentials overlap that product.
+        // (The paired form spills with it; 64-token tiles measured slower.)
+        constexpr bool kEarlyP = !kPaired && T == 128;
         constexpr int DH = D / 2;   // O columns per thread
         const int u = warp >> 3;
         const int sb = (warp >> 2) & 1;
@@ -1010,49 +1014,98 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         fresh = (m == -INFINITY);
                         resc = !fresh && (m_new > m + kRescaleThreshold);
                     }
-                    // The previous P V of this unit must be done: it reads the P
-                    // columns about to be overwritten and accumulates into O.
-                    if (n_mine > 0) {
-                        if (!(ok = wait_warp(BAR(BI.o_done(u)), (cnt - 1u) & 1u, abort_flag, P.status))) break;
-                        tc_fence_after();
-                    }
-                    if (__any_sync(0xffffffffu, resc)) {
-                        const float alpha = resc ? ex2(m - m_new) : 1.f;
-                        // 8 columns at a time: S is still held in registers here
-#pragma unroll
-                        for (int ch = 0; ch < DH / 8; ++ch) {
-                            float o[8];
-                            tmem_ld2x_8<DH>(tO + ch * 8, o);
-#pragma unroll
-                            for (int i = 0; i < 8; ++i) o[i] *= alpha;
-                            tmem_st2x_8f<DH>(tO + ch * 8, o);
-                        }
-                        l0 *= alpha;
-                        l1 *= alpha;
-                    }
-                    if (fresh || resc) m = m_new;
-                    const float neg_m = -m;
                     // this tile's part of l in 4 independent sums
                     float lq[4] = {0.f, 0.f, 0.f, 0.f};
+                    if constexpr (kEarlyP) {
+                        // O's rescale factor, from the old maximum
+                        const bool any_resc = __any_sync(0xffffffffu, resc);
+                        const float alpha = resc ? ex2(m - m_new) : 1.f;
+                        if (fresh || resc) m = m_new;
+                        const float neg_m = -m;
+                        // P of this tile into registers while the previous P V of the
+                        // unit may still run
+                        uint32_t pk[TH / 2];
 #pragma unroll
-                    for (int cc = 0; cc < TH / 16; ++cc) {
-                        uint32_t pk[8];
-                        if (member_row) {
-#pragma unroll
-                            for (int i = 0; i < 8; ++i) {
+                        for (int i = 0; i < TH / 2; ++i) {
+                            if (member_row) {
                                 float x0, x1;
-                                fma2_scalar(x0, x1, s[cc * 16 + 2 * i], s[cc * 16 + 2 * i + 1], c, neg_m);
+                                fma2_scalar(x0, x1, s[2 * i], s[2 * i + 1], c, neg_m);
                                 pk[i] = pack_bf16x2(ex2(x0), ex2(x1));
                                 // l sums the bf16 values P V actually uses, so the
                                 // weights P / l stay exactly normalised.
                                 add_bf16x2_f32(lq[2 * (i & 1)], lq[2 * (i & 1) + 1], pk[i]);
+                            } else {
+                                pk[i] = 0u;  // this tile of the unit does not select tile j: zero P rows
                             }
-                        } else {
-                            // this tile of the unit does not select tile j: zero P rows
-#pragma unroll
-                            for (int i = 0; i < 8; ++i) pk[i] = 0u;
                         }
-                        tmem_st2x_8<TH / 2>(tP + cc * 8, pk);
+                        // The previous P V of this unit must be done before P is
+                        // overwritten and O rescaled.
+                        if (n_mine > 0) {
+                            if (!(ok = wait_warp(BAR(BI.o_done(u)), (cnt - 1u) & 1u, abort_flag, P.status))) break;
+                            tc_fence_after();
+                        }
+                        if (any_resc) {
+#pragma unroll
+                            for (int ch = 0; ch < DH / 8; ++ch) {
+                                float o[8];
+                                tmem_ld2x_8<DH>(tO + ch * 8, o);
+#pragma unroll
+                                for (int i = 0; i < 8; ++i) o[i] *= alpha;
+                                tmem_st2x_8f<DH>(tO + ch * 8, o);
+                            }
+                            l0 *= alpha;
+                            l1 *= alpha;
+                        }
+#pragma unroll
+                        for (int cc = 0; cc < TH / 16; ++cc) {
+                            uint32_t pc[8];
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) pc[i] = pk[cc * 8 + i];
+                            tmem_st2x_8<TH / 2>(tP + cc * 8, pc);
+                        }
+                    } else {
+                        // The previous P V of this unit must be done: it reads the P
+                        // columns about to be overwritten and accumulates into O.
+                        if (n_mine > 0) {
+                            if (!(ok = wait_warp(BAR(BI.o_done(u)), (cnt - 1u) & 1u, abort_flag, P.status))) break;
+                            tc_fence_after();
+                        }
+                        if (__any_sync(0xffffffffu, resc)) {
+                            const float alpha = resc ? ex2(m - m_new) : 1.f;
+                            // 8 columns at a time: S is still held in registers here
+#pragma unroll
+                            for (int ch = 0; ch < DH / 8; ++ch) {
+                                float o[8];
+                                tmem_ld2x_8<DH>(tO + ch * 8, o);
+#pragma unroll
+                                for (int i = 0; i < 8; ++i) o[i] *= alpha;
+                                tmem_st2x_8f<DH>(tO + ch * 8, o);
+                            }
+                            l0 *= alpha;
+                            l1 *= alpha;
+                        }
+                        if (fresh || resc) m = m_new;
+                        const float neg_m = -m;
+#pragma unroll
+                        for (int cc = 0; cc < TH / 16; ++cc) {
+                            uint32_t pk[8];
+                            if (member_row) {
+#pragma unroll
+                                for (int i = 0; i < 8; ++i) {
+                                    float x0, x1;
+                                    fma2_scalar(x0, x1, s[cc * 16 + 2 * i], s[cc * 16 + 2 * i + 1], c, neg_m);
+                                    pk[i] = pack_bf16x2(ex2(x0), ex2(x1));
+                                    // l sums the bf16 values P V actually uses, so the
+                                    // weights P / l stay exactly normalised.
+                                    add_bf16x2_f32(lq[2 * (i & 1)], lq[2 * (i & 1) + 1], pk[i]);
+                                }
+                            } else {
+                                // this tile of the unit does not select tile j: zero P rows
+#pragma unroll
+                                for (int i = 0; i < 8; ++i) pk[i] = 0u;
+                            }
+                            tmem_st2x_8<TH / 2>(tP + cc * 8, pk);
+                        }
                     }
                     l0 += lq[0] + lq[2];
                     l1 += lq[1] + lq[3];
