@@ -201,6 +201,71 @@ def test_variants_ragged(vsa, oracle_mod, T, D, NT, narrow):
     _check_steps(vsa, w)
 
 
+def _rescale_events(q, k, w):
+    """Rows (over valid query rows) whose running maximum, taken over the
+    selected key tiles in ascending order, grows by more than 2^8 after the
+    first tile: the rows that take the softmax's lazy rescale of O.  Plain
+    float64 over the valid keys of each tile."""
+    B, H, Sp, D = q.shape
+    T, NT = w.T, w.NT
+    bs = w.block_sizes.numpy()
+    c = w.scale / math.log(2.0)
+    qd, kd = q.double().numpy(), k.double().numpy()
+    events = []
+    for b in range(B):
+        for h in range(H):
+            for t in range(NT):
+                n = int(w.q2k_num[b, h, t])
+                if bs[t] == 0 or n == 0:
+                    continue
+                qt = qd[b, h, t * T:t * T + bs[t]]
+                m = np.full(qt.shape[0], -np.inf)
+                ev = np.zeros(qt.shape[0], dtype=int)
+                for j in sorted(int(x) for x in w.q2k_idx[b, h, t, :n]):
+                    if bs[j] == 0:
+                        continue
+                    mx = (qt @ kd[b, h, j * T:j * T + bs[j]].T).max(axis=1) * c
+                    ev += (np.isfinite(m) & (mx > m + 8.0)).astype(int)
+                    m = np.maximum(m, mx)
+                events.append(ev)
+    return np.concatenate(events)
+
+
+@pytest.mark.parametrize("T,D,narrow", [(128, 128, True), (128, 128, False), (128, 64, True),
+                                        (64, 128, True), (64, 128, False), (64, 64, True)])
+def test_growing_max_rescales_o(vsa, oracle_mod, T, D, narrow):
+    """Scores that climb from key tile to key tile, at a rate drawn per query
+    row (some rows climb fast, so their running maximum grows by more than
+    2^8 several times and the softmax rescales O; some climb slowly and never
+    rescale; some fall, so the first tile keeps the maximum), on ragged tiles
+    with NaN/Inf padding.  Every element against the oracle, in the sparse
+    (split) and dense (paired issue, key-tile pairs) forms."""
+    NT = 8 if T == 128 else 12
+    B, H, Sp = 1, 4, NT * T
+    w = _random_case(500 + T + D + int(narrow), B, H, NT, T, D, max_kv=NT - 1 if narrow else None)
+    g = torch.Generator().manual_seed(900 + T + D)
+    # per query row: half climb fast, a quarter stay flat, a quarter fall
+    kind = torch.rand((B, H, Sp, 1), generator=g)
+    mag = torch.rand((B, H, Sp, 1), generator=g)
+    rate = torch.where(kind < 0.5, 4.0 + 4.0 * mag, torch.where(kind < 0.75, 2.0 * mag - 1.0, -4.0 - 4.0 * mag))
+    step = 8.0 if T == 128 else 6.0                                  # per key tile
+    ramp = (torch.arange(NT).repeat_interleave(T).float() * step)[None, None, :, None]
+    q = 0.5 * torch.randn((B, H, Sp, D), generator=g)
+    k = 0.5 * torch.randn((B, H, Sp, D), generator=g)
+    q[..., :1] += rate
+    k[..., :1] += ramp
+    q, k = (W.pad_tile_major(x.to(torch.bfloat16), w.block_sizes, T, "naninf") for x in (q, k))
+    w = dataclasses.replace(w, q=q, k=k)
+    ev = _rescale_events(q, k, w)
+    assert (ev >= 1).mean() > 0.2 and (ev >= 2).sum() > 50 and (ev == 0).mean() > 0.2, "the input must rescale O"
+    (qg, kg, vg), refs = _to_tile_major(w, vsa, oracle_mod)
+    out, lse = _run(vsa, qg, kg, vg, w)
+    dense_form = not narrow and (T == 64 or D == 128)
+    assert vsa.vsa_last_route()["layout"] == (vsa.VSA_LAYOUT_PAIRED if dense_form else vsa.VSA_LAYOUT_SPLIT)
+    _check(w, out, lse, refs, oracle_mod, list(range(w.B * w.H * w.NT)),
+           f"rescale T{T}D{D}{' narrow' if narrow else ''}")
+
+
 def test_many_waves(vsa, oracle_mod):
     """More work items than SMs: every CTA takes several items."""
     w = _random_case(7, 4, 48, 6, 128, 64, full=True)
