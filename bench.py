@@ -50,9 +50,9 @@ FALLBACK_HBM_GBS = 6800.0
 # hash of the attention kernel code the capture was taken with
 # (_attn_source_hash); a changed kernel reports null until it is captured again.
 ATTN_TRAFFIC = {
-    ("dense_b1h6d128_s31200_t128x244_lse", "2c78e5f3b9a2e942"): 353.67e6,  # 318.3 MB read + 35.3 MB written
-    ("uniform_b1h12d128_t128x128_k32", "2c78e5f3b9a2e942"): 196.57e6,      # 166.1 MB read + 30.4 MB written
-    ("dense_b1h6d128_s31200_t64x488_lse", "2c78e5f3b9a2e942"): 328.78e6,   # 289.3 MB read + 39.5 MB written
+    ("dense_b1h6d128_s31200_t128x244_lse", "b9d1febbcbcf269c"): 346.80e6,  # 313.4 MB read + 33.4 MB written
+    ("uniform_b1h12d128_t128x128_k32", "b9d1febbcbcf269c"): 251.08e6,      # 216.0 MB read + 35.0 MB written
+    ("dense_b1h6d128_s31200_t64x488_lse", "b9d1febbcbcf269c"): 328.78e6,   # 289.3 MB read + 39.5 MB written
     # (the T64 figure was captured at 3f9b1e775c8ba3b3; the paired form's code is unchanged since)
 }
 

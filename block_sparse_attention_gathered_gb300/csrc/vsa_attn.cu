@@ -908,10 +908,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         // The row maximum and the final row sum combine the halves with one
         // shuffle.
         constexpr int TH = C::KT / 2;  // S columns per thread
-        // Split form at 128-token tiles: P goes to registers before the wait for
-        // the unit's previous P V, so the exponentials overlap that product.
-        // (The paired form spills with it; 64-token tiles measured slower.)
-        constexpr bool kEarlyP = !kPaired && T == 128;
+        // 128-token tiles: P goes to registers before the wait for the unit's
+        // previous P V, so the exponentials overlap that product.  (64-token
+        // tiles measured slower that way.)
+        constexpr bool kEarlyP = T == 128;
         constexpr int DH = D / 2;   // O columns per thread
         const int u = warp >> 3;
         const int sb = (warp >> 2) & 1;
@@ -972,12 +972,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     if (!(ok = wait_warp(BAR(BI.s_full(u)), cnt & 1u, abort_flag, P.status))) break;
                     tc_fence_after();
                     // warp-uniform: does this warp's query tile take part in the
-                    // entry?  With 128-token tiles every entry of the unit is
-                    // its own; stating it at compile time measured 12-15 % faster
-                    // on sparse selections (split layout) and 1 % slower on dense
-                    // ones (paired), so the paired form keeps the test.
-                    const bool member_row =
-                        (T == 128 && !kIssuePaired) || ((entry_bits<T, C::KT>(mine) >> b) & 1u) != 0u;
+                    // entry?  With 128-token tiles every entry of the unit is its
+                    // own, stated at compile time (which also keeps the early P
+                    // free of spills).
+                    const bool member_row = (T == 128) || ((entry_bits<T, C::KT>(mine) >> b) & 1u) != 0u;
                     // per thread with 64-token tiles: does it select this half's tile?
                     const bool member_t = (C::KT == T) || ((mine >> (jt & 31)) & 1u) != 0u;
                     float s[TH];
