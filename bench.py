@@ -50,10 +50,8 @@ FALLBACK_HBM_GBS = 6800.0
 # hash of the attention kernel code the capture was taken with
 # (_attn_source_hash); a changed kernel reports null until it is captured again.
 ATTN_TRAFFIC = {
-    ("dense_b1h6d128_s31200_t128x244_lse", "b9d1febbcbcf269c"): 346.80e6,  # 313.4 MB read + 33.4 MB written
-    ("uniform_b1h12d128_t128x128_k32", "b9d1febbcbcf269c"): 251.08e6,      # 216.0 MB read + 35.0 MB written
-    ("dense_b1h6d128_s31200_t64x488_lse", "b9d1febbcbcf269c"): 328.78e6,   # 289.3 MB read + 39.5 MB written
-    # (the T64 figure was captured at 3f9b1e775c8ba3b3; the paired form's code is unchanged since)
+    ("dense_b1h6d128_s31200_t128x244_lse", "89a00684306c1328"): 254.28e6,  # 220.6 MB read + 33.7 MB written
+    ("uniform_b1h12d128_t128x128_k32", "89a00684306c1328"): 207.98e6,      # 173.5 MB read + 34.5 MB written
 }
 
 # Workloads timed after the headline step in the default run (attention, and
@@ -557,8 +555,10 @@ def run_ours(args, cfg):
                                    f"{'paired' if route.get('layout') == vsa.VSA_LAYOUT_PAIRED else 'split'}>"},
             "e2e": {"value": aggregate(eff, world, e2e_ms), "unit": UNIT, "ms_per_step": e2e_ms,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            # per step: [tile layout,] [tile pooling, selection,] work-ordering sort, attention, [un-tiling]
-            "gpu_launches": ((1 if token else 0) + 2 + (2 if select else 0) + (1 if untile else 0)) * args.steps,
+            # per step: [tile layout,] [tile pooling, selection,] work-ordering sort, attention,
+            # [split-tail merge,] [un-tiling]
+            "gpu_launches": ((1 if token else 0) + 2 + (2 if select else 0) + (1 if route.get("tail_parts", 0) > 1 else 0)
+                             + (1 if untile else 0)) * args.steps,
             "clocks": clk.summary(),
             "route": route,
             "steps_tail_full": steps_tail_full,

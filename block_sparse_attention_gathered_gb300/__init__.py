@@ -40,7 +40,7 @@ class VsaRoute(ctypes.Structure):
     _fields_ = [("kernel", ctypes.c_int32), ("tile", ctypes.c_int32), ("head_dim", ctypes.c_int32),
                 ("grid", ctypes.c_int32), ("block", ctypes.c_int32), ("stages", ctypes.c_int32),
                 ("work_items", ctypes.c_int64), ("sort_bins", ctypes.c_int32),
-                ("smem_bytes", ctypes.c_int32), ("layout", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("smem_bytes", ctypes.c_int32), ("layout", ctypes.c_int32), ("tail_parts", ctypes.c_int32)]
 
     def as_dict(self):
         return {k: getattr(self, k) for k, _ in self._fields_}
@@ -61,6 +61,7 @@ def _load() -> ctypes.CDLL:
     dims_p = ctypes.POINTER(VsaDims)
     sig = {
         "vsa_block_sparse_workspace_size": ([dims_p], sz),
+        "vsa_block_sparse_workspace_size_min": ([dims_p], sz),
         "vsa_block_sparse_fwd": ([P, P, P, P, P, P, P, P, dims_p, P, sz, P], i32),
         "vsa_block_sparse_fwd_noalloc": ([P, P, P, P, P, P, P, P, dims_p, P], i32),
         "vsa_tile_layout": ([P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, P], i32),
@@ -84,7 +85,7 @@ def _load() -> ctypes.CDLL:
 
 
 _lib = _load()
-EXPORTED = ("vsa_block_sparse_workspace_size", "vsa_block_sparse_fwd", "vsa_block_sparse_fwd_noalloc",
+EXPORTED = ("vsa_block_sparse_workspace_size", "vsa_block_sparse_workspace_size_min", "vsa_block_sparse_fwd", "vsa_block_sparse_fwd_noalloc",
             "vsa_block_sparse_bwd_workspace_size", "vsa_block_sparse_bwd", "vsa_tile_layout", "vsa_untile",
             "vsa_coarse_select_workspace_size", "vsa_coarse_select", "vsa_validate_indices",
             "vsa_check_device_status", "vsa_wait_probe", "vsa_last_route", "vsa_last_step_counts",
@@ -126,6 +127,10 @@ def vsa_wait_probe(arrive: bool, limit_us: int, stream=None) -> int:
 
 def vsa_block_sparse_workspace_size(dims: VsaDims) -> int:
     return int(_lib.vsa_block_sparse_workspace_size(ctypes.byref(dims)))
+
+
+def vsa_block_sparse_workspace_size_min(dims: VsaDims) -> int:
+    return int(_lib.vsa_block_sparse_workspace_size_min(ctypes.byref(dims)))
 
 
 def vsa_block_sparse_fwd(q, k, v, q2k_idx, q2k_num, block_sizes, out, lse, dims: VsaDims,

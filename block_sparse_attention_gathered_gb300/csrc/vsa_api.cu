@@ -162,10 +162,13 @@ int64_t items_per_seq(const vsa_dims *d) { return ((int64_t)d->num_tiles * d->ti
 
 constexpr size_t kWsHeader = 256;  // work counter, padded
 
-// Work items of the last, partly filled wave may run as two one-unit items
-// on two CTAs (at most kMaxSplit of them): the order list grows by one entry
-// per split item.
-constexpr int kMaxSplit = 256;
+// Work items of the last, partly filled wave may run as one-unit entries on
+// several CTAs (at most kMaxSplit entries in all, kMaxSplit and kMaxParts in
+// vsa_internal.h): the order list grows by at most kMaxSplit entries.
+// Beyond kTailMinItems work items (where a last wave can be partly filled on
+// this part, 148 SMs or more) the workspace also holds the split tail's
+// partial results.
+constexpr int64_t kTailMinItems = 128;
 
 // Dims the backward and the coarse selection accept: check_dims plus their
 // tighter tile limit.
@@ -190,11 +193,28 @@ size_t bitmap_bytes_per_cta(const vsa_dims *d) {
     return (size_t)2 * kItemBitmaps * bitmap_words(d) * sizeof(uint32_t);
 }
 
-size_t workspace_bytes_for(const vsa_dims *d) {
+// The least workspace the forward accepts: header, order list and (beyond
+// kSmemBitmapTiles kernel tiles) the bitmaps.
+size_t base_bytes_for(const vsa_dims *d) {
     if (!bitmaps_in_workspace(d)) return order_bytes_for(d);
     const int64_t n_items = (int64_t)d->B * d->H * items_per_seq(d);
     const int64_t ctas = n_items < kMaxGridCtas ? n_items : kMaxGridCtas;
     return bitmap_offset_for(d) + (size_t)ctas * bitmap_bytes_per_cta(d);
+}
+// Split-tail region, 256-byte aligned after the base: the work item of each
+// split tail item (kMaxSplit slots), then kMaxSplit pieces of (row maximum,
+// row sum) per unit row, then kMaxSplit pieces of unnormalised O rows (fp32).
+size_t tail_offset_for(const vsa_dims *d) { return (base_bytes_for(d) + 255) & ~(size_t)255; }
+constexpr size_t kTailCntBytes = (size_t)kMaxSplit * sizeof(int32_t);
+constexpr size_t kTailMlBytes = (size_t)kMaxSplit * kUnitRows * 2 * sizeof(float);
+size_t tail_bytes_for(const vsa_dims *d) {
+    const int64_t n_items = (int64_t)d->B * d->H * items_per_seq(d);
+    if (n_items <= kTailMinItems) return 0;
+    return kTailCntBytes + kTailMlBytes + (size_t)kMaxSplit * kUnitRows * d->head_dim * sizeof(float);
+}
+size_t workspace_bytes_for(const vsa_dims *d) {
+    const size_t tail = tail_bytes_for(d);
+    return tail ? tail_offset_for(d) + tail : base_bytes_for(d);
 }
 
 vsa_status encode_rows_map(CUtensorMap *m, const void *ptr, int64_t rows, int D, int box_rows) {
@@ -214,13 +234,17 @@ vsa_status encode_rows_map(CUtensorMap *m, const void *ptr, int64_t rows, int D,
 // Orders the 256-row work items by their total number of selected key tiles,
 // largest first (a counting sort into `bins` buckets), and resets the work
 // counter the attention kernel's CTAs draw from.  One CTA; equal keys land in
-// any order, which does not change any output (items are independent).
+// any order, which does not change any output (items are independent, and a
+// one-unit entry computes its unit exactly as the whole item does).  Items cut
+// into key ranges (parts > 1) do round differently, so those are not taken
+// from the sorted order but are always the last `split` items by index, which
+// keeps every output bit-identical from call to call.
 constexpr int kSchedThreads = 1024;
 
 __global__ void __launch_bounds__(kSchedThreads)
     schedule_kernel(const int32_t *__restrict__ q2k_num, int NT, int T, int max_kv, int G, int n_items, int bins,
-                    int split, int32_t *__restrict__ order, int32_t *__restrict__ counter,
-                    unsigned long long *__restrict__ steps) {
+                    int split, int parts, int32_t *__restrict__ order, int32_t *__restrict__ counter,
+                    int32_t *__restrict__ tail_items, unsigned long long *__restrict__ steps) {
     extern __shared__ int32_t sh[];
     int32_t *hist = sh;          // [bins], indexed by descending rank
     int32_t *cursor = sh + bins;  // [bins]
@@ -243,7 +267,9 @@ __global__ void __launch_bounds__(kSchedThreads)
         const int bin = (int)(w * (bins - 1) / wmax);
         return bins - 1 - bin;  // larger weight -> smaller rank
     };
-    for (int i = tid; i < n_items; i += kSchedThreads) atomicAdd(&hist[rank_of(i)], 1);
+    const int whole = n_items - split;
+    const int sorted = parts > 1 ? whole : n_items;  // items placed by the sort
+    for (int i = tid; i < sorted; i += kSchedThreads) atomicAdd(&hist[rank_of(i)], 1);
     __syncthreads();
     // exclusive scan of hist over ranks: each thread owns a contiguous run
     const int per = (bins + kSchedThreads - 1) / kSchedThreads;
@@ -275,20 +301,25 @@ __global__ void __launch_bounds__(kSchedThreads)
         pos += hist[i];
     }
     __syncthreads();
-    // entries are item << 2 | units: 0 both; the last `split` positions (the
-    // shortest items) become two entries each, unit 0 only (1) and unit 1
-    // only (2), so the last partial wave spreads over twice the CTAs
-    const int whole = n_items - split;
-    for (int i = tid; i < n_items; i += kSchedThreads) {
+    // entries are item << 5 | key part << 2 | units: 0 both; the `split` tail
+    // items (with parts == 1 the last sorted positions, the shortest items;
+    // else the last items by index) become 2 x parts entries each, unit 0 only
+    // (1) and unit 1 only (2), each in `parts` key-tile ranges, so the last
+    // partial wave spreads over 2 x parts times the CTAs
+    auto put_tail = [&](int ti, int i) {
+        const int q = whole + 2 * parts * ti;
+        for (int uu = 0; uu < 2; ++uu)
+            for (int part = 0; part < parts; ++part)
+                order[q + uu * parts + part] = (i << kEntryItemShift) | (part << 2) | (uu + 1);
+        if (tail_items) tail_items[ti] = i;  // for the merge of its ranges
+    };
+    for (int i = tid; i < sorted; i += kSchedThreads) {
         const int pos = atomicAdd(&cursor[rank_of(i)], 1);
-        if (pos < whole) {
-            order[pos] = i << 2;
-        } else {
-            const int q = whole + 2 * (pos - whole);
-            order[q] = (i << 2) | 1;
-            order[q + 1] = (i << 2) | 2;
-        }
+        if (pos < whole) order[pos] = i << kEntryItemShift;
+        else put_tail(pos - whole, i);
     }
+    if (parts > 1)
+        for (int ti = tid; ti < split; ti += kSchedThreads) put_tail(ti, whole + ti);
     if (tid == 0) {
         *counter = 0;
         steps[0] = 0ull;
@@ -352,6 +383,11 @@ size_t vsa_block_sparse_workspace_size(const vsa_dims *dims) {
     return workspace_bytes_for(dims);
 }
 
+size_t vsa_block_sparse_workspace_size_min(const vsa_dims *dims) {
+    if (check_dims(dims) != VSA_OK) return 0;
+    return base_bytes_for(dims);
+}
+
 vsa_status vsa_block_sparse_fwd(const void *q, const void *k, const void *v, const int32_t *q2k_idx,
                                 const int32_t *q2k_num, const int32_t *block_sizes, void *out, float *lse,
                                 const vsa_dims *dims, void *workspace, size_t workspace_bytes,
@@ -363,9 +399,12 @@ vsa_status vsa_block_sparse_fwd(const void *q, const void *k, const void *v, con
     if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) || !aligned(q2k_num, 4) ||
         !aligned(block_sizes, 4) || (q2k_idx && !aligned(q2k_idx, 4)) || (lse && !aligned(lse, 4)))
         return VSA_ERR_ALIGN;
-    const size_t need = workspace_bytes_for(dims);
+    const size_t need = base_bytes_for(dims);
     if (!workspace || workspace_bytes < need) return VSA_ERR_WORKSPACE;
     if (!aligned(workspace, 16)) return VSA_ERR_ALIGN;
+    // the split tail's partial results need the full size
+    const size_t tail_bytes = tail_bytes_for(dims);
+    const bool tail_room = tail_bytes > 0 && workspace_bytes >= tail_offset_for(dims) + tail_bytes;
     int dev = 0;
     if ((st = current_device(&dev)) != VSA_OK) return st;
     DeviceCache &dc = g_dev[dev];
@@ -419,14 +458,21 @@ vsa_status vsa_block_sparse_fwd(const void *q, const void *k, const void *v, con
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
     // One persistent CTA per SM.  When the last wave would fill at most half
-    // of them, its items are split into one-unit items.
+    // of them, its items are split into one-unit entries, and with 128-token
+    // kernel tiles and room in the workspace each of those into `parts`
+    // key-tile ranges, as many as keep the entries within the grid (a unit's
+    // time then drops to about 1/parts).
     // (kMaxGridCtas bounds the grid for the workspace's per-CTA bitmap regions)
     const int sms = std::min(dc.sm_count.load(std::memory_order_acquire), kMaxGridCtas);
     const int grid = n_items < sms ? n_items : sms;
     const int rem = n_items > grid ? n_items % grid : 0;
-    const int split = (rem > 0 && 2 * rem <= grid && rem <= kMaxSplit) ? rem : 0;
+    const int split = (rem > 0 && 2 * rem <= grid && 2 * rem <= kMaxSplit) ? rem : 0;
+    int parts = 1;
+    if (split > 0 && tail_room && Tk == 128) parts = std::max(1, std::min(kMaxParts, std::min(grid, kMaxSplit) / (2 * split)));
+    char *tail = reinterpret_cast<char *>(workspace) + tail_offset_for(dims);
+    int32_t *tail_items = parts > 1 ? reinterpret_cast<int32_t *>(tail) : nullptr;
     schedule_kernel<<<1, kSchedThreads, 2 * bins * sizeof(int32_t), s>>>(q2k_num, NT, T, dims->max_kv, G, n_items,
-                                                                        bins, split, order, counter,
+                                                                        bins, split, parts, order, counter, tail_items,
                                                                         dc.steps_ptr.load(std::memory_order_acquire));
     if (cudaGetLastError() != cudaSuccess) return VSA_ERR_CUDA;
 
@@ -448,11 +494,31 @@ vsa_status vsa_block_sparse_fwd(const void *q, const void *k, const void *v, con
     p.max_kv = dims->max_kv;
     p.G = G;
     p.bm_words = (NT * sub + 31) / 32;
-    p.n_items = n_items + split;
+    p.n_items = n_items - split + 2 * split * parts;
+    p.n_parts = parts;
+    p.tail_start = n_items - split;
+    p.tail_ml = parts > 1 ? reinterpret_cast<float2 *>(tail + kTailCntBytes) : nullptr;
+    p.tail_o = parts > 1 ? reinterpret_cast<float *>(tail + kTailCntBytes + kTailMlBytes) : nullptr;
     p.Sp = Sp;
     const float scale = dims->scale > 0.f ? dims->scale : 1.0f / std::sqrt((float)D);
     p.scale_log2 = scale * 1.4426950408889634f;
     if (launch_attn(Tk, D, paired, tm_q, tm_k, tm_v, p, grid, s) != cudaSuccess) return VSA_ERR_CUDA;
+    if (parts > 1) {
+        TailMergeParams mq;
+        mq.tail_o = p.tail_o;
+        mq.tail_ml = p.tail_ml;
+        mq.tail_items = tail_items;
+        mq.block_sizes = block_sizes;
+        mq.out = out;
+        mq.lse = lse;
+        mq.units = 2 * split;
+        mq.n_parts = parts;
+        mq.G = G;
+        mq.NT = NT * sub;
+        mq.sub = sub;
+        mq.Sp = Sp;
+        if (launch_tail_merge(D, mq, s) != cudaSuccess) return VSA_ERR_CUDA;
+    }
 
     const AttnLaunchInfo info = attn_launch_info(Tk, D, p.bm_global ? 0 : p.bm_words, paired);
     t_route.kernel = VSA_KERNEL_ATTN_TCGEN05;
@@ -465,6 +531,7 @@ vsa_status vsa_block_sparse_fwd(const void *q, const void *k, const void *v, con
     t_route.sort_bins = bins;
     t_route.smem_bytes = info.smem_bytes;
     t_route.layout = paired ? VSA_LAYOUT_PAIRED : VSA_LAYOUT_SPLIT;
+    t_route.tail_parts = split > 0 ? parts : 0;
     return VSA_OK;
 }
 

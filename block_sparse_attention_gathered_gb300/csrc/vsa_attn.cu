@@ -364,9 +364,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             int slot = 0;
             if (lane == 0) slot = atomicAdd(P.work_counter, 1);
             slot = __shfl_sync(0xffffffffu, slot, 0);
-            // order entries: work item << 2 | which units run (0 both, 1 or 2 one)
+            // order entries: work item << 5 | key part << 2 | which units run
+            // (0 both, 1 or 2 one)
             const int entry = (slot < P.n_items) ? __ldg(P.order + slot) : -1;
-            const int item = entry < 0 ? -1 : entry >> 2, mode = entry < 0 ? 0 : entry & 3;
+            const int item = entry < 0 ? -1 : entry >> kEntryItemShift, mode = entry < 0 ? 0 : entry & 3;
+            // a part of a split tail unit takes the key tiles [k_lo, k_hi) only
+            // (even bounds: a 64-token key-tile pair stays in one part)
+            int piece = -1, k_lo = 0, k_hi = NT;
+            if (entry >= 0 && mode != 0 && P.n_parts > 1) {
+                const int part = (entry >> 2) & 7;
+                piece = slot - P.tail_start;
+                k_lo = (part * NT / P.n_parts) & ~1;
+                k_hi = (part + 1 == P.n_parts) ? NT : ((part + 1) * NT / P.n_parts) & ~1;
+            }
             uint32_t *bmp = bm + p * kItemBitmaps * W;
             int bad = 0;
             uint32_t n_tail = 0, n_full = 0;  // this lane's (query tile, key tile) steps
@@ -397,6 +407,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         }
                         for (int h2 = 0; h2 < sub; ++h2) {
                             const int jj = j * sub + h2;
+                            if (jj < k_lo || jj >= k_hi) continue;  // another part's key tile
                             const int nj = tile_size(P.block_sizes, jj, sub);
                             if (nj <= 0) continue;
                             const uint32_t bit = 1u << (jj & 31);
@@ -415,6 +426,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 if (lane == 0) {
                     hdr[p * 4] = item;
                     hdr[p * 4 + 1] = mode;
+                    hdr[p * 4 + 2] = piece;
                 }
             } else if (lane == 0) {
                 hdr[p * 4] = -1;
@@ -932,6 +944,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             if (!wait_warp(BAR(BI.bm_full(p)), (it >> 1) & 1u, abort_flag, P.status)) break;
             const int item = hdr[p * 4];
             const int mode = hdr[p * 4 + 1];
+            const int piece = hdr[p * 4 + 2];  // >= 0: one key range of a split tail unit
             if (item < 0) break;
             const uint32_t *bmp = bm + p * kItemBitmaps * W;
             const int bh = item / P.G, g = item - (item / P.G) * P.G;
@@ -1122,13 +1135,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             }
             float l = l0 + l1;
             l += __shfl_xor_sync(0xffffffffu, l, 16);
-            // a unit that another CTA runs (a split item) leaves its rows alone
-            const bool write_row = t < NT && (mode == 0 || mode == u + 1);
+            // a unit that another CTA runs (a split item) leaves its rows alone;
+            // one key range of a split tail unit (128-token tiles; the host cuts
+            // no others) leaves unnormalised O, the row maximum and the row sum
+            // in the workspace instead, for tail_merge_kernel
+            const bool piece_row = T == 128 && piece >= 0 && mode == u + 1;
+            const bool write_row = t < NT && (mode == 0 || mode == u + 1) && piece < 0;
             const bool valid = r < n_t;
             const bool use_o = (n_mine > 0) && valid && (l != 0.f);  // NaN l keeps use_o: NaN row
             const float inv = use_o ? 1.f / l : 0.f;
             const int64_t orow = (int64_t)bh * Sp + (int64_t)t * T + r;
             uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(P.out) + orow * D + hf * DH);
+            float4 *po = reinterpret_cast<float4 *>(P.tail_o + ((size_t)(piece_row ? piece : 0) * kUnitRows + row) * D +
+                                                    hf * DH);
 #pragma unroll
             for (int ch = 0; ch < DH / 16; ++ch) {
                 float o[16];
@@ -1138,7 +1157,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
                     for (int i = 0; i < 16; ++i) o[i] = 0.f;
                 }
-                if (write_row) {
+                if (piece_row) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        po[ch * 4 + i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+                } else if (write_row) {
                     uint32_t wv[8];
 #pragma unroll
                     for (int i = 0; i < 8; ++i) wv[i] = use_o ? pack_bf16x2(o[2 * i] * inv, o[2 * i + 1] * inv) : 0u;
@@ -1146,6 +1169,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     dst[2 * ch + 1] = make_uint4(wv[4], wv[5], wv[6], wv[7]);
                 }
             }
+            if (piece_row && hf == 0)
+                P.tail_ml[(size_t)piece * kUnitRows + row] =
+                    make_float2(n_mine > 0 ? m : -INFINITY, n_mine > 0 ? l : 0.f);
             if (P.lse && write_row && hf == 0) {
                 float v = -INFINITY;
                 if (use_o) v = (m + lg2(l)) * 0.69314718055994531f;
@@ -1160,6 +1186,82 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     __syncthreads();
     tc_fence_after();
     if (warp == kSWarp) tmem_dealloc(tmem, C::kTmemCols);
+}
+
+// ------------------------------------------------------------------ split tail merge
+// Merges the key ranges of each split tail unit (128-token kernel tiles) into
+// the output: for a query row with ranges r = 0 .. np-1 (unnormalised O_r,
+// row maximum m_r in log2 units, row sum l_r)
+//   M = max m_r,  w_r = 2^(m_r - M),  L = sum w_r l_r,  O = sum w_r O_r / L,
+//   LSE = (M + log2 L) ln 2,
+// summed in range order, with the rules of the attention kernel's epilogue: a
+// row past the valid rows or with L == 0 is +0 and its LSE -inf (no range
+// selected a key tile: M = -inf, L = 0); a NaN L gives a NaN row.  One thread
+// per (unit, row, 16 columns).
+constexpr int kMergeThreads = 256;
+
+template <int D>
+__global__ void __launch_bounds__(kMergeThreads) tail_merge_kernel(TailMergeParams q) {
+    constexpr int kChunks = D / 16;
+    const int64_t gid = (int64_t)blockIdx.x * kMergeThreads + threadIdx.x;
+    if (gid >= (int64_t)q.units * kUnitRows * kChunks) return;
+    const int ch = (int)(gid % kChunks);
+    const int row = (int)((gid / kChunks) % kUnitRows);
+    const int unit = (int)(gid / ((int64_t)kChunks * kUnitRows));
+    const int item = q.tail_items[unit >> 1];
+    const int bh = item / q.G, g = item - (item / q.G) * q.G;
+    const int t = 2 * g + (unit & 1);  // the unit's 128-row kernel tile
+    if (t >= q.NT) return;
+    const bool valid = row < tile_size(q.block_sizes, t, q.sub);
+    const int np = q.n_parts;
+    const size_t b0 = (size_t)unit * np * kUnitRows + row;  // range r's row: b0 + r * kUnitRows
+    float mr[kMaxParts], wr[kMaxParts];
+#pragma unroll
+    for (int r = 0; r < kMaxParts; ++r) {
+        mr[r] = -INFINITY;
+        wr[r] = 0.f;
+        if (r < np) {
+            const float2 ml = __ldcg(q.tail_ml + b0 + (size_t)r * kUnitRows);
+            mr[r] = ml.x;
+            wr[r] = ml.y;
+        }
+    }
+    float M = -INFINITY;
+#pragma unroll
+    for (int r = 0; r < kMaxParts; ++r) M = fmaxf(M, mr[r]);
+    float L = 0.f;
+#pragma unroll
+    for (int r = 0; r < kMaxParts; ++r) {
+        const float w = (M != -INFINITY && mr[r] != -INFINITY) ? ex2(mr[r] - M) : 0.f;
+        L += w * wr[r];
+        wr[r] = w;
+    }
+    const bool use = valid && (L != 0.f);  // NaN L keeps it: NaN row
+    const float inv = use ? 1.f / L : 0.f;
+    float acc[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+#pragma unroll
+    for (int r = 0; r < kMaxParts; ++r) {
+        if (r >= np) break;
+        const float4 *src = reinterpret_cast<const float4 *>(q.tail_o + (b0 + (size_t)r * kUnitRows) * D) + ch * 4;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float4 x = __ldcg(src + i);
+            acc[4 * i] += wr[r] * x.x;
+            acc[4 * i + 1] += wr[r] * x.y;
+            acc[4 * i + 2] += wr[r] * x.z;
+            acc[4 * i + 3] += wr[r] * x.w;
+        }
+    }
+    const int64_t orow = (int64_t)bh * q.Sp + (int64_t)t * kUnitRows + row;
+    uint32_t wv[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) wv[i] = use ? pack_bf16x2(acc[2 * i] * inv, acc[2 * i + 1] * inv) : 0u;
+    uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(q.out) + orow * D) + ch * 2;
+    dst[0] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+    dst[1] = make_uint4(wv[4], wv[5], wv[6], wv[7]);
+    if (q.lse && ch == 0) q.lse[orow] = use ? (M + lg2(L)) * 0.69314718055994531f : -INFINITY;
 }
 
 // The dense form (kPaired) runs with the selection bitmaps in shared memory
@@ -1232,6 +1334,14 @@ cudaError_t launch_attn(int tile, int head_dim, bool paired, const CUtensorMap &
     if (tile == 128 && head_dim == 64) return launch_t<128, 64>(q, k, v, p, paired, grid, stream);
     if (tile == 64 && head_dim == 128) return launch_t<64, 128>(q, k, v, p, paired, grid, stream);
     return launch_t<64, 64>(q, k, v, p, paired, grid, stream);
+}
+
+cudaError_t launch_tail_merge(int head_dim, const TailMergeParams &q, cudaStream_t stream) {
+    const int64_t threads = (int64_t)q.units * kUnitRows * (head_dim / 16);
+    const unsigned blocks = (unsigned)((threads + kMergeThreads - 1) / kMergeThreads);
+    if (head_dim == 128) tail_merge_kernel<128><<<blocks, kMergeThreads, 0, stream>>>(q);
+    else tail_merge_kernel<64><<<blocks, kMergeThreads, 0, stream>>>(q);
+    return cudaGetLastError();
 }
 
 }  // namespace vsa

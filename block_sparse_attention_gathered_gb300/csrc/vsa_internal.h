@@ -22,6 +22,15 @@ constexpr int kSmemBitmapTiles = 8192;  // VSA_SMEM_BITMAP_TILES
 // only for those.
 constexpr int kItemBitmaps = 5;
 constexpr int kMaxGridCtas = 1024;      // bound on the attention grid (one CTA per SM), for workspace sizing
+// Split tail: the work items of a last wave that fills at most half of the
+// CTAs run as one-unit entries, and each of those can be cut further into up
+// to kMaxParts parts by key-tile range (at most kMaxSplit entries in all).
+// Each part leaves its unit's unnormalised O with the row maximum and row sum
+// in the workspace; tail_merge_kernel then merges them into the output.
+constexpr int kMaxSplit = 256;
+constexpr int kMaxParts = 8;
+// Order-list entries: work item << 5 | key part << 2 | units (0 both, 1 or 2 one).
+constexpr int kEntryItemShift = 5;
 
 struct AttnParams {
     const int32_t *q2k_idx;      // [B*H*NT, max_kv]
@@ -44,7 +53,30 @@ struct AttnParams {
     int32_t stages;              // K/V ring depth (set by launch_attn)
     int64_t Sp;                  // NT * tile
     float scale_log2;            // softmax scale * log2(e)
+    // split tail cut by key range (n_parts > 1 only): order slots from
+    // tail_start on are the parts, unit by unit (piece = slot - tail_start,
+    // its unit piece / n_parts)
+    int32_t n_parts;
+    int32_t tail_start;
+    float *tail_o;               // [kMaxSplit pieces][kUnitRows][D] unnormalised O
+    float2 *tail_ml;             // [kMaxSplit pieces][kUnitRows] (row maximum in log2 units, row sum)
 };
+
+// The split tail's merge (after the attention kernel, same stream): unit
+// 2 ti + uu is unit uu of work item tail_items[ti]; its ranges are pieces
+// unit * n_parts .. + n_parts - 1 of tail_o / tail_ml.
+struct TailMergeParams {
+    const float *tail_o;
+    const float2 *tail_ml;
+    const int32_t *tail_items;   // [units / 2] work item of each split tail item
+    const int32_t *block_sizes;
+    void *out;                   // bf16 [B*H*Sp, D]
+    float *lse;                  // or nullptr
+    int32_t units, n_parts, G, NT, sub;
+    int64_t Sp;
+};
+
+cudaError_t launch_tail_merge(int head_dim, const TailMergeParams &q, cudaStream_t stream);
 
 struct AttnLaunchInfo {
     int stages;

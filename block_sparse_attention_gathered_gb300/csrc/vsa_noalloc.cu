@@ -79,7 +79,7 @@ extern "C" vsa_status vsa_block_sparse_fwd_noalloc(const void *q, const void *k,
                                                    const int32_t *q2k_idx, const int32_t *q2k_num,
                                                    const int32_t *block_sizes, void *out, float *lse,
                                                    const vsa_dims *dims, vsa_stream_t stream) {
-    const size_t need = vsa_block_sparse_workspace_size(dims);
+    const size_t need = vsa_block_sparse_workspace_size_min(dims);
     if (need == 0)  // invalid dims: report the same error the main entry point gives
         return vsa_block_sparse_fwd(q, k, v, q2k_idx, q2k_num, block_sizes, out, lse, dims, nullptr, 0, stream);
     if (need > (size_t)VSA_NOALLOC_SCRATCH_BYTES) return VSA_ERR_LIMITS;

@@ -94,7 +94,8 @@ typedef struct {
     int32_t smem_bytes;   /* dynamic shared memory per CTA */
     int32_t layout;       /* VSA_LAYOUT_*: the attention kernel's form, sparse or dense
                              (results agree within the stated tolerance) */
-    int32_t reserved;
+    int32_t tail_parts;   /* 0: no split tail; else the key-tile ranges each one-unit
+                             entry of the split last wave was cut into (1: not cut) */
 } vsa_route;
 
 /* Attention kernel forms (vsa_route.layout).  SPLIT, the sparse form: one
@@ -119,9 +120,25 @@ typedef struct {
 #define VSA_KERNEL_UNTILE 5
 #define VSA_KERNEL_BWD 6
 
-/* Bytes of workspace vsa_block_sparse_fwd needs for `dims` (the on-device work
- * order and its counter).  Returns 0 when `dims` is invalid. */
+/* Bytes of workspace vsa_block_sparse_fwd should get for `dims`: the
+ * on-device work order and its counter, the selection bitmaps beyond
+ * VSA_SMEM_BITMAP_TILES kernel tiles, and, beyond 128 work items of 256 query
+ * rows, room for the split tail's partial results (256 x 128 rows of fp32 O
+ * plus row maximum and sum, about 17 MB at head_dim 128).  Returns 0 when
+ * `dims` is invalid.
+ *
+ * Split tail: when the last wave of work items would fill at most half of the
+ * SMs, each of its items runs as two one-unit (128-row) entries, and with
+ * 128-token kernel tiles each of those is cut into up to 8 ranges of key
+ * tiles on separate SMs; every range leaves its unnormalised O, row maximum
+ * and row sum in the workspace, and a small merge kernel on the same stream
+ * combines them in a fixed order, so results stay deterministic. */
 size_t vsa_block_sparse_workspace_size(const vsa_dims *dims);
+
+/* The least workspace vsa_block_sparse_fwd accepts for `dims` (no room for
+ * the split tail's partial results: the last wave then runs its one-unit
+ * entries whole).  Returns 0 when `dims` is invalid. */
+size_t vsa_block_sparse_workspace_size_min(const vsa_dims *dims);
 
 /*
  * Block-sparse attention forward (commit adding the sm_121a tile-128
@@ -139,7 +156,8 @@ size_t vsa_block_sparse_workspace_size(const vsa_dims *dims);
  *                gives a NaN row; padding rows r >= n_t are written as +0.
  *   lse          NULL, or fp32 [B, H, NT*tile]: natural-log log-sum-exp of the
  *                scaled scores per row; -inf for padding rows and empty rows.
- *   workspace    device scratch of vsa_block_sparse_workspace_size(dims) bytes,
+ *   workspace    device scratch of vsa_block_sparse_workspace_size(dims) bytes
+ *                (at least vsa_block_sparse_workspace_size_min(dims)),
  *                16-byte aligned; contents need not be initialised; must not
  *                be used by another call that runs concurrently.
  *
@@ -169,10 +187,12 @@ vsa_status vsa_block_sparse_fwd(const void *q, const void *k, const void *v, con
  *
  *   - Problems needing more scratch than the array holds return
  *     VSA_ERR_LIMITS before anything is launched.  The scratch of a problem is
- *     vsa_block_sparse_workspace_size(): a 256-byte header plus 4 bytes per
- *     work item (256 query rows of one (batch, head)) and 4 bytes for each of
- *     up to 256 split entries, so at most
+ *     vsa_block_sparse_workspace_size_min(): a 256-byte header plus 4 bytes
+ *     per work item (256 query rows of one (batch, head)) and 4 bytes for each
+ *     of up to 256 split entries, so at most
  *     (VSA_NOALLOC_SCRATCH_BYTES - 256) / 4 - 256 = 261,824 work items fit.
+ *     The array has no room for the split tail's partial results, so a last
+ *     wave runs its one-unit entries whole.
  *   - The first call on a device looks up the array's device address; make
  *     that first call before any stream capture on the device.  The address
  *     belongs to the device's current context: after cudaDeviceReset (a new

@@ -280,10 +280,14 @@ def test_many_waves(vsa, oracle_mod):
 @pytest.mark.parametrize("form", ["sparse", "dense"])
 def test_split_last_wave(vsa, oracle_mod, T, form):
     """One work item per SM plus a few: the last wave's items run as one-unit
-    items on two CTAs each, and each CTA writes only its unit's rows.  Both
-    forms: short rows of q2k_idx (sparse) and rows that hold every key tile
-    at D = 128 (dense: the paired MMA issue at 128- and 256-token tiles,
-    key-tile pairs at 64)."""
+    entries, and each CTA writes only its unit's rows.  With 128-token kernel
+    tiles each unit is also cut into key-tile ranges on separate CTAs: every
+    range leaves its partial O, row maximum and row sum in the workspace and
+    the last one merges them (ranges with no selected key tile included, as
+    the sparse case's three-tile rows leave most ranges empty).  Both forms:
+    short rows of q2k_idx (sparse) and rows that hold every key tile at
+    D = 128 (dense: the paired MMA issue at 128- and 256-token tiles, key-tile
+    pairs at 64)."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     n_items = sms + 5
     NT = n_items * 256 // T
@@ -296,12 +300,27 @@ def test_split_last_wave(vsa, oracle_mod, T, form):
     r = vsa.vsa_last_route()
     assert r["work_items"] == n_items
     assert r["layout"] == (vsa.VSA_LAYOUT_PAIRED if form == "dense" else vsa.VSA_LAYOUT_SPLIT)
+    # 128-token kernel tiles: each one-unit entry is cut into key-tile ranges
+    # (as many as keep the 2 x 5 units' ranges within the grid, at most 8)
+    assert r["tail_parts"] == (1 if T == 64 else min(8, min(sms, 256) // 10))
     _check(w, out, lse, refs, oracle_mod, list(range(w.B * w.H * w.NT)), f"split T{T} {form}")
-    _check_steps(vsa, w)   # split items count their unit once, on the CTA that runs it
+    _check_steps(vsa, w)   # split items count each (query tile, key tile) step once
     # bit-identical across runs, although which items are split may differ
     # (items of equal length take their places in any order)
     again, _ = _run(vsa, q, k, v, w)
     assert torch.equal(out.view(torch.int16), again.view(torch.int16))
+    # the least workspace has no room for the ranges' partial results: the
+    # one-unit entries then run whole, against the same oracle
+    dims = vsa.make_dims(w.B, w.H, w.NT, w.T, w.D, w.q2k_idx.shape[-1], w.scale)
+    ws = torch.empty(vsa.vsa_block_sparse_workspace_size_min(dims), dtype=torch.uint8, device="cuda")
+    whole = torch.full_like(q, float("nan"))
+    whole_lse = torch.full(lse.shape, float("nan"), dtype=torch.float32, device="cuda")
+    vsa.vsa_block_sparse_fwd(q, k, v, w.q2k_idx.cuda(), w.q2k_num.cuda(), w.block_sizes.cuda(), whole, whole_lse,
+                             dims, ws)
+    torch.cuda.synchronize()
+    assert vsa.vsa_check_device_status() == 0
+    assert vsa.vsa_last_route()["tail_parts"] == 1
+    _check(w, whole, whole_lse, refs, oracle_mod, list(range(w.B * w.H * w.NT)), f"split T{T} {form} whole units")
 
 
 @pytest.mark.parametrize("T", [64, 128])

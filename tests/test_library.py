@@ -106,6 +106,15 @@ def test_tile_256_limits(vsa):
     assert vsa.vsa_coarse_select_workspace_size(vsa.make_dims(1, 1, 8193, 64, 64, 2)) == 0
 
 
+def _with_tail(base, items, D):
+    """The full forward workspace: beyond 128 work items, the split tail's
+    region after the base (256-byte aligned): 256 work-item slots, 256 pieces
+    of 128 (row maximum, row sum) pairs, 256 pieces of 128 fp32 O rows."""
+    if items <= 128:
+        return base
+    return (base + 255) // 256 * 256 + 256 * 4 + 256 * 128 * 8 + 256 * 128 * D * 4
+
+
 def test_bitmap_workspace_beyond_shared_memory(vsa):
     # up to 8192 kernel tiles the selection bitmaps live in shared memory and
     # the workspace is the header plus the order list; beyond, each CTA (at
@@ -113,27 +122,39 @@ def test_bitmap_workspace_beyond_shared_memory(vsa):
     # (two buffers of the four slot bitmaps and the partial-tile bitmap)
     small = vsa.make_dims(1, 1, 8192, 64, 64, 2)
     items = 8192 * 64 // 256
-    assert vsa.vsa_block_sparse_workspace_size(small) == 256 + 4 * (items + 256)
+    assert vsa.vsa_block_sparse_workspace_size_min(small) == 256 + 4 * (items + 256)
+    assert vsa.vsa_block_sparse_workspace_size(small) == _with_tail(256 + 4 * (items + 256), items, 64)
     big = vsa.make_dims(1, 1, 8200, 64, 64, 2)
     items = 8200 * 64 // 256
     order = 256 + 4 * (items + 256)
     words = (8200 + 31) // 32
-    assert vsa.vsa_block_sparse_workspace_size(big) == ((order + 255) // 256) * 256 + 1024 * 2 * 5 * words * 4
+    base = ((order + 255) // 256) * 256 + 1024 * 2 * 5 * words * 4
+    assert vsa.vsa_block_sparse_workspace_size_min(big) == base
+    assert vsa.vsa_block_sparse_workspace_size(big) == _with_tail(base, items, 64)
     few = vsa.make_dims(1, 1, 8200, 256, 64, 2)  # 16400 kernel tiles, 8200 work items
     words = (16400 + 31) // 32
     order = 256 + 4 * (8200 + 256)
-    assert vsa.vsa_block_sparse_workspace_size(few) == ((order + 255) // 256) * 256 + 1024 * 2 * 5 * words * 4
+    base = ((order + 255) // 256) * 256 + 1024 * 2 * 5 * words * 4
+    assert vsa.vsa_block_sparse_workspace_size_min(few) == base
+    assert vsa.vsa_block_sparse_workspace_size(few) == _with_tail(base, 8200, 64)
     # one 256-row work item per 256-token tile
     assert vsa.vsa_block_sparse_workspace_size(vsa.make_dims(2, 3, 10, 256, 64, 4)) == 256 + 4 * (6 * 10 + 256)
 
 
 def test_workspace_size(vsa):
     # header (256 bytes) + one int32 per 256-query-row work item, + 256 for
-    # items of a partial last wave split into one-unit items
+    # the entries of a partial last wave split into one-unit entries; beyond
+    # 128 work items, the split tail's partial results
     d = vsa.make_dims(1, 6, 244, 128, 128, 244)
-    assert vsa.vsa_block_sparse_workspace_size(d) == 256 + 4 * (6 * 122 + 256)
+    assert vsa.vsa_block_sparse_workspace_size_min(d) == 256 + 4 * (6 * 122 + 256)
+    assert vsa.vsa_block_sparse_workspace_size(d) == _with_tail(256 + 4 * (6 * 122 + 256), 6 * 122, 128)
+    assert vsa.vsa_block_sparse_workspace_size(d) - vsa.vsa_block_sparse_workspace_size_min(d) < 18 << 20
     d = vsa.make_dims(2, 8, 63, 64, 64, 31)
-    assert vsa.vsa_block_sparse_workspace_size(d) == 256 + 4 * (16 * 16 + 256)
+    assert vsa.vsa_block_sparse_workspace_size(d) == _with_tail(256 + 4 * (16 * 16 + 256), 16 * 16, 64)
+    d = vsa.make_dims(1, 2, 10, 128, 64, 4)   # 10 work items: no split tail region
+    assert vsa.vsa_block_sparse_workspace_size(d) == 256 + 4 * (10 + 256)
+    assert vsa.vsa_block_sparse_workspace_size_min(d) == vsa.vsa_block_sparse_workspace_size(d)
+    assert vsa.vsa_block_sparse_workspace_size_min(vsa.make_dims(256, 256, 4, 64, 64, 2)) == 0
 
 
 def _align256(x):

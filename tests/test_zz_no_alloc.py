@@ -35,7 +35,7 @@ def test_oversized_problem_is_refused_before_launch(vsa):
     # 1 MiB scratch; the check happens before any device call, so the fake
     # pointers below are never touched.
     d = vsa.make_dims(1, 2048, 8192, 64, 64, 4)
-    assert vsa.vsa_block_sparse_workspace_size(d) > vsa.VSA_NOALLOC_SCRATCH_BYTES
+    assert vsa.vsa_block_sparse_workspace_size_min(d) > vsa.VSA_NOALLOC_SCRATCH_BYTES
     P = ctypes.c_void_p
     fake = P(0x100000)
     st = vsa.library().vsa_block_sparse_fwd_noalloc(fake, fake, fake, fake, fake, fake, fake, None,
@@ -49,13 +49,15 @@ def test_oversized_problem_is_refused_before_launch(vsa):
 
 
 def test_noalloc_limit_at_boundary(vsa):
-    """The scratch of a problem is a 256-byte header plus 4 bytes per work item
-    and per possible split entry (256 of them): exactly 1 MiB holds 261,824
-    work items; one more is refused before anything reaches the device."""
+    """The scratch of a problem is its least forward workspace: a 256-byte
+    header plus 4 bytes per work item and per possible split entry (256 of
+    them): exactly 1 MiB holds 261,824 work items; one more is refused before
+    anything reaches the device.  (The split tail's partial results do not
+    fit: a last wave then runs its one-unit entries whole.)"""
     fit = vsa.make_dims(1, 64, 8182, 128, 64, 1)      # 64 heads x 4091 items = 261,824
     over = vsa.make_dims(1, 75, 6982, 128, 64, 1)     # 75 heads x 3491 items = 261,825
-    assert vsa.vsa_block_sparse_workspace_size(fit) == vsa.VSA_NOALLOC_SCRATCH_BYTES
-    assert vsa.vsa_block_sparse_workspace_size(over) == vsa.VSA_NOALLOC_SCRATCH_BYTES + 4
+    assert vsa.vsa_block_sparse_workspace_size_min(fit) == vsa.VSA_NOALLOC_SCRATCH_BYTES
+    assert vsa.vsa_block_sparse_workspace_size_min(over) == vsa.VSA_NOALLOC_SCRATCH_BYTES + 4
     assert (vsa.VSA_NOALLOC_SCRATCH_BYTES - 256) // 4 - 256 == 261824
     fake = ctypes.c_void_p(0x100000)
     st = vsa.library().vsa_block_sparse_fwd_noalloc(fake, fake, fake, fake, fake, fake, fake, None,
