@@ -50,8 +50,10 @@ FALLBACK_HBM_GBS = 6800.0
 # hash of the attention kernel code the capture was taken with
 # (_attn_source_hash); a changed kernel reports null until it is captured again.
 ATTN_TRAFFIC = {
-    ("dense_b1h6d128_s31200_t128x244_lse", "89a00684306c1328"): 254.28e6,  # 220.6 MB read + 33.7 MB written
-    ("uniform_b1h12d128_t128x128_k32", "89a00684306c1328"): 207.98e6,      # 173.5 MB read + 34.5 MB written
+    ("dense_b1h6d128_s31200_t128x244_lse", "bed0972dfe06b682"): 254.28e6,  # 220.6 MB read + 33.7 MB written
+    ("uniform_b1h12d128_t128x128_k32", "bed0972dfe06b682"): 207.98e6,      # 173.5 MB read + 34.5 MB written
+    # (both captured at 89a00684306c1328; the one later change compiles the split
+    # tail's range code out of the 64-token kernels only)
 }
 
 # Workloads timed after the headline step in the default run (attention, and

@@ -369,9 +369,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             const int entry = (slot < P.n_items) ? __ldg(P.order + slot) : -1;
             const int item = entry < 0 ? -1 : entry >> kEntryItemShift, mode = entry < 0 ? 0 : entry & 3;
             // a part of a split tail unit takes the key tiles [k_lo, k_hi) only
-            // (even bounds: a 64-token key-tile pair stays in one part)
+            // (even bounds: a 64-token key-tile pair stays in one part; the
+            // host cuts units of 128-token kernel tiles only)
             int piece = -1, k_lo = 0, k_hi = NT;
-            if (entry >= 0 && mode != 0 && P.n_parts > 1) {
+            if (T == 128 && entry >= 0 && mode != 0 && P.n_parts > 1) {
                 const int part = (entry >> 2) & 7;
                 piece = slot - P.tail_start;
                 k_lo = (part * NT / P.n_parts) & ~1;
@@ -407,7 +408,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         }
                         for (int h2 = 0; h2 < sub; ++h2) {
                             const int jj = j * sub + h2;
-                            if (jj < k_lo || jj >= k_hi) continue;  // another part's key tile
+                            if (T == 128 && (jj < k_lo || jj >= k_hi)) continue;  // another part's key tile
                             const int nj = tile_size(P.block_sizes, jj, sub);
                             if (nj <= 0) continue;
                             const uint32_t bit = 1u << (jj & 31);
@@ -944,7 +945,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             if (!wait_warp(BAR(BI.bm_full(p)), (it >> 1) & 1u, abort_flag, P.status)) break;
             const int item = hdr[p * 4];
             const int mode = hdr[p * 4 + 1];
-            const int piece = hdr[p * 4 + 2];  // >= 0: one key range of a split tail unit
+            const int piece = (T == 128) ? hdr[p * 4 + 2] : -1;  // >= 0: one key range of a split tail unit
             if (item < 0) break;
             const uint32_t *bmp = bm + p * kItemBitmaps * W;
             const int bh = item / P.G, g = item - (item / P.G) * P.G;
